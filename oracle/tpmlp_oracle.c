@@ -1,0 +1,148 @@
+/*
+ * CPU oracle for the tensor-parallel MLP block -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+ * load this code. It shares nothing with the CUDA library: plain fp64 loops on
+ * bf16 inputs widened exactly to double, no blocking, no fusion, no reordering of
+ * any sum beyond what the definition below states.
+ *
+ * What it computes (the block as the pages define it):
+ *
+ *   Column-parallel first layer: W1 [H, F] is split by columns into k equal,
+ *   contiguous shards W1_i = W1[:, i*f:(i+1)*f], f = F/k; every shard sees the
+ *   same X and produces Y_i = X W1_i, and concatenating the Y_i gives X W1.
+ *   (千亿参数模型如何拆分到多张GPU上训练, "方案一：按列切分权重矩阵";
+ *    大模型分布式并行策略详解 §4.1; AI大模型分布式训练 §2.1 ColumnParallelLinear,
+ *    whose bias is sliced with the output columns.)
+ *
+ *   GeLU is applied to each shard's output on its own, with no exchange before
+ *   it, because it acts element by element (same section of the first page).
+ *   Reading: the exact form GeLU(a) = a * Phi(a) = a/2 * (1 + erf(a / sqrt 2)).
+ *
+ *   Row-parallel second layer: W2 [F, H] is split by rows into the matching
+ *   shards W2_i = W2[i*f:(i+1)*f, :]; shard i forms the partial Z_i = Y_i W2_i and
+ *   the block output is the sum Z = sum_i Z_i, which the pages obtain with one
+ *   All-Reduce (千亿参数模型…, "方案二：按行切分权重矩阵", Z = Y1 V1 + Y2 V2;
+ *   大模型分布式并行策略详解 §4.1; AI大模型分布式训练 §2.2 RowParallelLinear).
+ *
+ *   Reading for the output bias: b2 is added once, after the sum over shards.
+ *
+ *   Z[m, n] = b2[n] + sum_{i=0}^{k-1} sum_{j=i f}^{(i+1) f - 1}
+ *                 GeLU(b1[j] + sum_h X[m, h] W1[h, j]) * W2[j, n]
+ *
+ * Sums run in index order: over h for each pre-activation, over j inside a shard
+ * for each partial, then over shards i = 0..k-1 (the "all-reduce"), then + b2.
+ * Rows of X are independent, so any subset of rows is evaluated exactly.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 -> double, exact: a bf16 is the upper 16 bits of an IEEE fp32. */
+static double widen_bf16(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* GeLU(a) = a * Phi(a), Phi the standard normal CDF = (1 + erf(a / sqrt(2))) / 2. */
+double oracle_gelu(double a) { return 0.5 * a * (1.0 + erf(a / sqrt(2.0))); }
+
+#define ORACLE_ACT_GELU 0
+#define ORACLE_ACT_IDENTITY 1 /* test-only: drops the nonlinearity so the block is two plain products */
+
+/*
+ * Evaluate the block for R token rows.
+ *   X        bf16 [x_rows][H]; rows[r] (or r if rows == NULL) selects the row of X
+ *   W1       bf16 [H][F] (math orientation: Y = X W1), b1 bf16 [F]
+ *   W2       bf16 [F][H], b2 bf16 [H]
+ *   k        shard count, F % k == 0
+ *   act      ORACLE_ACT_GELU or ORACLE_ACT_IDENTITY
+ *   Z        out, double [R][H]
+ *   Y        out or NULL, double [R][F]: the concatenated shard activations
+ *   P        out or NULL, double [R][k][H]: each shard's partial Z_i (before the sum)
+ * Returns 0, or -1 on bad arguments / allocation failure.
+ */
+int oracle_tpmlp_f64(const uint16_t *X, int64_t x_rows, const int64_t *rows, int64_t R,
+                     const uint16_t *W1, const uint16_t *b1, const uint16_t *W2,
+                     const uint16_t *b2, int64_t H, int64_t F, int32_t k, int32_t act,
+                     double *Z, double *Y, double *P) {
+    if (!X || !W1 || !b1 || !W2 || !b2 || !Z || H <= 0 || F <= 0 || k <= 0 || R < 0) return -1;
+    if (F % k != 0) return -1;
+    if (act != ORACLE_ACT_GELU && act != ORACLE_ACT_IDENTITY) return -1;
+    const int64_t f = F / k;
+    int failed = 0;
+
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc(sizeof(double) * (size_t)f);
+        double *part = (double *)malloc(sizeof(double) * (size_t)H);
+        double *zsum = (double *)malloc(sizeof(double) * (size_t)H);
+        if (!acc || !part || !zsum) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < R; ++r) {
+                const int64_t m = rows ? rows[r] : r;
+                if (m < 0 || m >= x_rows) {
+#pragma omp atomic write
+                    failed = 1;
+                    continue;
+                }
+                const uint16_t *x = X + m * H;
+                for (int64_t n = 0; n < H; ++n) zsum[n] = 0.0;
+
+                for (int32_t i = 0; i < k; ++i) {
+                    const int64_t j0 = (int64_t)i * f; /* first column of shard i */
+
+                    /* Column shard i: acc[jj] = sum_h X[m,h] * W1[h, j0+jj] */
+                    for (int64_t jj = 0; jj < f; ++jj) acc[jj] = 0.0;
+                    for (int64_t h = 0; h < H; ++h) {
+                        const double xh = widen_bf16(x[h]);
+                        const uint16_t *w = W1 + h * F + j0;
+                        for (int64_t jj = 0; jj < f; ++jj) acc[jj] += xh * widen_bf16(w[jj]);
+                    }
+                    /* + b1 slice, then the activation, element by element */
+                    for (int64_t jj = 0; jj < f; ++jj) {
+                        const double a = acc[jj] + widen_bf16(b1[j0 + jj]);
+                        acc[jj] = (act == ORACLE_ACT_GELU) ? oracle_gelu(a) : a;
+                        if (Y) Y[r * F + j0 + jj] = acc[jj];
+                    }
+
+                    /* Row shard i: part[n] = sum_{jj} Y_i[jj] * W2[j0+jj, n] */
+                    for (int64_t n = 0; n < H; ++n) part[n] = 0.0;
+                    for (int64_t jj = 0; jj < f; ++jj) {
+                        const double y = acc[jj];
+                        const uint16_t *w = W2 + (j0 + jj) * H;
+                        for (int64_t n = 0; n < H; ++n) part[n] += y * widen_bf16(w[n]);
+                    }
+                    if (P)
+                        for (int64_t n = 0; n < H; ++n) P[(r * k + i) * H + n] = part[n];
+
+                    /* The all-reduce: sum of the shards' partials, in shard order */
+                    for (int64_t n = 0; n < H; ++n) zsum[n] += part[n];
+                }
+                /* Output bias, once, after the sum */
+                for (int64_t n = 0; n < H; ++n) Z[r * H + n] = zsum[n] + widen_bf16(b2[n]);
+            }
+        }
+        free(acc);
+        free(part);
+        free(zsum);
+    }
+    return failed ? -1 : 0;
+}
+
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,200 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics fix,
+never against the oracle itself re-typed. Each ``pin_*`` takes an ``oracle.Oracle``
+and raises AssertionError on a mismatch, so the same pins run against the real
+oracle (test_oracle.py) and against copies with a planted mistake
+(test_oracle_mutants.py).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+import sys
+
+import numpy as np
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as fh:
+        return json.load(fh)
+
+
+def _bits(values) -> np.ndarray:
+    """Exact bf16 bit patterns of dyadic test values (asserts exactness)."""
+    a = np.asarray(values, dtype=np.float64)
+    b = synth.round_bf16(a)
+    assert np.array_equal(synth.bf16_to_f64(b), a), "test value not exact in bf16"
+    return b
+
+
+def _rel_fro(a, b) -> float:
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+def _small(seed=7, H=64, F=256, M=37):
+    d = synth.make_inputs(H, F, M, seed)
+    f64 = {k: synth.bf16_to_f64(v) for k, v in d.items()}
+    return d, f64
+
+
+# ---------------------------------------------------------------------------------
+def pin_gelu_table(orc):
+    """GeLU(a) = a * Phi(a) against textbook values of the normal CDF."""
+    t = _load("normal_cdf_table.json")
+    for a_s, phi in t["phi"].items():
+        a = float(a_s)
+        got = orc.gelu(a)
+        want = a * phi
+        assert abs(got - want) <= 2e-16 * max(1.0, abs(want)) + 1e-18, (a, got, want)
+    # the tanh form would give a value 1.5e-4 away at a = 1
+    assert abs(orc.gelu(1.0) - t["tanh_approximation_at_1"]) > 1e-4
+
+
+def pin_gelu_ndtr(orc):
+    """GeLU(a) = a * ndtr(a): scipy's normal CDF is a different routine (erfc based)."""
+    from scipy.special import ndtr
+    for a in np.linspace(-8.0, 8.0, 1601):
+        got = orc.gelu(float(a))
+        want = float(a * ndtr(a))
+        assert abs(got - want) <= 4e-16 * max(1.0, abs(a)), (a, got, want)
+
+
+def pin_gelu_odd_part(orc):
+    """Phi(a) + Phi(-a) = 1  =>  GeLU(a) - GeLU(-a) = a."""
+    for a in np.linspace(0.0, 6.0, 601):
+        d = orc.gelu(float(a)) - orc.gelu(float(-a))
+        assert abs(d - a) <= 4e-16 * max(1.0, a), (a, d)
+
+
+def pin_bruteforce_golden(orc):
+    """The hand-summed H=2, F=8, k=2 case (tests/golden/bruteforce_h2_f8_k2.json)."""
+    g = _load("bruteforce_h2_f8_k2.json")
+    phi = {float(a): p for a, p in _load("normal_cdf_table.json")["phi"].items()}
+
+    def gel(a):
+        return a * phi[a]
+
+    X, W1, b1 = _bits(g["X"]), _bits(g["W1"]), _bits(g["b1"])
+    W2, b2 = _bits(g["W2"]), _bits(g["b2"])
+    r = orc.tpmlp(X, W1, b1, W2, b2, g["k"], want_y=True, want_partials=True)
+    pre = g["pre_activation_by_hand"]
+    for j, a in enumerate(pre):
+        assert abs(r["Y"][0, j] - gel(a)) <= 1e-15, (j, r["Y"][0, j], gel(a))
+    for n, coeff in enumerate(g["Z_coefficients"]):
+        want = coeff["bias"] + sum(c * gel(float(a)) for a, c in coeff.items() if a != "bias")
+        assert abs(r["Z"][0, n] - want) <= 1e-14, (n, r["Z"][0, n], want)
+    for i, shard in enumerate(g["P_coefficients"]):
+        for n, coeff in enumerate(shard):
+            want = sum(c * gel(float(a)) for a, c in coeff.items())
+            assert abs(r["P"][0, i, n] - want) <= 1e-14, (i, n, r["P"][0, i, n], want)
+
+
+def pin_identity_matches_numpy(orc):
+    """Activation switched off: Z = (X W1 + b1) W2 + b2, checked against numpy's float64
+    matmul (a library primitive, independent of the oracle's loops). Catches transposed
+    operands, wrong shard offsets, dropped or repeated biases."""
+    for k in (1, 4):
+        d, f = _small()
+        r = orc.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], k, act=oracle.ACT_IDENTITY,
+                      want_y=True)
+        A = f["X"] @ f["W1"] + f["b1"]
+        Z = A @ f["W2"] + f["b2"]
+        assert _rel_fro(r["Y"], A) <= 1e-13, _rel_fro(r["Y"], A)
+        assert _rel_fro(r["Z"], Z) <= 1e-12, _rel_fro(r["Z"], Z)
+
+
+def pin_concat_identity(orc):
+    """Column split: the concatenated shard activations equal GeLU(X W1 + b1) of the
+    unsharded product (numpy matmul + scipy ndtr), and are identical for every k."""
+    from scipy.special import ndtr
+    d, f = _small()
+    A = f["X"] @ f["W1"] + f["b1"]
+    Yref = A * ndtr(A)
+    ys = []
+    for k in (1, 2, 4, 8):
+        r = orc.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], k, want_y=True)
+        assert _rel_fro(r["Y"], Yref) <= 1e-13, (k, _rel_fro(r["Y"], Yref))
+        ys.append(r["Y"])
+    for y in ys[1:]:
+        assert np.array_equal(y, ys[0])
+
+
+def pin_row_split_sum(orc):
+    """Row split: each partial is Y[:, shard] W2[shard, :], and their sum equals the
+    unsharded Y W2 (numpy float64) to 1e-12 relative."""
+    k = 4
+    d, f = _small()
+    r = orc.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], k, want_y=True, want_partials=True)
+    Y, P = r["Y"], r["P"]
+    F = Y.shape[1]
+    fw = F // k
+    for i in range(k):
+        Pi = Y[:, i * fw:(i + 1) * fw] @ f["W2"][i * fw:(i + 1) * fw, :]
+        assert _rel_fro(P[:, i, :], Pi) <= 1e-12, (i, _rel_fro(P[:, i, :], Pi))
+    full = Y @ f["W2"]
+    assert _rel_fro(P.sum(axis=1), full) <= 1e-12
+    assert _rel_fro(r["Z"], full + f["b2"]) <= 1e-12
+
+
+def pin_k_invariance(orc):
+    """The block's output does not depend on the shard count k."""
+    d, _ = _small(seed=11, H=64, F=512, M=19)
+    z1 = orc.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], 1)["Z"]
+    for k in (2, 4, 8, 16):
+        zk = orc.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], k)["Z"]
+        assert _rel_fro(zk, z1) <= 1e-12, (k, _rel_fro(zk, z1))
+
+
+def pin_w2_zero(orc):
+    """W2 = 0  =>  Z = b2 exactly, whatever X, W1, b1 and k are."""
+    d, f = _small()
+    W2 = np.zeros_like(d["W2"])
+    for k in (1, 4):
+        r = orc.tpmlp(d["X"], d["W1"], d["b1"], W2, d["b2"], k)
+        assert np.array_equal(r["Z"], np.broadcast_to(f["b2"], r["Z"].shape)), k
+
+
+def pin_w1_zero(orc):
+    """W1 = 0  =>  every row's activation is GeLU(b1), and Z = GeLU(b1) W2 + b2."""
+    from scipy.special import ndtr
+    d, f = _small()
+    W1 = np.zeros_like(d["W1"])
+    r = orc.tpmlp(d["X"], W1, d["b1"], d["W2"], d["b2"], 4, want_y=True)
+    gb = f["b1"] * ndtr(f["b1"])
+    assert np.max(np.abs(r["Y"] - gb)) <= 1e-17
+    z = gb @ f["W2"] + f["b2"]
+    assert _rel_fro(r["Z"], np.broadcast_to(z, r["Z"].shape)) <= 1e-12
+
+
+def pin_rows_independent(orc):
+    """Any subset of token rows is evaluated exactly as in the full evaluation."""
+    d, _ = _small(M=23)
+    full = orc.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], 4)["Z"]
+    rows = np.array([22, 0, 5, 17], dtype=np.int64)
+    sub = orc.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], 4, rows=rows)["Z"]
+    assert np.array_equal(sub, full[rows])
+
+
+def pin_x_linear_without_activation(orc):
+    """With the activation off and biases zero the block is linear in X:
+    f(2X) = 2 f(X) exactly (doubling is exact in binary floating point)."""
+    d, _ = _small()
+    zb1 = np.zeros_like(d["b1"])
+    zb2 = np.zeros_like(d["b2"])
+    X2 = synth.round_bf16(2.0 * synth.bf16_to_f64(d["X"]))
+    z = orc.tpmlp(d["X"], d["W1"], zb1, d["W2"], zb2, 4, act=oracle.ACT_IDENTITY)["Z"]
+    z2 = orc.tpmlp(X2, d["W1"], zb1, d["W2"], zb2, 4, act=oracle.ACT_IDENTITY)["Z"]
+    assert np.array_equal(z2, 2.0 * z)
+
+
+ALL_PINS = [
+    pin_gelu_table, pin_gelu_ndtr, pin_gelu_odd_part, pin_bruteforce_golden,
+    pin_identity_matches_numpy, pin_concat_identity, pin_row_split_sum, pin_k_invariance,
+    pin_w2_zero, pin_w1_zero, pin_rows_independent, pin_x_linear_without_activation,
+]

@@ -1,0 +1,52 @@
+"""Plant one plausible mistake at a time in a copy of the oracle's C source (on the
+CPU) and check that at least one pin catches it. This is what shows that the pins
+constrain every term of the oracle: the bias slices, the shard offsets, the order of
+the operands, the activation's form and the single sum over shards."""
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+MUTANTS = {
+    "drop_b1": ("const double a = acc[jj] + widen_bf16(b1[j0 + jj]);",
+                "const double a = acc[jj];"),
+    "b1_without_shard_offset": ("widen_bf16(b1[j0 + jj])", "widen_bf16(b1[jj])"),
+    "b2_added_per_shard": ("Z[r * H + n] = zsum[n] + widen_bf16(b2[n]);",
+                           "Z[r * H + n] = zsum[n] + k * widen_bf16(b2[n]);"),
+    "drop_b2": ("Z[r * H + n] = zsum[n] + widen_bf16(b2[n]);", "Z[r * H + n] = zsum[n];"),
+    "w1_without_shard_offset": ("const uint16_t *w = W1 + h * F + j0;",
+                                "const uint16_t *w = W1 + h * F;"),
+    "w2_without_shard_offset": ("const uint16_t *w = W2 + (j0 + jj) * H;",
+                                "const uint16_t *w = W2 + jj * H;"),
+    "gelu_missing_half": ("return 0.5 * a * (1.0 + erf(a / sqrt(2.0)));",
+                          "return a * (1.0 + erf(a / sqrt(2.0)));"),
+    "gelu_sign_flip": ("return 0.5 * a * (1.0 + erf(a / sqrt(2.0)));",
+                       "return 0.5 * a * (1.0 - erf(a / sqrt(2.0)));"),
+    "gelu_wrong_scale": ("return 0.5 * a * (1.0 + erf(a / sqrt(2.0)));",
+                         "return 0.5 * a * (1.0 + erf(a / 2.0));"),
+    "gelu_tanh_form": ("return 0.5 * a * (1.0 + erf(a / sqrt(2.0)));",
+                       "return 0.5 * a * (1.0 + tanh(0.7978845608028654 * (a + 0.044715 * a * a * a)));"),
+    "last_shard_dropped": ("for (int32_t i = 0; i < k; ++i) {",
+                           "for (int32_t i = 0; i < k - (k > 1); ++i) {"),
+    "partial_not_reset": ("for (int64_t n = 0; n < H; ++n) part[n] = 0.0;", ""),
+    "x_row_ignores_selection": ("const uint16_t *x = X + m * H;", "const uint16_t *x = X + r * H;"),
+    "y_written_without_shard_offset": ("Y[r * F + j0 + jj] = acc[jj];", "Y[r * F + jj] = acc[jj];"),
+    "activation_dropped": ("acc[jj] = (act == ORACLE_ACT_GELU) ? oracle_gelu(a) : a;",
+                              "acc[jj] = a;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    orc = oracle.compile_source(src.replace(old, new), str(tmp_path / f"mut_{name}.so"))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            caught.append(pin.__name__)
+            break
+    assert caught, f"no pin caught the planted mistake {name}"
