@@ -1,0 +1,169 @@
+/*
+ * tpmlp -- the tensor-parallel (Megatron-style) MLP block on one GB300 (sm_103a).
+ *
+ * The block (千亿参数模型如何拆分到多张GPU上训练, "方案一：按列切分权重矩阵" and
+ * "方案二：按行切分权重矩阵"; 大模型分布式并行策略详解：TP、DP、PP、CP、EP核心原理与实战 §4.1;
+ * AI大模型分布式训练：张量并行与流水线并行深度实践 §2.1-2.2):
+ *
+ *     Y_i = GeLU(X W1_i + b1_i)            i = 0..k-1, W1_i = W1[:, i f:(i+1) f]
+ *     Z   = sum_i Y_i W2_i + b2                        W2_i = W2[i f:(i+1) f, :]
+ *
+ * with X [B, S, H], W1 [H, F], W2 [F, H], F = 4H on the pages' models (any F works),
+ * f = F / k the shard width, and GeLU the exact erf form. The pages run each shard on
+ * its own GPU and add the k partials with one All-Reduce; here all k shards run on one
+ * GPU and the sum over shards is accumulated in the same fp32 tensor-memory tile of the
+ * second GEMM, so it costs no extra pass over memory and no collective.
+ *
+ * Conventions for every call:
+ *  - Pointers named "device" are CUDA device addresses on the context's device; the
+ *    caller owns them and keeps them alive until the stream work that uses them is done.
+ *  - Tensors are dense, row-major, bfloat16 unless stated otherwise; device pointers must
+ *    be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). All
+ *    device work is enqueued on it; no call synchronises unless its comment says so.
+ *  - Every call returns TPMLP_OK (0) or a negative tpmlp_status; no C++ exception or abort
+ *    ever crosses this interface. A failed call leaves the context usable unless it
+ *    returned TPMLP_ERR_CUDA (a sticky CUDA error, after which the context should be
+ *    destroyed).
+ *  - A context is used from one host thread at a time.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TPMLP_API __attribute__((visibility("default")))
+#else
+#define TPMLP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tpmlp_ctx tpmlp_ctx; /* opaque, owned by the library */
+
+typedef enum {
+    TPMLP_OK = 0,
+    TPMLP_ERR_INVALID_ARG = -1,       /* null pointer, non-positive size, ... */
+    TPMLP_ERR_UNSUPPORTED_SHAPE = -2, /* see tpmlp_create's shape rules */
+    TPMLP_ERR_NOT_PACKED = -3,        /* forward before tpmlp_pack_shards */
+    TPMLP_ERR_CUDA = -4,              /* a CUDA runtime/driver call failed (see tpmlp_last_error) */
+    TPMLP_ERR_OOM = -5,               /* device allocation failed */
+    TPMLP_ERR_DEVICE_TIMEOUT = -6,    /* a kernel gave up waiting on a pipeline barrier */
+    TPMLP_ERR_ARCH = -7,              /* the current device is not sm_103 */
+    TPMLP_ERR_MISALIGNED = -8         /* a device pointer is not 16-byte aligned */
+} tpmlp_status;
+
+/* Flags for tpmlp_create. */
+#define TPMLP_FLAG_Z_FP32 0x1u /* Z is written as fp32 instead of bf16 */
+
+/*
+ * Create a context for one block shape on the current CUDA device.
+ *   out      receives the context (set to NULL on failure)
+ *   H        hidden size (columns of X and Z); a multiple of 64
+ *   F        intermediate size (columns of W1, rows of W2); a multiple of 64
+ *   k        shard count: F % k == 0 and f = F/k a multiple of 64 (the pages' tensor
+ *            parallel degree; shards are contiguous, equal column blocks of W1 and the
+ *            matching row blocks of W2 -- AI大模型分布式训练 §2.1 splits W into
+ *            [hidden, ffn/k] pieces)
+ *   flags    0 or TPMLP_FLAG_Z_FP32
+ * Allocates the packed-weight buffers (2*H*F bf16 + (F+H) fp32) and a device status word;
+ * the intermediate activation buffer is allocated by tpmlp_reserve or the first forward.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ARCH (device is not sm_103), OOM, CUDA.
+ */
+TPMLP_API int tpmlp_create(tpmlp_ctx **out, int64_t H, int64_t F, int32_t k, uint32_t flags);
+
+/*
+ * Pack the weights into the kernels' layout (one-time per weight set; the shard packer).
+ *   W1 device bf16 [H, F]   b1 device bf16 [F]   W2 device bf16 [F, H]   b2 device bf16 [H]
+ * W1 is in the pages' math orientation (Y = X W1, AI大模型分布式训练 §2.1 allocates the
+ * column-parallel weight as [in_features, out_features / k]), not [out, in].
+ * Writes W1p [k][f][H] (each column shard transposed so that its reduction dimension H is
+ * contiguous), W2p [k][H][f] (each row shard transposed likewise), and fp32 copies of b1
+ * and b2. The raw weights may be freed once the stream has passed this call.
+ * Errors: INVALID_ARG, MISALIGNED, CUDA.
+ */
+TPMLP_API int tpmlp_pack_shards(tpmlp_ctx *ctx, const void *W1, const void *b1, const void *W2,
+                      const void *b2, void *stream);
+
+/*
+ * Make sure the intermediate buffer Y [M, F] (bf16) holds at least max_tokens rows.
+ * Synchronises the device when it has to grow the buffer. Forward calls grow it on demand;
+ * call this first to keep allocation out of a timed or captured region.
+ * Errors: INVALID_ARG, OOM, CUDA.
+ */
+TPMLP_API int tpmlp_reserve(tpmlp_ctx *ctx, int64_t max_tokens);
+
+/*
+ * The block's forward pass: Z = sum_i GeLU(X W1_i + b1_i) W2_i + b2.
+ *   X   device bf16 [B, S, H] (M = B*S token rows, each independent)
+ *   Z   device [B, S, H], bf16 (or fp32 with TPMLP_FLAG_Z_FP32); must not overlap X
+ * Two kernel launches on `stream`: the first GEMM with its fused bias + GeLU epilogue
+ * writing Y [M, F] bf16 into the context's buffer, then the second GEMM, which sums all k
+ * shards' partials in one fp32 accumulator and adds b2 once. B*S == 0 is a no-op.
+ * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, OOM (growing Y), CUDA. A pipeline timeout
+ * inside a kernel is reported by tpmlp_get_status, not here.
+ */
+TPMLP_API int tpmlp_forward(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z, void *stream);
+
+/*
+ * tpmlp_forward on host buffers: copies X (host, [B,S,H] bf16) to a device staging buffer,
+ * runs the forward pass and copies Z back to host memory, all on `stream`, then waits for
+ * the stream. Page-locked host memory gives asynchronous, full-speed copies; pageable
+ * memory works but is slower. Staging buffers are owned by the context and grow on demand.
+ * Errors: as tpmlp_forward.
+ */
+TPMLP_API int tpmlp_forward_host(tpmlp_ctx *ctx, const void *X_host, int64_t B, int64_t S, void *Z_host,
+                       void *stream);
+
+/*
+ * The first step alone (column-parallel GEMM of every shard + b1 + GeLU):
+ *   Y[m, i f + j] = GeLU(b1[i f + j] + sum_h X[m, h] W1[h, i f + j])   rounded to bf16
+ *   X device bf16 [M, H]; Y device bf16 [M, F] (shard i in columns [i f, (i+1) f)).
+ * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, CUDA.
+ */
+TPMLP_API int tpmlp_gemm1(tpmlp_ctx *ctx, const void *X, int64_t M, void *Y, void *stream);
+
+/*
+ * The second step alone (row-parallel GEMM of every shard, the sum over shards -- the
+ * pages' All-Reduce -- done in the fp32 accumulator, + b2):
+ *   Z[m, n] = b2[n] + sum_i sum_{j<f} Y[m, i f + j] W2[i f + j, n]
+ *   Y device bf16 [M, F]; Z device [M, H] (bf16, or fp32 with TPMLP_FLAG_Z_FP32).
+ * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, CUDA.
+ */
+TPMLP_API int tpmlp_gemm2(tpmlp_ctx *ctx, const void *Y, int64_t M, void *Z, void *stream);
+
+/*
+ * Read and clear the device status word that the kernels set when a bounded wait gives up
+ * (synchronises `stream`). Returns TPMLP_OK, TPMLP_ERR_DEVICE_TIMEOUT or TPMLP_ERR_CUDA.
+ * *detail (optional) receives the raw word: which barrier wait gave up.
+ */
+TPMLP_API int tpmlp_get_status(tpmlp_ctx *ctx, void *stream, int32_t *detail);
+
+/*
+ * Where the packed weights live (for tests that unpack and compare them bit for bit).
+ *   which: 0 = W1p bf16 [k][f][H], 1 = W2p bf16 [k][H][f], 2 = b1 fp32 [F], 3 = b2 fp32 [H]
+ * *ptr receives a device pointer owned by the context; *bytes its size.
+ * Errors: INVALID_ARG, NOT_PACKED.
+ */
+TPMLP_API int tpmlp_packed_buffer(const tpmlp_ctx *ctx, int32_t which, const void **ptr, int64_t *bytes);
+
+/* Release everything the context owns (synchronises its device first). NULL is a no-op. */
+TPMLP_API void tpmlp_destroy(tpmlp_ctx *ctx);
+
+/* Static, human-readable text for a tpmlp_status value. */
+TPMLP_API const char *tpmlp_strerror(int status);
+
+/* The last CUDA error text recorded on this context ("" if none); valid until the next call. */
+TPMLP_API const char *tpmlp_last_error(const tpmlp_ctx *ctx);
+
+/* The number of kernel launches this context has issued so far (pack + forward). */
+TPMLP_API int64_t tpmlp_launch_count(const tpmlp_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

@@ -1,0 +1,293 @@
+"""tensor_transformer_mlp_tmem_gb300 -- the Megatron-style tensor-parallel MLP block on one
+GB300, all k shards on one GPU, the cross-shard sum done in tensor memory.
+
+This module is the Python binding of ``libtpmlp.so`` (include/tpmlp.h): the functions
+below carry the C entry points' names and only marshal arguments (device pointers, sizes,
+streams). Every step of the block runs in the library's CUDA kernels; there is no Python
+or CPU fallback, and importing a function whose library is missing raises.
+
+The block (千亿参数模型如何拆分到多张GPU上训练, "方案一"/"方案二"; 大模型分布式并行策略详解 §4.1;
+AI大模型分布式训练 §2.1-2.2):  Y_i = GeLU(X W1_i + b1_i),  Z = sum_i Y_i W2_i + b2.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "TPMLP", "TpmlpError", "load_library", "library_path",
+    "tpmlp_create", "tpmlp_pack_shards", "tpmlp_reserve", "tpmlp_forward", "tpmlp_forward_host",
+    "tpmlp_gemm1", "tpmlp_gemm2", "tpmlp_get_status", "tpmlp_packed_buffer", "tpmlp_destroy",
+    "tpmlp_strerror", "tpmlp_last_error", "tpmlp_launch_count",
+    "TPMLP_OK", "TPMLP_ERR_INVALID_ARG", "TPMLP_ERR_UNSUPPORTED_SHAPE", "TPMLP_ERR_NOT_PACKED",
+    "TPMLP_ERR_CUDA", "TPMLP_ERR_OOM", "TPMLP_ERR_DEVICE_TIMEOUT", "TPMLP_ERR_ARCH",
+    "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32",
+]
+
+TPMLP_OK = 0
+TPMLP_ERR_INVALID_ARG = -1
+TPMLP_ERR_UNSUPPORTED_SHAPE = -2
+TPMLP_ERR_NOT_PACKED = -3
+TPMLP_ERR_CUDA = -4
+TPMLP_ERR_OOM = -5
+TPMLP_ERR_DEVICE_TIMEOUT = -6
+TPMLP_ERR_ARCH = -7
+TPMLP_ERR_MISALIGNED = -8
+TPMLP_FLAG_Z_FP32 = 0x1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libtpmlp.so")
+
+
+class TpmlpError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {tpmlp_strerror(status)} ({status})"
+        if detail:
+            msg += f": {detail}"
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libtpmlp.so (built in-tree by ``__graft_entry__.build()``). Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run `python -c 'import __graft_entry__ as g; "
+                           f"g.build()'` (nvcc, sm_103a). There is no fallback path.")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+    sig = {
+        "tpmlp_create": ([ctypes.POINTER(vp), i64, i64, i32, u32], ctypes.c_int),
+        "tpmlp_pack_shards": ([vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "tpmlp_reserve": ([vp, i64], ctypes.c_int),
+        "tpmlp_forward": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_forward_host": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_gemm1": ([vp, vp, i64, vp, vp], ctypes.c_int),
+        "tpmlp_gemm2": ([vp, vp, i64, vp, vp], ctypes.c_int),
+        "tpmlp_get_status": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
+        "tpmlp_packed_buffer": ([vp, i32, ctypes.POINTER(vp), ctypes.POINTER(i64)], ctypes.c_int),
+        "tpmlp_destroy": ([vp], None),
+        "tpmlp_strerror": ([ctypes.c_int], ctypes.c_char_p),
+        "tpmlp_last_error": ([vp], ctypes.c_char_p),
+        "tpmlp_launch_count": ([vp], i64),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def _ptr(x) -> int | None:
+    """Device/host address of a torch tensor, numpy array, ctypes object or int."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    if hasattr(x, "ctypes"):
+        return int(x.ctypes.data)
+    if isinstance(x, ctypes.c_void_p):
+        return x.value
+    raise TypeError(f"cannot take the address of {type(x).__name__}")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return int(torch.cuda.current_stream().cuda_stream) or None
+        except Exception:  # torch absent: the legacy default stream
+            pass
+        return None
+    if isinstance(s, int):
+        return s or None
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream) or None
+    raise TypeError("stream must be a torch.cuda.Stream, an int handle or None")
+
+
+def _check(rc: int, where: str, ctx=None):
+    if rc != TPMLP_OK:
+        detail = tpmlp_last_error(ctx) if ctx is not None else ""
+        raise TpmlpError(rc, where, detail)
+
+
+# ------------------------------------------------------------------ C entry points
+def tpmlp_create(H: int, F: int, k: int, flags: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(load_library().tpmlp_create(ctypes.byref(out), H, F, k, flags), "tpmlp_create")
+    return out.value
+
+
+def tpmlp_pack_shards(ctx: int, W1, b1, W2, b2, stream=None) -> None:
+    _check(load_library().tpmlp_pack_shards(ctx, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
+                                            _stream(stream)), "tpmlp_pack_shards", ctx)
+
+
+def tpmlp_reserve(ctx: int, max_tokens: int) -> None:
+    _check(load_library().tpmlp_reserve(ctx, max_tokens), "tpmlp_reserve", ctx)
+
+
+def tpmlp_forward(ctx: int, X, B: int, S: int, Z, stream=None) -> None:
+    _check(load_library().tpmlp_forward(ctx, _ptr(X), B, S, _ptr(Z), _stream(stream)),
+           "tpmlp_forward", ctx)
+
+
+def tpmlp_forward_host(ctx: int, X_host, B: int, S: int, Z_host, stream=None) -> None:
+    _check(load_library().tpmlp_forward_host(ctx, _ptr(X_host), B, S, _ptr(Z_host),
+                                             _stream(stream)), "tpmlp_forward_host", ctx)
+
+
+def tpmlp_gemm1(ctx: int, X, M: int, Y, stream=None) -> None:
+    _check(load_library().tpmlp_gemm1(ctx, _ptr(X), M, _ptr(Y), _stream(stream)), "tpmlp_gemm1",
+           ctx)
+
+
+def tpmlp_gemm2(ctx: int, Y, M: int, Z, stream=None) -> None:
+    _check(load_library().tpmlp_gemm2(ctx, _ptr(Y), M, _ptr(Z), _stream(stream)), "tpmlp_gemm2",
+           ctx)
+
+
+def tpmlp_get_status(ctx: int, stream=None):
+    """Returns (status, raw detail word); clears the device status word."""
+    detail = ctypes.c_int32(0)
+    rc = load_library().tpmlp_get_status(ctx, _stream(stream), ctypes.byref(detail))
+    if rc not in (TPMLP_OK, TPMLP_ERR_DEVICE_TIMEOUT):
+        _check(rc, "tpmlp_get_status", ctx)
+    return rc, int(detail.value)
+
+
+def tpmlp_packed_buffer(ctx: int, which: int):
+    """(device pointer, bytes) of a packed buffer: 0 W1p, 1 W2p, 2 b1 fp32, 3 b2 fp32."""
+    p = ctypes.c_void_p()
+    n = ctypes.c_int64()
+    _check(load_library().tpmlp_packed_buffer(ctx, which, ctypes.byref(p), ctypes.byref(n)),
+           "tpmlp_packed_buffer", ctx)
+    return p.value, n.value
+
+
+def tpmlp_destroy(ctx) -> None:
+    load_library().tpmlp_destroy(ctx)
+
+
+def tpmlp_strerror(status: int) -> str:
+    return load_library().tpmlp_strerror(status).decode()
+
+
+def tpmlp_last_error(ctx) -> str:
+    return load_library().tpmlp_last_error(ctx).decode()
+
+
+def tpmlp_launch_count(ctx) -> int:
+    return int(load_library().tpmlp_launch_count(ctx))
+
+
+# ------------------------------------------------------------------ object wrapper
+class TPMLP:
+    """One block shape on the current CUDA device (torch supplies memory and streams).
+
+        mlp = TPMLP(H, F, k)
+        mlp.pack(W1, b1, W2, b2)       # bf16 CUDA tensors [H,F], [F], [F,H], [H]
+        Z = mlp(X)                     # X bf16 [B, S, H] -> Z [B, S, H]
+    """
+
+    def __init__(self, H: int, F: int, k: int, z_fp32: bool = False):
+        self.H, self.F, self.k = H, F, k
+        self.z_fp32 = z_fp32
+        self.ctx = tpmlp_create(H, F, k, TPMLP_FLAG_Z_FP32 if z_fp32 else 0)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            tpmlp_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @staticmethod
+    def _require(t, dtype, shape, what):
+        import torch
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{what} must be a CUDA tensor")
+        if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+            raise ValueError(f"{what}: expected contiguous {dtype} {tuple(shape)}, got "
+                             f"{t.dtype} {tuple(t.shape)}")
+
+    def pack(self, W1, b1, W2, b2, stream=None):
+        import torch
+        bf = torch.bfloat16
+        self._require(W1, bf, (self.H, self.F), "W1")
+        self._require(b1, bf, (self.F,), "b1")
+        self._require(W2, bf, (self.F, self.H), "W2")
+        self._require(b2, bf, (self.H,), "b2")
+        tpmlp_pack_shards(self.ctx, W1, b1, W2, b2, stream)
+
+    def reserve(self, max_tokens: int):
+        tpmlp_reserve(self.ctx, max_tokens)
+
+    def out_dtype(self):
+        import torch
+        return torch.float32 if self.z_fp32 else torch.bfloat16
+
+    def forward(self, X, Z=None, stream=None):
+        import torch
+        if X.dim() != 3:
+            raise ValueError("X must be [B, S, H]")
+        B, S, H = X.shape
+        self._require(X, torch.bfloat16, (B, S, self.H), "X")
+        if Z is None:
+            Z = torch.empty((B, S, self.H), dtype=self.out_dtype(), device=X.device)
+        else:
+            self._require(Z, self.out_dtype(), (B, S, self.H), "Z")
+        tpmlp_forward(self.ctx, X, B, S, Z, stream)
+        return Z
+
+    __call__ = forward
+
+    def gemm1(self, X2d, Y=None, stream=None):
+        import torch
+        M = X2d.shape[0]
+        self._require(X2d, torch.bfloat16, (M, self.H), "X")
+        if Y is None:
+            Y = torch.empty((M, self.F), dtype=torch.bfloat16, device=X2d.device)
+        tpmlp_gemm1(self.ctx, X2d, M, Y, stream)
+        return Y
+
+    def gemm2(self, Y, Z=None, stream=None):
+        import torch
+        M = Y.shape[0]
+        self._require(Y, torch.bfloat16, (M, self.F), "Y")
+        if Z is None:
+            Z = torch.empty((M, self.H), dtype=self.out_dtype(), device=Y.device)
+        tpmlp_gemm2(self.ctx, Y, M, Z, stream)
+        return Z
+
+    def status(self, stream=None):
+        return tpmlp_get_status(self.ctx, stream)
+
+    @property
+    def launches(self) -> int:
+        return tpmlp_launch_count(self.ctx)

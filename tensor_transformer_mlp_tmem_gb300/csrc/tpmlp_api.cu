@@ -1,0 +1,439 @@
+// The C ABI of the tensor-parallel MLP library (declared in include/tpmlp.h): argument
+// checks, buffers, tensor-map encoding and kernel launches. No C++ exception and no abort
+// crosses this boundary: every entry point returns a tpmlp_status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "tpmlp.h"
+#include "tpmlp_gemm.cuh"
+#include "tpmlp_pack.cuh"
+
+struct tpmlp_ctx {
+    int device = -1;
+    int num_sms = 0;
+    int64_t H = 0, F = 0, f = 0;
+    int32_t k = 0;
+    uint32_t flags = 0;
+    int bn1 = 0, bn2 = 0;  // output tile widths of GEMM1 / GEMM2
+
+    uint16_t* W1p = nullptr;  // [k][f][H]
+    uint16_t* W2p = nullptr;  // [k][H][f]
+    float* b1 = nullptr;      // [F]
+    float* b2 = nullptr;      // [H]
+    bool packed = false;
+    CUtensorMap tmW1{}, tmW2{};
+
+    uint16_t* Y = nullptr;  // [y_rows][F] intermediate activations
+    int64_t y_rows = 0;
+    void* Xs = nullptr;  // staging for tpmlp_forward_host
+    void* Zs = nullptr;
+    int64_t stage_rows = 0;
+
+    int* status = nullptr;  // device status word
+    int64_t launches = 0;
+    std::string last_error;
+};
+
+namespace {
+
+using tpmlp::GemmArgs;
+using tpmlp::Mode;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+int fail_cuda(tpmlp_ctx* c, cudaError_t e, const char* what) {
+    if (c) c->last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return e == cudaErrorMemoryAllocation ? TPMLP_ERR_OOM : TPMLP_ERR_CUDA;
+}
+
+#define TPMLP_CUDA(ctx, call)                                   \
+    do {                                                        \
+        cudaError_t e_ = (call);                                \
+        if (e_ != cudaSuccess) return fail_cuda(ctx, e_, #call); \
+    } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int get_encoder(tpmlp_ctx* c) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess && fn)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else if (g_encode_err == cudaSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+    });
+    if (!g_encode) return fail_cuda(c, g_encode_err, "cuTensorMapEncodeTiled entry point");
+    return TPMLP_OK;
+}
+
+// bf16 tensor map with the 128-byte swizzle; dims/strides innermost first, strides in bytes
+// for dims 1..rank-1. Out-of-range boxes are zero filled.
+int encode_map(tpmlp_ctx* c, CUtensorMap* map, const void* ptr, int rank, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box) {
+    int rc = get_encoder(c);
+    if (rc) return rc;
+    cuuint64_t d[3], s[2];
+    cuuint32_t b[3], e[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), d, s,
+                          b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        c->last_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(int(r));
+        return TPMLP_ERR_CUDA;
+    }
+    return TPMLP_OK;
+}
+
+int pick_bn(int64_t width) {
+    if (width % 256 == 0) return 256;
+    if (width % 128 == 0) return 128;
+    return 64;
+}
+
+template <int BN, int STAGES, Mode MODE, bool F32>
+int launch_gemm(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                cudaStream_t s) {
+    auto kern = tpmlp::tpmlp_gemm_kernel<BN, STAGES, MODE, F32>;
+    constexpr uint32_t smem = tpmlp::GemmSmem<BN, STAGES>::kTotal;
+    TPMLP_CUDA(c, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    const int grid = std::min(args.num_tiles, c->num_sms);
+    kern<<<grid, tpmlp::kNumThreads, smem, s>>>(a, b, args);
+    TPMLP_CUDA(c, cudaGetLastError());
+    ++c->launches;
+    return TPMLP_OK;
+}
+
+// Stage depth per tile width: 192 KB of operand ring in every case.
+template <Mode MODE, bool F32>
+int dispatch_gemm(tpmlp_ctx* c, int bn, const CUtensorMap& a, const CUtensorMap& b,
+                  const GemmArgs& args, cudaStream_t s) {
+    switch (bn) {
+        case 256: return launch_gemm<256, 4, MODE, F32>(c, a, b, args, s);
+        case 128: return launch_gemm<128, 6, MODE, F32>(c, a, b, args, s);
+        default: return launch_gemm<64, 8, MODE, F32>(c, a, b, args, s);
+    }
+}
+
+GemmArgs base_args(const tpmlp_ctx* c, int64_t M, int ldo, int bn) {
+    GemmArgs a{};
+    a.M = static_cast<int>(M);
+    a.ldo = ldo;
+    a.f = static_cast<int>(c->f);
+    a.k = c->k;
+    a.m_blocks = static_cast<int>((M + tpmlp::kBM - 1) / tpmlp::kBM);
+    a.n_blocks = ldo / bn;
+    a.num_tiles = a.m_blocks * a.n_blocks;
+    a.group_m = 8;
+    a.status = c->status;
+    return a;
+}
+
+int check_ctx(const tpmlp_ctx* c) {
+    if (!c) return TPMLP_ERR_INVALID_ARG;
+    if (!c->packed) return TPMLP_ERR_NOT_PACKED;
+    return TPMLP_OK;
+}
+
+int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
+    CUtensorMap tmX;
+    const uint64_t dims[2] = {static_cast<uint64_t>(c->H), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(c->H) * 2};
+    const uint32_t box[2] = {tpmlp::kBK, tpmlp::kBM};
+    int rc = encode_map(c, &tmX, X, 2, dims, strides, box);
+    if (rc) return rc;
+    GemmArgs a = base_args(c, M, static_cast<int>(c->F), c->bn1);
+    a.kb_tile = static_cast<int>(c->H / tpmlp::kBK);
+    a.kb_shard = a.kb_tile;
+    a.bias = c->b1;
+    a.out = Y;
+    return dispatch_gemm<Mode::kGemm1, false>(c, c->bn1, tmX, c->tmW1, a, s);
+}
+
+int run_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, cudaStream_t s) {
+    CUtensorMap tmY;
+    const uint64_t dims[2] = {static_cast<uint64_t>(c->F), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(c->F) * 2};
+    const uint32_t box[2] = {tpmlp::kBK, tpmlp::kBM};
+    int rc = encode_map(c, &tmY, Y, 2, dims, strides, box);
+    if (rc) return rc;
+    GemmArgs a = base_args(c, M, static_cast<int>(c->H), c->bn2);
+    a.kb_shard = static_cast<int>(c->f / tpmlp::kBK);
+    a.kb_tile = a.kb_shard * c->k;
+    a.bias = c->b2;
+    a.out = Z;
+    if (c->flags & TPMLP_FLAG_Z_FP32)
+        return dispatch_gemm<Mode::kGemm2, true>(c, c->bn2, tmY, c->tmW2, a, s);
+    return dispatch_gemm<Mode::kGemm2, false>(c, c->bn2, tmY, c->tmW2, a, s);
+}
+
+int ensure_y(tpmlp_ctx* c, int64_t rows) {
+    if (rows <= c->y_rows) return TPMLP_OK;
+    const int64_t want = ((rows + tpmlp::kBM - 1) / tpmlp::kBM) * tpmlp::kBM;
+    TPMLP_CUDA(c, cudaDeviceSynchronize());  // the old buffer may still be in use
+    if (c->Y) cudaFree(c->Y);
+    c->Y = nullptr;
+    c->y_rows = 0;
+    TPMLP_CUDA(c, cudaMalloc(&c->Y, static_cast<size_t>(want) * c->F * 2));
+    c->y_rows = want;
+    return TPMLP_OK;
+}
+
+int check_tokens(int64_t B, int64_t S) {
+    if (B < 0 || S < 0) return TPMLP_ERR_INVALID_ARG;
+    if (S > 0 && B > (int64_t(1) << 31) / S) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    return TPMLP_OK;
+}
+
+int z_elem_bytes(const tpmlp_ctx* c) { return (c->flags & TPMLP_FLAG_Z_FP32) ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flags) {
+    if (!out) return TPMLP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (H <= 0 || F <= 0 || k <= 0) return TPMLP_ERR_INVALID_ARG;
+    if (flags & ~TPMLP_FLAG_Z_FP32) return TPMLP_ERR_INVALID_ARG;
+    if (H % 64 || F % 64 || F % k || (F / k) % 64) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (H > (int64_t(1) << 20) || F > (int64_t(1) << 22)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TPMLP_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return TPMLP_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return TPMLP_ERR_ARCH;
+
+    tpmlp_ctx* c = new (std::nothrow) tpmlp_ctx();
+    if (!c) return TPMLP_ERR_OOM;
+    c->device = dev;
+    c->num_sms = prop.multiProcessorCount;
+    c->H = H;
+    c->F = F;
+    c->k = k;
+    c->f = F / k;
+    c->flags = flags;
+    c->bn1 = pick_bn(c->f);
+    c->bn2 = pick_bn(H);
+    int rc = TPMLP_OK;
+    cudaError_t e;
+    if ((e = cudaMalloc(&c->W1p, static_cast<size_t>(H) * F * 2)) != cudaSuccess ||
+        (e = cudaMalloc(&c->W2p, static_cast<size_t>(H) * F * 2)) != cudaSuccess ||
+        (e = cudaMalloc(&c->b1, static_cast<size_t>(F) * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&c->b2, static_cast<size_t>(H) * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&c->status, sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(c->status, 0, sizeof(int))) != cudaSuccess) {
+        rc = (e == cudaErrorMemoryAllocation) ? TPMLP_ERR_OOM : TPMLP_ERR_CUDA;
+        tpmlp_destroy(c);
+        return rc;
+    }
+    *out = c;
+    return TPMLP_OK;
+}
+
+int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* W2, const void* b2,
+                      void* stream) {
+    if (!c || !W1 || !b1 || !W2 || !b2) return TPMLP_ERR_INVALID_ARG;
+    if (!aligned16(W1) || !aligned16(W2) || (reinterpret_cast<uintptr_t>(b1) & 1) ||
+        (reinterpret_cast<uintptr_t>(b2) & 1))
+        return TPMLP_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int T = tpmlp::kTransposeTile;
+    {
+        // W1 [H][F] -> W1p [F][H] (= [k][f][H]: shard i is rows [i f, (i+1) f))
+        dim3 grid(static_cast<unsigned>(c->F / T), static_cast<unsigned>(c->H / T), 1);
+        tpmlp::transpose_bf16_kernel<<<grid, dim3(64, 4), 0, s>>>(
+            static_cast<const uint16_t*>(W1), c->W1p, static_cast<int>(c->H),
+            static_cast<int>(c->F), 0, 0);
+        TPMLP_CUDA(c, cudaGetLastError());
+        ++c->launches;
+    }
+    {
+        // W2 [F][H] = k blocks [f][H] -> W2p [k][H][f]
+        dim3 grid(static_cast<unsigned>(c->H / T), static_cast<unsigned>(c->f / T),
+                  static_cast<unsigned>(c->k));
+        tpmlp::transpose_bf16_kernel<<<grid, dim3(64, 4), 0, s>>>(
+            static_cast<const uint16_t*>(W2), c->W2p, static_cast<int>(c->f),
+            static_cast<int>(c->H), static_cast<long long>(c->f) * c->H,
+            static_cast<long long>(c->f) * c->H);
+        TPMLP_CUDA(c, cudaGetLastError());
+        ++c->launches;
+    }
+    tpmlp::bf16_to_f32_kernel<<<static_cast<unsigned>((c->F + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint16_t*>(b1), c->b1, c->F);
+    TPMLP_CUDA(c, cudaGetLastError());
+    tpmlp::bf16_to_f32_kernel<<<static_cast<unsigned>((c->H + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint16_t*>(b2), c->b2, c->H);
+    TPMLP_CUDA(c, cudaGetLastError());
+    c->launches += 2;
+
+    // tensor maps of the packed shards: box 64 (reduction) x BN (output columns) x 1 shard
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(c->H), static_cast<uint64_t>(c->f),
+                                  static_cast<uint64_t>(c->k)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(c->H) * 2,
+                                     static_cast<uint64_t>(c->f) * c->H * 2};
+        const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(c->bn1), 1};
+        int rc = encode_map(c, &c->tmW1, c->W1p, 3, dims, strides, box);
+        if (rc) return rc;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(c->f), static_cast<uint64_t>(c->H),
+                                  static_cast<uint64_t>(c->k)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(c->f) * 2,
+                                     static_cast<uint64_t>(c->f) * c->H * 2};
+        const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(c->bn2), 1};
+        int rc = encode_map(c, &c->tmW2, c->W2p, 3, dims, strides, box);
+        if (rc) return rc;
+    }
+    c->packed = true;
+    return TPMLP_OK;
+}
+
+int tpmlp_reserve(tpmlp_ctx* c, int64_t max_tokens) {
+    if (!c || max_tokens < 0) return TPMLP_ERR_INVALID_ARG;
+    if (max_tokens > (int64_t(1) << 31)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    return ensure_y(c, max_tokens);
+}
+
+int tpmlp_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (!X || !Y || M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(X) || !aligned16(Y)) return TPMLP_ERR_MISALIGNED;
+    if (M == 0) return TPMLP_OK;
+    return run_gemm1(c, X, M, Y, static_cast<cudaStream_t>(stream));
+}
+
+int tpmlp_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (!Y || !Z || M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(Y) || !aligned16(Z)) return TPMLP_ERR_MISALIGNED;
+    if (M == 0) return TPMLP_OK;
+    return run_gemm2(c, Y, M, Z, static_cast<cudaStream_t>(stream));
+}
+
+int tpmlp_forward(tpmlp_ctx* c, const void* X, int64_t B, int64_t S, void* Z, void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (!X || !Z) return TPMLP_ERR_INVALID_ARG;
+    if ((rc = check_tokens(B, S))) return rc;
+    if (!aligned16(X) || !aligned16(Z)) return TPMLP_ERR_MISALIGNED;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if ((rc = ensure_y(c, M))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = run_gemm1(c, X, M, c->Y, s))) return rc;
+    return run_gemm2(c, c->Y, M, Z, s);
+}
+
+int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void* Z_host,
+                       void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
+    if ((rc = check_tokens(B, S))) return rc;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if (M > c->stage_rows) {
+        TPMLP_CUDA(c, cudaDeviceSynchronize());
+        if (c->Xs) cudaFree(c->Xs);
+        if (c->Zs) cudaFree(c->Zs);
+        c->Xs = c->Zs = nullptr;
+        c->stage_rows = 0;
+        TPMLP_CUDA(c, cudaMalloc(&c->Xs, static_cast<size_t>(M) * c->H * 2));
+        TPMLP_CUDA(c, cudaMalloc(&c->Zs, static_cast<size_t>(M) * c->H * z_elem_bytes(c)));
+        c->stage_rows = M;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    TPMLP_CUDA(c, cudaMemcpyAsync(c->Xs, X_host, static_cast<size_t>(M) * c->H * 2,
+                                  cudaMemcpyHostToDevice, s));
+    if ((rc = tpmlp_forward(c, c->Xs, B, S, c->Zs, stream))) return rc;
+    TPMLP_CUDA(c, cudaMemcpyAsync(Z_host, c->Zs, static_cast<size_t>(M) * c->H * z_elem_bytes(c),
+                                  cudaMemcpyDeviceToHost, s));
+    TPMLP_CUDA(c, cudaStreamSynchronize(s));
+    return TPMLP_OK;
+}
+
+int tpmlp_get_status(tpmlp_ctx* c, void* stream, int32_t* detail) {
+    if (!c) return TPMLP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    TPMLP_CUDA(c, cudaStreamSynchronize(s));
+    int v = 0;
+    TPMLP_CUDA(c, cudaMemcpy(&v, c->status, sizeof(int), cudaMemcpyDeviceToHost));
+    TPMLP_CUDA(c, cudaMemset(c->status, 0, sizeof(int)));
+    if (detail) *detail = v;
+    return v ? TPMLP_ERR_DEVICE_TIMEOUT : TPMLP_OK;
+}
+
+int tpmlp_packed_buffer(const tpmlp_ctx* c, int32_t which, const void** ptr, int64_t* bytes) {
+    if (!c || !ptr || !bytes) return TPMLP_ERR_INVALID_ARG;
+    if (!c->packed) return TPMLP_ERR_NOT_PACKED;
+    switch (which) {
+        case 0: *ptr = c->W1p; *bytes = c->H * c->F * 2; return TPMLP_OK;
+        case 1: *ptr = c->W2p; *bytes = c->H * c->F * 2; return TPMLP_OK;
+        case 2: *ptr = c->b1; *bytes = c->F * 4; return TPMLP_OK;
+        case 3: *ptr = c->b2; *bytes = c->H * 4; return TPMLP_OK;
+        default: return TPMLP_ERR_INVALID_ARG;
+    }
+}
+
+void tpmlp_destroy(tpmlp_ctx* c) {
+    if (!c) return;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (c->device >= 0 && cur != c->device) cudaSetDevice(c->device);
+    cudaDeviceSynchronize();
+    cudaFree(c->W1p);
+    cudaFree(c->W2p);
+    cudaFree(c->b1);
+    cudaFree(c->b2);
+    cudaFree(c->Y);
+    cudaFree(c->Xs);
+    cudaFree(c->Zs);
+    cudaFree(c->status);
+    if (cur >= 0 && cur != c->device) cudaSetDevice(cur);
+    delete c;
+}
+
+const char* tpmlp_strerror(int status) {
+    switch (status) {
+        case TPMLP_OK: return "ok";
+        case TPMLP_ERR_INVALID_ARG: return "invalid argument";
+        case TPMLP_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (H, F, F/k multiples of 64; F % k == 0)";
+        case TPMLP_ERR_NOT_PACKED: return "weights not packed (call tpmlp_pack_shards first)";
+        case TPMLP_ERR_CUDA: return "CUDA error (see tpmlp_last_error)";
+        case TPMLP_ERR_OOM: return "device out of memory";
+        case TPMLP_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on a pipeline barrier";
+        case TPMLP_ERR_ARCH: return "device is not sm_103 (GB300)";
+        case TPMLP_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+        default: return "unknown status";
+    }
+}
+
+const char* tpmlp_last_error(const tpmlp_ctx* c) { return c ? c->last_error.c_str() : ""; }
+
+int64_t tpmlp_launch_count(const tpmlp_ctx* c) { return c ? c->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,341 @@
+// The two GEMMs of the tensor-parallel MLP block, as one persistent, warp-specialised
+// sm_103a kernel template:
+//
+//   GEMM1 (column-parallel layer, every shard i):  Y[:, i f + j] = GeLU(X W1_i + b1_i)[:, j]
+//   GEMM2 (row-parallel layer + the sum over shards): Z = b2 + sum_i Y_i W2_i
+//
+// (千亿参数模型如何拆分到多张GPU上训练, "方案一"/"方案二"; 大模型分布式并行策略详解 §4.1.)
+//
+// Per CTA (one per SM, looping over output tiles of kBM x BN):
+//   warp 0      TMA producer: streams kBM x 64 tiles of A and BN x 64 tiles of B (both
+//               K-major, 128-byte swizzled) into a STAGES-deep shared-memory ring.
+//   warp 1      allocates tensor memory (2 x BN fp32 columns: two accumulators) and, from
+//               one lane, issues tcgen05.mma (M = 128, N = BN, K = 16 per instruction).
+//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (each warp owns the 32
+//               TMEM lanes = output rows its warp rank may access), bias, GeLU (GEMM1),
+//               conversion and stores. The accumulator is handed back to the MMA warp as
+//               soon as it has been read, so the next tile's MMAs overlap this epilogue.
+//
+// GEMM2's reduction runs shard-major: shard 0's f/64 blocks, then shard 1's, ... all into
+// the SAME fp32 accumulator. That accumulation is the on-chip replacement for the pages'
+// All-Reduce of the k partial outputs (AI大模型分布式训练 §2.2 sums the RowParallelLinear
+// partials with dist.all_reduce): no partial ever leaves tensor memory.
+//
+// Every wait is bounded (see ptx::mbar_wait); a CTA that gives up records a code in the
+// device status word, drains its in-flight copies and MMAs, frees its tensor memory and
+// returns.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace tpmlp {
+
+constexpr int kBM = 128;        // output rows per tile = TMEM lanes
+constexpr int kBK = 64;         // reduction depth per stage: one 128-byte swizzle row of bf16
+constexpr int kUmmaK = 16;      // reduction depth of one kind::f16 MMA
+constexpr int kNumThreads = 192;
+constexpr int kEpiWarps = 4;
+
+enum class Mode : int { kGemm1 = 1, kGemm2 = 2 };
+
+// Wait sites recorded in the status word when a bounded wait gives up: (mode << 8) | site.
+enum : int { kSiteProducer = 1, kSiteMmaAccum = 2, kSiteMmaFull = 3, kSiteEpilogue = 4 };
+
+struct GemmArgs {
+    int M;          // valid output rows (token rows)
+    int ldo;        // output columns = row pitch of `out` in elements
+    int f;          // shard width
+    int k;          // shard count
+    int kb_tile;    // 64-deep reduction blocks per output tile
+    int kb_shard;   // 64-deep reduction blocks per shard (GEMM2)
+    int m_blocks;   // ceil(M / kBM)
+    int n_blocks;   // ldo / BN
+    int num_tiles;  // m_blocks * n_blocks
+    int group_m;    // tile rasterisation: this many row blocks share a column sweep
+    const float* bias;  // [ldo] fp32
+    void* out;          // [M][ldo] bf16 or fp32
+    int* status;        // device status word
+};
+
+// Shared-memory matrix descriptor for a K-major operand tile stored as rows of 64 bf16
+// (128 bytes) with the 128-byte swizzle, 8-row swizzle atoms 1024 bytes apart (the layout
+// TMA writes with CU_TENSOR_MAP_SWIZZLE_128B and a 64-element inner box).
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4 (not used for swizzled K-major; 1)
+//   bits 32-45  stride-dimension byte offset >> 4 (1024 B between 8-row groups)
+//   bits 46-47  descriptor version (1 for tcgen05)
+//   bits 49-51  base offset (0: atoms are 1024-byte aligned)
+//   bits 61-63  swizzle mode (2 = 128-byte swizzle)
+__device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9 and
+// 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+template <int BN, int STAGES>
+struct GemmSmem {
+    static constexpr uint32_t kABytes = kBM * kBK * 2;
+    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kCtrlBytes = 8 * (2 * STAGES + 5) + 8;
+    static constexpr uint32_t kTotal = 1024 /*alignment slack*/ + STAGES * kStageBytes + kCtrlBytes;
+    static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; power of two >= 32
+};
+
+// GeLU, exact form a * Phi(a) = a/2 * (1 + erf(a / sqrt 2)), with CUDA's erff.
+__device__ __forceinline__ float gelu_erf(float a) {
+    return 0.5f * a * (1.0f + erff(a * 0.70710678118654752440f));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// One 32-column slice of one output row: + bias, (GeLU), convert, store.
+template <Mode MODE, bool OUT_F32>
+__device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const float* __restrict__ bias,
+                                               void* __restrict__ out, int row, int M, int ldo,
+                                               int col) {
+    float x[32];
+    const float4* b4 = reinterpret_cast<const float4*>(bias + col);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float4 bb = __ldg(b4 + j);
+        x[4 * j + 0] = __uint_as_float(v[4 * j + 0]) + bb.x;
+        x[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + bb.y;
+        x[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + bb.z;
+        x[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + bb.w;
+    }
+    if constexpr (MODE == Mode::kGemm1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = gelu_erf(x[j]);
+    }
+    if (row >= M) return;
+    if constexpr (OUT_F32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) +
+                                                static_cast<size_t>(row) * ldo + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) +
+                                              static_cast<size_t>(row) * ldo + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]),
+                                pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
+                                pack_bf16x2(x[8 * j + 4], x[8 * j + 5]),
+                                pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+    }
+}
+
+__device__ __forceinline__ void decode_tile(const GemmArgs& a, int t, int& m_blk, int& n_blk) {
+    const int per_group = a.group_m * a.n_blocks;
+    const int g = t / per_group;
+    const int first_m = g * a.group_m;
+    const int gm = min(a.m_blocks - first_m, a.group_m);
+    const int local = t - g * per_group;
+    m_blk = first_m + local % gm;
+    n_blk = local / gm;
+}
+
+// A: GEMM1 -> X [M][H] (2-D map, box 64 x 128); GEMM2 -> Y [M][F] (2-D map, box 64 x 128).
+// B: GEMM1 -> W1p [k][f][H] (3-D map, box 64 x BN x 1); GEMM2 -> W2p [k][H][f] (same box).
+template <int BN, int STAGES, Mode MODE, bool OUT_F32>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    tpmlp_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+    using L = GemmSmem<BN, STAGES>;
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+    constexpr int kCode = static_cast<int>(MODE) << 8;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    // control block after the stage ring
+    const uint32_t ctrl = base + STAGES * L::kStageBytes;
+    auto full_bar = [&](int s) { return ctrl + 8u * s; };
+    auto empty_bar = [&](int s) { return ctrl + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return ctrl + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return ctrl + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = ctrl + 8u * (2 * STAGES + 4);
+    uint32_t* const tmem_holder =
+        reinterpret_cast<uint32_t*>(base_ptr + STAGES * L::kStageBytes + 8 * (2 * STAGES + 5));
+    volatile uint32_t* const abort_flag = tmem_holder + 1;
+
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), kEpiWarps);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), L::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+                int m_blk, n_blk;
+                decode_tile(args, t, m_blk, n_blk);
+                const int m0 = m_blk * kBM;
+                const int n0 = n_blk * BN;
+                const int shard1 = (MODE == Mode::kGemm1) ? n0 / args.f : 0;
+                const int n_in_shard1 = n0 - shard1 * args.f;
+                for (int kb = 0; kb < args.kb_tile; ++kb) {
+                    if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status,
+                                        kCode | kSiteProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * L::kStageBytes;
+                    const uint32_t sb = sa + L::kABytes;
+                    ptx::mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
+                    if constexpr (MODE == Mode::kGemm1) {
+                        ptx::tma_load_2d(sa, &tmA, full_bar(stage), kb * kBK, m0);
+                        ptx::tma_load_3d(sb, &tmB, full_bar(stage), kb * kBK, n_in_shard1, shard1);
+                    } else {
+                        const int i = kb / args.kb_shard;               // shard of this block
+                        const int kk = (kb - i * args.kb_shard) * kBK;  // offset inside shard i
+                        ptx::tma_load_2d(sa, &tmA, full_bar(stage), i * args.f + kk, m0);
+                        ptx::tma_load_3d(sb, &tmB, full_bar(stage), kk, n0, i);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // wait for the copies still in flight before the CTA may exit
+                for (uint32_t s = 0; s < STAGES && s < issued; ++s) {
+                    const uint32_t last = s + ((issued - 1 - s) / STAGES) * STAGES;
+                    ptx::mbar_wait_drain(full_bar(s), (last / STAGES) & 1u);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+                if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status,
+                                    kCode | kSiteMmaAccum)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < args.kb_tile; ++kb) {
+                    if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, args.status,
+                                        kCode | kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = base + stage * L::kStageBytes;
+                    const uint64_t da = sdesc_k128(sa);
+                    const uint64_t db = sdesc_k128(sa + L::kABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        // advance both descriptors by kk * 16 elements = 32 bytes (>> 4 = 2)
+                        ptx::mma_bf16_ss(d_tmem, da + 2u * kk, db + 2u * kk, kIdesc,
+                                         (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty_bar(stage));  // stage free once these MMAs finish
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull_bar(acc));  // accumulator complete
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // every MMA this thread issued has completed before tensor memory is released
+            ptx::mma_commit(drain_bar);
+            ptx::mbar_wait_drain(drain_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lanes [32q, 32q+32) = tile rows this warp may read
+        uint32_t acc = 0, acc_phase = 0;
+        for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+            int m_blk, n_blk;
+            decode_tile(args, t, m_blk, n_blk);
+            const int m0 = m_blk * kBM;
+            const int n0 = n_blk * BN;
+            bool ok = ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status,
+                                     kCode | kSiteEpilogue);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            ptx::tc_fence_after();
+            const int row = m0 + q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(taddr + c, v);
+                ptx::tmem_wait_ld(v);
+                if (c + 32 == BN) {
+                    // all of this warp's accumulator columns are in registers: hand it back
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+                }
+                epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo,
+                                              n0 + c);
+            }
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+}  // namespace tpmlp

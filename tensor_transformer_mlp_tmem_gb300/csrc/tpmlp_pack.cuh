@@ -1,0 +1,51 @@
+// The shard packer: lays the weights out the way the GEMM kernel's TMA loads want them.
+//
+// The pages split the first weight by columns and the second by rows into k equal,
+// contiguous pieces (AI大模型分布式训练 §2.1-2.2: W [hidden, ffn] into k pieces of
+// [hidden, ffn/k]; the row-parallel weight into [in/k, out]); here every piece is also
+// transposed so that its reduction dimension is contiguous (K-major), which is what the
+// tensor cores read with the 128-byte swizzle:
+//
+//   W1 [H][F]  ->  W1p [k][f][H]   W1p[i][j][h] = W1[h][i f + j]   (column shard i, transposed)
+//   W2 [F][H]  ->  W2p [k][H][f]   W2p[i][n][j] = W2[i f + j][n]   (row shard i, transposed)
+//   b1, b2 (bf16) -> fp32 copies (b1 keeps the shard-major order: slice i = b1[i f, (i+1) f))
+//
+// Packing is a pure permutation of bits (plus an exact bf16 -> fp32 widening of the biases).
+#pragma once
+
+#include <cstdint>
+
+namespace tpmlp {
+
+constexpr int kTransposeTile = 64;
+
+// out[b][c][r] = in[b][r][c] for a batch of R x C bf16 matrices (bit copies).
+__global__ void __launch_bounds__(256)
+    transpose_bf16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int R, int C,
+                          long long in_batch_stride, long long out_batch_stride) {
+    __shared__ uint16_t tile[kTransposeTile][kTransposeTile + 2];
+    const long long b = blockIdx.z;
+    const int r0 = blockIdx.y * kTransposeTile;
+    const int c0 = blockIdx.x * kTransposeTile;
+    const uint16_t* src = in + b * in_batch_stride;
+    uint16_t* dst = out + b * out_batch_stride;
+    const int tx = threadIdx.x;  // 0..63
+    for (int i = threadIdx.y; i < kTransposeTile; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + tx;
+        if (r < R && c < C) tile[i][tx] = src[static_cast<size_t>(r) * C + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < kTransposeTile; i += blockDim.y) {
+        const int c = c0 + i, r = r0 + tx;
+        if (c < C && r < R) dst[static_cast<size_t>(c) * R + r] = tile[tx][i];
+    }
+}
+
+__global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ in, float* __restrict__ out,
+                                   long long n) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        out[i] = __uint_as_float(static_cast<uint32_t>(in[i]) << 16);
+}
+
+}  // namespace tpmlp
