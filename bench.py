@@ -1,0 +1,394 @@
+"""Benchmark of the tensor-parallel MLP block forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 7b] [--impl reference]
+
+A step is one forward pass of the whole block -- the column-parallel GEMM with its fused
+bias + GeLU, then the row-parallel GEMM whose accumulator sums all k shards and adds b2 --
+over one batch of seeded synthetic input already resident in HBM. L2 is flushed (a
+256 MiB write) between timed steps, outside the timed events. The printed JSON line
+carries throughput (TFLOP/s of the two contractions, tokens/s), the roofline of the
+dominant kernel, an end-to-end figure through the host-buffer entry point, SM clocks
+sampled during the timed region, and the fp64 CPU oracle timed on a bounded sample of
+the same workload on this host's cores.
+
+With N > 1 (torchrun), every rank runs an independent replica on its own GPU (the block
+needs no exchange between replicas); ranks meet only at the timing barriers.
+
+``--impl reference`` times the fp64 CPU oracle as the reference arm on the same workload
+(rank 0 only; each step a bounded sample of token rows).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "TP-MLP forward TFLOP/s and tokens/s on 1 GB300; % of dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def workload_config(w: synth.Workload, extra=None) -> dict:
+    cfg = {
+        "workload": f"{w.name} TP-MLP: X [B={w.B},S={w.S},H={w.H}] bf16, W1 [{w.H},{w.F}], "
+                    f"W2 [{w.F},{w.H}], erf GeLU, k={w.k} shards, seeded synthetic",
+        "B": w.B, "S": w.S, "M": w.M, "H": w.H, "F": w.F, "k": w.k, "seed": w.seed,
+        "flops_per_step": w.flops,
+        "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+    }
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception as e:  # no nvidia-smi: record nothing
+            log("clock sampling unavailable:", e)
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for ln in fh:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        mx = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[0] >= 0.5 * mx] or rows
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[2])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def oracle_sample(w: synth.Workload, d: dict, budget_s: float, max_rows: int):
+    """Time the fp64 oracle on a bounded, seeded sample of token rows of the workload."""
+    import oracle
+    cal_rows = synth.sample_rows(w.M, min(max(oracle.threads(), 4), max_rows))
+    t0 = time.perf_counter()
+    oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=cal_rows)
+    t_cal = time.perf_counter() - t0
+    per_row = t_cal / len(cal_rows)
+    R = int(max(len(cal_rows), min(max_rows, budget_s / max(per_row, 1e-9))))
+    rows = synth.sample_rows(w.M, R)
+    t0 = time.perf_counter()
+    oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = len(rows) * 4 * w.H * w.F
+    return {"rows": len(rows), "seconds": dt, "tflops": flops / dt / 1e12,
+            "tokens_per_s": len(rows) / dt, "cores": oracle.threads()}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, w: synth.Workload):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    d = synth.workload_inputs(w)
+    steps, warm = args.steps, args.warmup
+    budget = args.reference_budget_s
+    # rows per step so that the whole run stays within the budget
+    cal_rows = synth.sample_rows(w.M, max(oracle.threads(), 4))
+    t0 = time.perf_counter()
+    oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=cal_rows)
+    per_row = (time.perf_counter() - t0) / len(cal_rows)
+    R = int(max(1, min(w.M, budget / (steps + warm) / max(per_row, 1e-9))))
+    rows = synth.sample_rows(w.M, R)
+    for _ in range(warm):
+        oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=rows)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=rows)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    flops = len(rows) * 4 * w.H * w.F
+    value = flops / t / 1e12
+    sample = (f"{len(rows)} of {w.M} token rows per step (seeded spread incl. first/last), full "
+              f"weights, all {w.H} outputs; fp64 oracle, OpenMP over rows")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "tokens_per_s": len(rows) / t,
+        "config": workload_config(w, {"parallelism": "host cores (oracle)", "rows_per_step": len(rows)}),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, w: synth.Workload):
+    import torch
+    import tensor_transformer_mlp_tmem_gb300 as tp
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    d = synth.workload_inputs(w)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    X = to_dev(d["X"]).view(w.B, w.S, w.H)
+    W1, b1, W2, b2 = (to_dev(d[n]) for n in ("W1", "b1", "W2", "b2"))
+    Z = torch.empty((w.B, w.S, w.H), dtype=torch.bfloat16, device=dev)
+    Y = torch.empty((w.M, w.F), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    mlp = tp.TPMLP(w.H, w.F, w.k)
+    mlp.pack(W1, b1, W2, b2)
+    mlp.reserve(w.M)
+    torch.cuda.synchronize(dev)
+    del W1, W2  # raw weights are not needed after packing
+
+    def step(ev=None):
+        # one pass of the whole block: GEMM1 (+b1, GeLU) then GEMM2 (sum over shards, +b2)
+        if ev is not None:
+            ev[0].record(stream)
+        tp.tpmlp_gemm1(mlp.ctx, X, w.M, Y, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        tp.tpmlp_gemm2(mlp.ctx, Y, w.M, Z, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    rc, detail = mlp.status()
+    if rc != tp.TPMLP_OK:
+        raise RuntimeError(f"device status after warm-up: {detail:#x}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = mlp.launches
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall = time.perf_counter() - t_wall0
+    launches = mlp.launches - launches0
+    clk = clocks.stop()
+    rc, detail = mlp.status()
+    if rc != tp.TPMLP_OK:
+        raise RuntimeError(f"device status after timed steps: {detail:#x}")
+
+    g1 = [e[0].elapsed_time(e[1]) for e in evs]
+    g2 = [e[1].elapsed_time(e[2]) for e in evs]
+    st = [a + b for a, b in zip(g1, g2)]
+    ms_step = statistics.mean(st)
+    if pg is not None:
+        t = torch.tensor([ms_step, t_wall], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_step, t_wall = float(t[0]), float(t[1])
+
+    # ---- end to end through the host-buffer entry point (pinned host memory)
+    Xh = torch.from_numpy(np.ascontiguousarray(d["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    Zh = torch.empty((w.M, w.H), dtype=torch.bfloat16).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        tp.tpmlp_forward_host(mlp.ctx, Xh, w.B, w.S, Zh, stream)
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        tp.tpmlp_forward_host(mlp.ctx, Xh, w.B, w.S, Zh, stream)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if pg is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t[0])
+    rc, detail = mlp.status()
+    if rc != tp.TPMLP_OK:
+        raise RuntimeError(f"device status after e2e steps: {detail:#x}")
+
+    flops_step = w.flops
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    tokens = world * w.M / (ms_step * 1e-3)
+    peaks, peak_src = load_peaks()
+    peak_burst = peaks["bf16_tflops"]
+    peak_sust = peaks.get("bf16_tflops_sustained", peak_burst)
+    kern = {"gemm1": statistics.mean(g1), "gemm2": statistics.mean(g2)}
+    dom = max(kern, key=kern.get)
+    achieved = (flops_step / 2) / (kern[dom] * 1e-3) / 1e12
+    # the kernels run back to back for the whole timed region (seconds): sustained peak
+    peak = peak_sust
+    traffic = measured_traffic(w.name, dom)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) X, N(0,1/fan_in) weights, N(0,0.02^2) biases)",
+        "tokens_per_s": tokens,
+        "pct_of_dense_bf16_peak": 100.0 * (value / world) / peak,
+        "pct_of_dense_bf16_peak_burst": 100.0 * (value / world) / peak_burst,
+        "wall_ms_per_step_incl_l2_flush": t_wall * 1e3 / args.steps,
+        "kernel_ms": kern,
+        "config": workload_config(w, {"parallelism": "replicas" if world > 1 else "single GPU",
+                                      "output": "bf16"}),
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS bf16 loop under "
+                                    f"the power cap)", "traffic": traffic},
+        "e2e": {"value": world * flops_step / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": w.M * w.H * 2, "d2h_bytes_per_step": w.M * w.H * 2,
+                "ms_per_step": e2e_s * 1e3, "api": "tpmlp_forward_host (pinned host X, Z)"},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(w, d, args.cpu_budget_s, args.cpu_max_rows)
+        line["cpu_baseline"] = {
+            "value": cb["tflops"], "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
+            "sample": f"{cb['rows']} of {w.M} token rows (seeded spread incl. first/last), full "
+                      f"weights, all {w.H} outputs; {cb['seconds']:.1f} s; fp64 plain loops, "
+                      f"OpenMP over rows",
+            "tokens_per_s": cb["tokens_per_s"]}
+    mlp.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    (profiles/ncu_traffic.json-like lines in profiles/*.md: `traffic <workload> <kernel> <bytes>`),
+    or None when no capture of the current kernel exists."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, fn)) as fh:
+            for ln in fh:
+                parts = ln.strip().strip("`").split()
+                if len(parts) == 4 and parts[0] == "traffic" and parts[1] == workload \
+                        and parts[2] == kernel:
+                    try:
+                        return float(parts[3])
+                    except ValueError:
+                        return None
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="7b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--k", type=int, default=None, help="override the shard count")
+    ap.add_argument("--impl", default="tpmlp", choices=["tpmlp", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--cpu-max-rows", type=int, default=4096)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = synth.WORKLOADS[args.workload]
+    if args.k is not None:
+        w = synth.Workload(w.name, w.B, w.S, w.H, w.F, args.k, w.seed)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -102,7 +102,8 @@ TPMLP_API int tpmlp_reserve(tpmlp_ctx *ctx, int64_t max_tokens);
  *   Z   device [B, S, H], bf16 (or fp32 with TPMLP_FLAG_Z_FP32); must not overlap X
  * Two kernel launches on `stream`: the first GEMM with its fused bias + GeLU epilogue
  * writing Y [M, F] bf16 into the context's buffer, then the second GEMM, which sums all k
- * shards' partials in one fp32 accumulator and adds b2 once. B*S == 0 is a no-op.
+ * shards' partials in one fp32 accumulator and adds b2 once. B*S == 0 is a no-op (X and
+ * Z may then be NULL).
  * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, OOM (growing Y), CUDA. A pipeline timeout
  * inside a kernel is reported by tpmlp_get_status, not here.
  */
@@ -122,6 +123,7 @@ TPMLP_API int tpmlp_forward_host(tpmlp_ctx *ctx, const void *X_host, int64_t B, 
  * The first step alone (column-parallel GEMM of every shard + b1 + GeLU):
  *   Y[m, i f + j] = GeLU(b1[i f + j] + sum_h X[m, h] W1[h, i f + j])   rounded to bf16
  *   X device bf16 [M, H]; Y device bf16 [M, F] (shard i in columns [i f, (i+1) f)).
+ * M == 0 is a no-op (pointers may then be NULL).
  * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, CUDA.
  */
 TPMLP_API int tpmlp_gemm1(tpmlp_ctx *ctx, const void *X, int64_t M, void *Y, void *stream);
@@ -131,6 +133,7 @@ TPMLP_API int tpmlp_gemm1(tpmlp_ctx *ctx, const void *X, int64_t M, void *Y, voi
  * pages' All-Reduce -- done in the fp32 accumulator, + b2):
  *   Z[m, n] = b2[n] + sum_i sum_{j<f} Y[m, i f + j] W2[i f + j, n]
  *   Y device bf16 [M, F]; Z device [M, H] (bf16, or fp32 with TPMLP_FLAG_Z_FP32).
+ * M == 0 is a no-op (pointers may then be NULL).
  * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, CUDA.
  */
 TPMLP_API int tpmlp_gemm2(tpmlp_ctx *ctx, const void *Y, int64_t M, void *Z, void *stream);

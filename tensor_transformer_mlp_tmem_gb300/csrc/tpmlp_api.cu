@@ -317,31 +317,33 @@ int tpmlp_reserve(tpmlp_ctx* c, int64_t max_tokens) {
 int tpmlp_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, void* stream) {
     int rc = check_ctx(c);
     if (rc) return rc;
-    if (!X || !Y || M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (M == 0) return TPMLP_OK;
+    if (!X || !Y) return TPMLP_ERR_INVALID_ARG;
     if (M > (int64_t(1) << 31)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(X) || !aligned16(Y)) return TPMLP_ERR_MISALIGNED;
-    if (M == 0) return TPMLP_OK;
     return run_gemm1(c, X, M, Y, static_cast<cudaStream_t>(stream));
 }
 
 int tpmlp_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, void* stream) {
     int rc = check_ctx(c);
     if (rc) return rc;
-    if (!Y || !Z || M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (M == 0) return TPMLP_OK;
+    if (!Y || !Z) return TPMLP_ERR_INVALID_ARG;
     if (M > (int64_t(1) << 31)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(Y) || !aligned16(Z)) return TPMLP_ERR_MISALIGNED;
-    if (M == 0) return TPMLP_OK;
     return run_gemm2(c, Y, M, Z, static_cast<cudaStream_t>(stream));
 }
 
 int tpmlp_forward(tpmlp_ctx* c, const void* X, int64_t B, int64_t S, void* Z, void* stream) {
     int rc = check_ctx(c);
     if (rc) return rc;
-    if (!X || !Z) return TPMLP_ERR_INVALID_ARG;
     if ((rc = check_tokens(B, S))) return rc;
-    if (!aligned16(X) || !aligned16(Z)) return TPMLP_ERR_MISALIGNED;
     const int64_t M = B * S;
     if (M == 0) return TPMLP_OK;
+    if (!X || !Z) return TPMLP_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Z)) return TPMLP_ERR_MISALIGNED;
     if ((rc = ensure_y(c, M))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((rc = run_gemm1(c, X, M, c->Y, s))) return rc;
@@ -352,10 +354,10 @@ int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, v
                        void* stream) {
     int rc = check_ctx(c);
     if (rc) return rc;
-    if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
     if ((rc = check_tokens(B, S))) return rc;
     const int64_t M = B * S;
     if (M == 0) return TPMLP_OK;
+    if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
     if (M > c->stage_rows) {
         TPMLP_CUDA(c, cudaDeviceSynchronize());
         if (c->Xs) cudaFree(c->Xs);

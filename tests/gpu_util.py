@@ -48,7 +48,7 @@ class DeviceView:
 
     def __init__(self, ptr: int, shape, typestr: str):
         self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
-                                         "data": (ptr, True), "version": 3, "strides": None}
+                                         "data": (ptr, False), "version": 3, "strides": None}
 
 
 def device_tensor(ptr: int, shape, dtype: str) -> torch.Tensor:

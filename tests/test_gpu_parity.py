@@ -36,9 +36,9 @@ def test_pack_layout_is_exact_permutation(lib, H, F, k):
         torch.cuda.synchronize()
         p, n = tp.tpmlp_packed_buffer(mlp.ctx, 0)
         assert n == H * F * 2
-        W1p = device_tensor(p, (k, f, H), "u16").cpu().numpy()
+        W1p = device_tensor(p, (k, f, H), "i16").cpu().numpy().view(np.uint16)
         p, _ = tp.tpmlp_packed_buffer(mlp.ctx, 1)
-        W2p = device_tensor(p, (k, H, f), "u16").cpu().numpy()
+        W2p = device_tensor(p, (k, H, f), "i16").cpu().numpy().view(np.uint16)
         p, _ = tp.tpmlp_packed_buffer(mlp.ctx, 2)
         b1p = device_tensor(p, (F,), "f32").cpu().numpy()
         p, _ = tp.tpmlp_packed_buffer(mlp.ctx, 3)
