@@ -153,6 +153,30 @@ TPMLP_API int tpmlp_get_status(tpmlp_ctx *ctx, void *stream, int32_t *detail);
  */
 TPMLP_API int tpmlp_packed_buffer(const tpmlp_ctx *ctx, int32_t which, const void **ptr, int64_t *bytes);
 
+/*
+ * Forward pass that allocates nothing (no counterpart on the pages; an addition for
+ * callers that cannot call cudaMalloc when they run the block -- e.g. a serving process
+ * whose own allocator has taken the device's free memory at start-up, or a latency-critical
+ * stream on which an allocation's implicit device synchronisation is not acceptable).
+ *
+ * Same arguments, result and errors as tpmlp_forward, but the intermediate activations
+ * Y [B*S, F] (bf16) are written to a fixed array compiled into the library,
+ * TPMLP_NOALLOC_SCRATCH_BYTES long, instead of the context's buffer. This call makes no
+ * cudaMalloc/cudaFree and no other allocating call. Every GPU that loads the library holds
+ * that array until the process exits.
+ *  - B*S*F*2 > TPMLP_NOALLOC_SCRATCH_BYTES is rejected with TPMLP_ERR_UNSUPPORTED_SHAPE
+ *    (tpmlp_last_error states the sizes); nothing is launched.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *    with the context's device current; make that first call before any stream capture.
+ *  - All calls in the process share the one array per device, and it keeps the previous
+ *    call's contents (nothing in it needs to start at zero). Calls whose kernels overlap on
+ *    the GPU -- on different streams, or from different contexts -- race on it; serialise them.
+ * The weights still come from a context created and packed beforehand.
+ */
+#define TPMLP_NOALLOC_SCRATCH_BYTES (32ll << 20) /* 32 MiB */
+TPMLP_API int tpmlp_forward_noalloc(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z,
+                                    void *stream);
+
 /* Release everything the context owns (synchronises its device first). NULL is a no-op. */
 TPMLP_API void tpmlp_destroy(tpmlp_ctx *ctx);
 

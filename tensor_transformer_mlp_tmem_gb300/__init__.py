@@ -17,6 +17,7 @@ import os
 __all__ = [
     "TPMLP", "TpmlpError", "load_library", "library_path",
     "tpmlp_create", "tpmlp_pack_shards", "tpmlp_reserve", "tpmlp_forward", "tpmlp_forward_host",
+    "tpmlp_forward_noalloc", "TPMLP_NOALLOC_SCRATCH_BYTES",
     "tpmlp_gemm1", "tpmlp_gemm2", "tpmlp_get_status", "tpmlp_packed_buffer", "tpmlp_destroy",
     "tpmlp_strerror", "tpmlp_last_error", "tpmlp_launch_count",
     "TPMLP_OK", "TPMLP_ERR_INVALID_ARG", "TPMLP_ERR_UNSUPPORTED_SHAPE", "TPMLP_ERR_NOT_PACKED",
@@ -34,6 +35,7 @@ TPMLP_ERR_DEVICE_TIMEOUT = -6
 TPMLP_ERR_ARCH = -7
 TPMLP_ERR_MISALIGNED = -8
 TPMLP_FLAG_Z_FP32 = 0x1
+TPMLP_NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's fixed scratch for tpmlp_forward_noalloc
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 
@@ -71,6 +73,7 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_reserve": ([vp, i64], ctypes.c_int),
         "tpmlp_forward": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_forward_host": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_forward_noalloc": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_gemm1": ([vp, vp, i64, vp, vp], ctypes.c_int),
         "tpmlp_gemm2": ([vp, vp, i64, vp, vp], ctypes.c_int),
         "tpmlp_get_status": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
@@ -150,6 +153,14 @@ def tpmlp_forward(ctx: int, X, B: int, S: int, Z, stream=None) -> None:
 def tpmlp_forward_host(ctx: int, X_host, B: int, S: int, Z_host, stream=None) -> None:
     _check(load_library().tpmlp_forward_host(ctx, _ptr(X_host), B, S, _ptr(Z_host),
                                              _stream(stream)), "tpmlp_forward_host", ctx)
+
+
+def tpmlp_forward_noalloc(ctx: int, X, B: int, S: int, Z, stream=None) -> None:
+    """tpmlp_forward without any allocation: Y goes to the library's fixed device array
+    (B*S*F*2 <= TPMLP_NOALLOC_SCRATCH_BYTES). For callers that cannot allocate device memory
+    when they run the block. Calls that overlap on the GPU share that array and race."""
+    _check(load_library().tpmlp_forward_noalloc(ctx, _ptr(X), B, S, _ptr(Z), _stream(stream)),
+           "tpmlp_forward_noalloc", ctx)
 
 
 def tpmlp_gemm1(ctx: int, X, M: int, Y, stream=None) -> None:

@@ -439,3 +439,72 @@ const char* tpmlp_last_error(const tpmlp_ctx* c) { return c ? c->last_error.c_st
 int64_t tpmlp_launch_count(const tpmlp_ctx* c) { return c ? c->launches : 0; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free forward pass.
+//
+// Some callers cannot call cudaMalloc at the point where they run the block: a serving
+// process that hands all free device memory to its own allocator at start-up (caches,
+// memory pools) and forbids later driver allocations, or code on a latency-critical path
+// where an allocation would implicitly synchronise the device. For them the intermediate
+// activations Y live in one fixed device array compiled into this library instead of a
+// buffer the context allocates. The array is TPMLP_NOALLOC_SCRATCH_BYTES long; every GPU
+// that loads the library holds it until the process exits.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_y[TPMLP_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+// The device address of g_noalloc_y on the context's device. In host code the array's
+// name is only a host-side stand-in, so the address is looked up once per device, with
+// that device current, and cached.
+int noalloc_scratch(tpmlp_ctx* c, void** out) {
+    if (c->device < 0 || c->device >= kNoallocMaxDevices) return TPMLP_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[c->device]) {
+        int cur = -1;
+        TPMLP_CUDA(c, cudaGetDevice(&cur));
+        if (cur != c->device) {
+            c->last_error = "tpmlp_forward_noalloc: the context's device must be current";
+            return TPMLP_ERR_INVALID_ARG;
+        }
+        void* p = nullptr;
+        TPMLP_CUDA(c, cudaGetSymbolAddress(&p, g_noalloc_y));
+        if (!p) {
+            c->last_error = "cudaGetSymbolAddress returned a null scratch address";
+            return TPMLP_ERR_CUDA;
+        }
+        g_noalloc_ptr[c->device] = p;
+    }
+    *out = g_noalloc_ptr[c->device];
+    return TPMLP_OK;
+}
+
+}  // namespace
+
+extern "C" int tpmlp_forward_noalloc(tpmlp_ctx* c, const void* X, int64_t B, int64_t S, void* Z,
+                                     void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if ((rc = check_tokens(B, S))) return rc;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if (!X || !Z) return TPMLP_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Z)) return TPMLP_ERR_MISALIGNED;
+    const int64_t y_bytes = M * c->F * 2;
+    if (y_bytes > static_cast<int64_t>(TPMLP_NOALLOC_SCRATCH_BYTES)) {
+        c->last_error = "tpmlp_forward_noalloc: Y needs " + std::to_string(y_bytes) +
+                        " bytes (B*S*F*2) but the static scratch holds " +
+                        std::to_string(static_cast<int64_t>(TPMLP_NOALLOC_SCRATCH_BYTES)) +
+                        "; use tpmlp_forward or fewer tokens per call";
+        return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    }
+    void* y = nullptr;
+    if ((rc = noalloc_scratch(c, &y))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = run_gemm1(c, X, M, y, s))) return rc;
+    return run_gemm2(c, y, M, Z, s);
+}

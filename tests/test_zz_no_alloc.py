@@ -1,0 +1,63 @@
+"""tpmlp_forward_noalloc: the forward pass for callers that cannot allocate device memory
+when they run the block (their allocator owns the free memory, or an allocation's implicit
+synchronisation is not acceptable on their stream). Its intermediate activations live in a
+fixed array compiled into the library instead of a context buffer.
+
+Checked through the C ABI against tpmlp_forward on two calls in a row (different inputs, so
+the second call runs on top of the first call's leftover scratch contents), plus the size
+limit and the no-allocation property. This file is collected last on purpose."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import tensor_transformer_mlp_tmem_gb300 as tp
+from gpu_util import assert_close, inputs_on_device, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def test_forward_noalloc_matches_forward_twice(lib):
+    H, F, k, M = 256, 1024, 4, 300
+    d = synth.make_inputs(H, F, M, 91)
+    dd = inputs_on_device(d)
+    with tp.TPMLP(H, F, k) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        for call, seed in enumerate((92, 93)):
+            X = to_dev(synth.normal_bf16(seed, synth.STREAM_X, (M, H), 1.0)).view(1, M, H)
+            Z_ref = torch.empty((1, M, H), dtype=torch.bfloat16, device="cuda")
+            Z_na = torch.full((1, M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+            tp.tpmlp_forward(mlp.ctx, X, 1, M, Z_ref)
+            torch.cuda.synchronize()
+            free0 = torch.cuda.mem_get_info()[0]
+            tp.tpmlp_forward_noalloc(mlp.ctx, X, 1, M, Z_na)
+            torch.cuda.synchronize()
+            free1 = torch.cuda.mem_get_info()[0]
+            rc, detail = mlp.status()
+            assert rc == tp.TPMLP_OK, f"call {call}: device status {detail:#x}"
+            if call == 1:  # the first call may have loaded the array with the module
+                assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+            assert_close(to_f64(Z_na.view(M, H)), to_f64(Z_ref.view(M, H)),
+                         what=f"noalloc call {call} vs tpmlp_forward")
+
+
+def test_forward_noalloc_rejects_oversize(lib):
+    H, F, k = 256, 1024, 4
+    M = tp.TPMLP_NOALLOC_SCRATCH_BYTES // (F * 2) + 1  # one token row beyond the limit
+    d = synth.make_inputs(H, F, 1, 94)
+    dd = inputs_on_device(d)
+    X = torch.zeros((1, M, H), dtype=torch.bfloat16, device="cuda")
+    Z = torch.zeros((1, M, H), dtype=torch.bfloat16, device="cuda")
+    with tp.TPMLP(H, F, k) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        n0 = mlp.launches
+        with pytest.raises(tp.TpmlpError) as e:
+            tp.tpmlp_forward_noalloc(mlp.ctx, X, 1, M, Z)
+        assert e.value.status == tp.TPMLP_ERR_UNSUPPORTED_SHAPE
+        assert "static scratch" in str(e.value)
+        assert mlp.launches == n0
+        # the largest size that fits still runs
+        Mmax = M - 1
+        tp.tpmlp_forward_noalloc(mlp.ctx, X[:, :Mmax], 1, Mmax, Z[:, :Mmax])
+        torch.cuda.synchronize()
+        assert mlp.status()[0] == tp.TPMLP_OK
