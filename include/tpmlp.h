@@ -57,7 +57,9 @@ typedef enum {
 } tpmlp_status;
 
 /* Flags for tpmlp_create. */
-#define TPMLP_FLAG_Z_FP32 0x1u /* Z is written as fp32 instead of bf16 */
+#define TPMLP_FLAG_Z_FP32 0x1u    /* Z is written as fp32 instead of bf16 */
+#define TPMLP_FLAG_SINGLE_SM 0x2u /* use only the single-SM kernel (128-row tiles), never the
+                                     CTA-pair kernel (256 x 256 tiles on two SMs); same results */
 
 /*
  * Create a context for one block shape on the current CUDA device.
@@ -68,7 +70,7 @@ typedef enum {
  *            parallel degree; shards are contiguous, equal column blocks of W1 and the
  *            matching row blocks of W2 -- AI大模型分布式训练 §2.1 splits W into
  *            [hidden, ffn/k] pieces)
- *   flags    0 or TPMLP_FLAG_Z_FP32
+ *   flags    0, or TPMLP_FLAG_Z_FP32 and/or TPMLP_FLAG_SINGLE_SM
  * Allocates the packed-weight buffers (2*H*F bf16 + (F+H) fp32) and a device status word;
  * the intermediate activation buffer is allocated by tpmlp_reserve or the first forward.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ARCH (device is not sm_103), OOM, CUDA.

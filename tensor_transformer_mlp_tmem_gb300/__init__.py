@@ -22,7 +22,7 @@ __all__ = [
     "tpmlp_strerror", "tpmlp_last_error", "tpmlp_launch_count",
     "TPMLP_OK", "TPMLP_ERR_INVALID_ARG", "TPMLP_ERR_UNSUPPORTED_SHAPE", "TPMLP_ERR_NOT_PACKED",
     "TPMLP_ERR_CUDA", "TPMLP_ERR_OOM", "TPMLP_ERR_DEVICE_TIMEOUT", "TPMLP_ERR_ARCH",
-    "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32",
+    "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM",
 ]
 
 TPMLP_OK = 0
@@ -35,6 +35,7 @@ TPMLP_ERR_DEVICE_TIMEOUT = -6
 TPMLP_ERR_ARCH = -7
 TPMLP_ERR_MISALIGNED = -8
 TPMLP_FLAG_Z_FP32 = 0x1
+TPMLP_FLAG_SINGLE_SM = 0x2
 TPMLP_NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's fixed scratch for tpmlp_forward_noalloc
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -216,10 +217,11 @@ class TPMLP:
         Z = mlp(X)                     # X bf16 [B, S, H] -> Z [B, S, H]
     """
 
-    def __init__(self, H: int, F: int, k: int, z_fp32: bool = False):
+    def __init__(self, H: int, F: int, k: int, z_fp32: bool = False, single_sm: bool = False):
         self.H, self.F, self.k = H, F, k
         self.z_fp32 = z_fp32
-        self.ctx = tpmlp_create(H, F, k, TPMLP_FLAG_Z_FP32 if z_fp32 else 0)
+        flags = (TPMLP_FLAG_Z_FP32 if z_fp32 else 0) | (TPMLP_FLAG_SINGLE_SM if single_sm else 0)
+        self.ctx = tpmlp_create(H, F, k, flags)
 
     def close(self):
         if getattr(self, "ctx", None):

@@ -14,6 +14,7 @@
 
 #include "tpmlp.h"
 #include "tpmlp_gemm.cuh"
+#include "tpmlp_gemm_2sm.cuh"
 #include "tpmlp_pack.cuh"
 
 struct tpmlp_ctx {
@@ -29,7 +30,9 @@ struct tpmlp_ctx {
     float* b1 = nullptr;      // [F]
     float* b2 = nullptr;      // [H]
     bool packed = false;
-    CUtensorMap tmW1{}, tmW2{};
+    CUtensorMap tmW1{}, tmW2{};            // B boxes for the single-SM kernel (BN rows)
+    CUtensorMap tmW1_pair{}, tmW2_pair{};  // B boxes for the CTA-pair kernel (128 rows)
+    bool pair1 = false, pair2 = false;     // GEMM1 / GEMM2 run on CTA pairs
 
     uint16_t* Y = nullptr;  // [y_rows][F] intermediate activations
     int64_t y_rows = 0;
@@ -41,6 +44,26 @@ struct tpmlp_ctx {
     int64_t launches = 0;
     std::string last_error;
 };
+
+// Tile rasterisation: consecutive tiles walk down this many row blocks before moving to the
+// next column block, so the CTAs that run at the same time share operand tiles in L2.
+#ifndef TPMLP_GROUP_M1
+#define TPMLP_GROUP_M1 16
+#endif
+#ifndef TPMLP_GROUP_M2
+#define TPMLP_GROUP_M2 8
+#endif
+// Operand-ring depth for 256-wide output tiles (48 KB per stage).
+#ifndef TPMLP_STAGES_256
+#define TPMLP_STAGES_256 4
+#endif
+// CTA-pair kernel: stages of 32 KB per CTA, and fp32 accumulators of 256 columns each.
+#ifndef TPMLP_PAIR_STAGES
+#define TPMLP_PAIR_STAGES 6
+#endif
+#ifndef TPMLP_PAIR_ACC
+#define TPMLP_PAIR_ACC 2
+#endif
 
 namespace {
 
@@ -126,22 +149,53 @@ template <Mode MODE, bool F32>
 int dispatch_gemm(tpmlp_ctx* c, int bn, const CUtensorMap& a, const CUtensorMap& b,
                   const GemmArgs& args, cudaStream_t s) {
     switch (bn) {
-        case 256: return launch_gemm<256, 4, MODE, F32>(c, a, b, args, s);
+        case 256: return launch_gemm<256, TPMLP_STAGES_256, MODE, F32>(c, a, b, args, s);
         case 128: return launch_gemm<128, 6, MODE, F32>(c, a, b, args, s);
         default: return launch_gemm<64, 8, MODE, F32>(c, a, b, args, s);
     }
 }
 
-GemmArgs base_args(const tpmlp_ctx* c, int64_t M, int ldo, int bn) {
+// Largest number of CTA pairs of this kernel that can be resident at once.
+template <typename Kernel>
+int max_resident_pairs(tpmlp_ctx* c, Kernel kern, uint32_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (c->num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(tpmlp::kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();  // clear; fall back to one pair per two SMs
+        n = c->num_sms / 2;
+    }
+    return n;
+}
+
+template <int STAGES, int NUM_ACC, Mode MODE, bool F32>
+int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                cudaStream_t s) {
+    auto kern = tpmlp::tpmlp_gemm_pair_kernel<STAGES, NUM_ACC, MODE, F32>;
+    constexpr uint32_t smem = tpmlp::PairSmem<STAGES, NUM_ACC>::kTotal;
+    static_assert(smem <= 232448, "shared memory per CTA");
+    TPMLP_CUDA(c, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    static int resident = 0;  // same for every GB300; looked up on first use
+    if (resident <= 0) resident = max_resident_pairs(c, kern, smem);
+    const int pairs = std::min(args.num_tiles, resident);
+    kern<<<2 * pairs, tpmlp::kNumThreads, smem, s>>>(a, b, args);
+    TPMLP_CUDA(c, cudaGetLastError());
+    ++c->launches;
+    return TPMLP_OK;
+}
+
+GemmArgs base_args(const tpmlp_ctx* c, int64_t M, int ldo, int bm, int bn, int group_m) {
     GemmArgs a{};
     a.M = static_cast<int>(M);
     a.ldo = ldo;
     a.f = static_cast<int>(c->f);
     a.k = c->k;
-    a.m_blocks = static_cast<int>((M + tpmlp::kBM - 1) / tpmlp::kBM);
+    a.m_blocks = static_cast<int>((M + bm - 1) / bm);
     a.n_blocks = ldo / bn;
     a.num_tiles = a.m_blocks * a.n_blocks;
-    a.group_m = 8;
+    a.group_m = group_m;
     a.status = c->status;
     return a;
 }
@@ -159,11 +213,16 @@ int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
     const uint32_t box[2] = {tpmlp::kBK, tpmlp::kBM};
     int rc = encode_map(c, &tmX, X, 2, dims, strides, box);
     if (rc) return rc;
-    GemmArgs a = base_args(c, M, static_cast<int>(c->F), c->bn1);
+    const bool pair = c->pair1;
+    GemmArgs a = base_args(c, M, static_cast<int>(c->F), pair ? tpmlp::kPairBM : tpmlp::kBM,
+                           pair ? tpmlp::kPairBN : c->bn1, TPMLP_GROUP_M1);
     a.kb_tile = static_cast<int>(c->H / tpmlp::kBK);
     a.kb_shard = a.kb_tile;
     a.bias = c->b1;
     a.out = Y;
+    if (pair)
+        return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1, false>(c, tmX,
+                                                                                   c->tmW1_pair, a, s);
     return dispatch_gemm<Mode::kGemm1, false>(c, c->bn1, tmX, c->tmW1, a, s);
 }
 
@@ -174,11 +233,20 @@ int run_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, cudaStream_t s) {
     const uint32_t box[2] = {tpmlp::kBK, tpmlp::kBM};
     int rc = encode_map(c, &tmY, Y, 2, dims, strides, box);
     if (rc) return rc;
-    GemmArgs a = base_args(c, M, static_cast<int>(c->H), c->bn2);
+    const bool pair = c->pair2;
+    GemmArgs a = base_args(c, M, static_cast<int>(c->H), pair ? tpmlp::kPairBM : tpmlp::kBM,
+                           pair ? tpmlp::kPairBN : c->bn2, TPMLP_GROUP_M2);
     a.kb_shard = static_cast<int>(c->f / tpmlp::kBK);
     a.kb_tile = a.kb_shard * c->k;
     a.bias = c->b2;
     a.out = Z;
+    if (pair) {
+        if (c->flags & TPMLP_FLAG_Z_FP32)
+            return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, true>(
+                c, tmY, c->tmW2_pair, a, s);
+        return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, false>(
+            c, tmY, c->tmW2_pair, a, s);
+    }
     if (c->flags & TPMLP_FLAG_Z_FP32)
         return dispatch_gemm<Mode::kGemm2, true>(c, c->bn2, tmY, c->tmW2, a, s);
     return dispatch_gemm<Mode::kGemm2, false>(c, c->bn2, tmY, c->tmW2, a, s);
@@ -212,7 +280,7 @@ int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flag
     if (!out) return TPMLP_ERR_INVALID_ARG;
     *out = nullptr;
     if (H <= 0 || F <= 0 || k <= 0) return TPMLP_ERR_INVALID_ARG;
-    if (flags & ~TPMLP_FLAG_Z_FP32) return TPMLP_ERR_INVALID_ARG;
+    if (flags & ~(TPMLP_FLAG_Z_FP32 | TPMLP_FLAG_SINGLE_SM)) return TPMLP_ERR_INVALID_ARG;
     if (H % 64 || F % 64 || F % k || (F / k) % 64) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if (H > (int64_t(1) << 20) || F > (int64_t(1) << 22)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
 
@@ -233,6 +301,9 @@ int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flag
     c->flags = flags;
     c->bn1 = pick_bn(c->f);
     c->bn2 = pick_bn(H);
+    // 256 x 256 tiles on CTA pairs wherever the output width allows it
+    c->pair1 = c->bn1 == 256 && !(flags & TPMLP_FLAG_SINGLE_SM);
+    c->pair2 = c->bn2 == 256 && !(flags & TPMLP_FLAG_SINGLE_SM);
     int rc = TPMLP_OK;
     cudaError_t e;
     if ((e = cudaMalloc(&c->W1p, static_cast<size_t>(H) * F * 2)) != cudaSuccess ||
@@ -294,6 +365,9 @@ int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* 
         const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(c->bn1), 1};
         int rc = encode_map(c, &c->tmW1, c->W1p, 3, dims, strides, box);
         if (rc) return rc;
+        const uint32_t box_pair[3] = {tpmlp::kBK, 128, 1};
+        rc = encode_map(c, &c->tmW1_pair, c->W1p, 3, dims, strides, box_pair);
+        if (rc) return rc;
     }
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(c->f), static_cast<uint64_t>(c->H),
@@ -302,6 +376,9 @@ int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* 
                                      static_cast<uint64_t>(c->f) * c->H * 2};
         const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(c->bn2), 1};
         int rc = encode_map(c, &c->tmW2, c->W2p, 3, dims, strides, box);
+        if (rc) return rc;
+        const uint32_t box_pair[3] = {tpmlp::kBK, 128, 1};
+        rc = encode_map(c, &c->tmW2_pair, c->W2p, 3, dims, strides, box_pair);
         if (rc) return rc;
     }
     c->packed = true;

@@ -1,0 +1,241 @@
+// The two GEMMs of the tensor-parallel MLP block on CTA pairs (tcgen05 cta_group::2).
+//
+// Same computation and epilogues as tpmlp_gemm.cuh (Y_i = GeLU(X W1_i + b1_i) for every shard;
+// Z = b2 + sum_i Y_i W2_i with the sum over shards taken in one fp32 accumulator), but each
+// output tile is 256 x 256 and is computed by a cluster of two CTAs on two SMs:
+//
+//   CTA rank r (r = 0, 1) of the pair loads rows [m0 + 128 r, +128) of A and rows
+//   [n0 + 128 r, +128) of B into its own shared memory. One thread of rank 0 issues
+//   tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): the tensor cores read A and B from
+//   both CTAs and write rows [128 r, +128) of the 256 x 256 fp32 accumulator into CTA r's
+//   tensor memory.
+//
+// Per CTA a pipeline stage is 32 KB (instead of 48 KB for a 128 x 256 tile on one SM), so the
+// same shared memory holds more stages in flight, and every operand byte fetched from L2
+// feeds twice as many multiply-adds.
+//
+// Synchronisation:
+//   full[s]   (rank 0)  rank 0 arms it with both CTAs' bytes; both CTAs' TMA loads complete on it
+//   empty[s]  (both)    the MMA thread's multicast commit frees stage s in both CTAs
+//   tfull[a]  (both)    multicast commit: accumulator a is complete in both CTAs
+//   tempty[a] (rank 0)  8 arrivals (4 epilogue warps per CTA): accumulator a has been read
+// All waits are bounded (ptx::mbar_wait); see tpmlp_gemm.cuh for the abort protocol.
+#pragma once
+
+#include "tpmlp_gemm.cuh"
+
+namespace tpmlp {
+
+constexpr int kPairBM = 256;  // output rows per pair tile (128 per CTA)
+constexpr int kPairBN = 256;  // output columns per pair tile (B: 128 rows per CTA)
+
+template <int STAGES, int NUM_ACC>
+struct PairSmem {
+    static constexpr uint32_t kABytes = 128 * kBK * 2;  // this CTA's 128 rows of A
+    static constexpr uint32_t kBBytes = 128 * kBK * 2;  // this CTA's 128 rows of B
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kCtrlBytes = 8 * (2 * STAGES + 2 * NUM_ACC + 1) + 8;
+    static constexpr uint32_t kTotal = 1024 + STAGES * kStageBytes + kCtrlBytes;
+    static constexpr uint32_t kTmemCols = NUM_ACC * kPairBN;  // 256 or 512
+};
+
+template <int STAGES, int NUM_ACC, Mode MODE, bool OUT_F32>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
+    tpmlp_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+    using L = PairSmem<STAGES, NUM_ACC>;
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, kPairBN);
+    constexpr int kCode = (static_cast<int>(MODE) << 8) | 0x80;  // 0x80: pair kernel
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    const uint32_t ctrl = base + STAGES * L::kStageBytes;
+    auto full_bar = [&](int s) { return ctrl + 8u * s; };
+    auto empty_bar = [&](int s) { return ctrl + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return ctrl + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return ctrl + 8u * (2 * STAGES + NUM_ACC + b); };
+    const uint32_t drain_bar = ctrl + 8u * (2 * STAGES + 2 * NUM_ACC);
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(
+        base_ptr + STAGES * L::kStageBytes + 8 * (2 * STAGES + 2 * NUM_ACC + 1));
+    volatile uint32_t* const abort_flag = tmem_holder + 1;
+
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < NUM_ACC; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), 2 * kEpiWarps);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_addr(tmem_holder), L::kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // barriers of both CTAs initialised, tensor memory allocated
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------- TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < args.num_tiles; t += num_pairs) {
+                int m_blk, n_blk;
+                decode_tile(args, t, m_blk, n_blk);
+                const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;  // this CTA's A rows
+                const int n0 = n_blk * kPairBN;
+                const int nb = n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
+                const int shard1 = (MODE == Mode::kGemm1) ? n0 / args.f : 0;
+                const int nb_in_shard1 = nb - shard1 * args.f;
+                for (int kb = 0; kb < args.kb_tile; ++kb) {
+                    if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status,
+                                        kCode | kSiteProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * L::kStageBytes;
+                    const uint32_t sb = sa + L::kABytes;
+                    const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // rank 0's barrier
+                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
+                    if constexpr (MODE == Mode::kGemm1) {
+                        ptx::tma_load_2d_pair(sa, &tmA, fb, kb * kBK, m0);
+                        ptx::tma_load_3d_pair(sb, &tmB, fb, kb * kBK, nb_in_shard1, shard1);
+                    } else {
+                        const int i = kb / args.kb_shard;               // shard of this block
+                        const int kk = (kb - i * args.kb_shard) * kBK;  // offset inside shard i
+                        ptx::tma_load_2d_pair(sa, &tmA, fb, i * args.f + kk, m0);
+                        ptx::tma_load_3d_pair(sb, &tmB, fb, kk, nb, i);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                if (leader) {
+                    for (uint32_t s = 0; s < STAGES && s < issued; ++s) {
+                        const uint32_t last = s + ((issued - 1 - s) / STAGES) * STAGES;
+                        ptx::mbar_wait_drain(full_bar(s), (last / STAGES) & 1u);
+                    }
+                } else {
+                    // this CTA's copies complete on rank 0's barriers: give them time to land
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    while (ptx::globaltimer_ns() - t0 < 2000000ull) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA issuer (rank 0)
+        if (leader && lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < args.num_tiles; t += num_pairs) {
+                if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status,
+                                    kCode | kSiteMmaAccum)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kPairBN;
+                for (int kb = 0; kb < args.kb_tile; ++kb) {
+                    if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, args.status,
+                                        kCode | kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = base + stage * L::kStageBytes;
+                    const uint64_t da = sdesc_k128(sa);
+                    const uint64_t db = sdesc_k128(sa + L::kABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+                        ptx::mma_bf16_ss_pair(d_tmem, da + 2u * kk, db + 2u * kk, kIdesc,
+                                              (kb | kk) != 0 ? 1u : 0u);
+                    ptx::mma_commit_pair(empty_bar(stage), 0x3);  // stage s free in both CTAs
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(tfull_bar(acc), 0x3);  // accumulator ready in both CTAs
+                if (++acc == NUM_ACC) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            ptx::mma_commit_pair(drain_bar, 0x1);
+            ptx::mbar_wait_drain(drain_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- epilogue (both CTAs)
+        const int q = warp & 3;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int t = pair; t < args.num_tiles; t += num_pairs) {
+            int m_blk, n_blk;
+            decode_tile(args, t, m_blk, n_blk);
+            const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;
+            const int n0 = n_blk * kPairBN;
+            bool ok = ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status,
+                                     kCode | kSiteEpilogue);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            ptx::tc_fence_after();
+            const int row = m0 + q * 32 + lane;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kPairBN;
+#pragma unroll 1
+            for (int c = 0; c < kPairBN; c += 32) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(taddr + c, v);
+                ptx::tmem_wait_ld(v);
+                if (c + 32 == kPairBN) {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+                }
+                epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo,
+                                              n0 + c);
+            }
+            if (++acc == NUM_ACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // no CTA leaves while its peer may still signal it
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, L::kTmemCols);
+    }
+}
+
+}  // namespace tpmlp

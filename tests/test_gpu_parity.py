@@ -211,3 +211,41 @@ def test_argument_errors_on_device(lib):
             tp.tpmlp_forward(mlp.ctx, dd["X"], -1, 128, Z)
         assert e.value.status == tp.TPMLP_ERR_INVALID_ARG
         assert mlp.status()[0] == tp.TPMLP_OK
+
+
+# ----------------------------------------------------------------------------- both kernels
+@pytest.mark.parametrize("H,F,k,M", [(256, 1024, 2, 128), (256, 1024, 4, 777), (1024, 4096, 4, 1000),
+                                     (512, 2048, 8, 4096), (768, 3072, 3, 300)])
+def test_pair_and_single_sm_kernels_agree(lib, H, F, k, M):
+    """The CTA-pair kernel (256 x 256 tiles on two SMs) and the single-SM kernel (128-row
+    tiles) reduce in the same order, so Y and Z agree bit for bit; both match the oracle."""
+    d = synth.make_inputs(H, F, M, 101)
+    dd = inputs_on_device(d)
+    outs = []
+    for single in (True, False):
+        with tp.TPMLP(H, F, k, single_sm=single) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            Y = mlp.gemm1(dd["X"])
+            Z = mlp.gemm2(Y)
+            torch.cuda.synchronize()
+            assert mlp.status()[0] == tp.TPMLP_OK
+            outs.append((bits_of(Y), bits_of(Z)))
+    assert np.array_equal(outs[0][0], outs[1][0]), "Y differs between kernels"
+    assert np.array_equal(outs[0][1], outs[1][1]), "Z differs between kernels"
+    ref = oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], k)["Z"]
+    assert_close(f64(outs[1][1]), ref, what=f"pair kernel H={H} F={F} k={k} M={M}")
+
+
+def test_single_sm_kernel_on_a_large_workload(lib):
+    """7B-shaped block with the single-SM kernel forced (sampled rows vs the oracle)."""
+    w = synth.WORKLOADS["7b"]
+    d = synth.workload_inputs(w)
+    dd = inputs_on_device(d)
+    with tp.TPMLP(w.H, w.F, w.k, single_sm=True) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        Z = mlp(dd["X"].view(w.B, w.S, w.H))
+        torch.cuda.synchronize()
+        assert mlp.status()[0] == tp.TPMLP_OK
+    sel = synth.sample_rows(w.M, 32)
+    ref = oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=sel)["Z"]
+    assert_close(to_f64(Z.view(w.M, w.H))[sel], ref, what="7b single-SM")
