@@ -316,6 +316,10 @@ def run_gpu(args, w: synth.Workload):
         "pct_of_dense_bf16_peak_burst": 100.0 * (value / world) / peak_burst,
         "wall_ms_per_step_incl_l2_flush": t_wall * 1e3 / args.steps,
         "kernel_ms": kern,
+        "hbm_gbs_algorithmic": {  # algorithmic bytes of each launch / its mean event time
+            "gemm1": alg_bytes(w, "gemm1") / (kern["gemm1"] * 1e-3) / 1e9,
+            "gemm2": alg_bytes(w, "gemm2") / (kern["gemm2"] * 1e-3) / 1e9,
+            "peak_hbm_gbs": peaks["hbm_gbs"]},
         "config": workload_config(w, {"parallelism": "replicas" if world > 1 else "single GPU",
                                       "output": "bf16"}),
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
@@ -343,6 +347,14 @@ def run_gpu(args, w: synth.Workload):
         pg.barrier()
         pg.destroy_process_group()
     return 0
+
+
+def alg_bytes(w: synth.Workload, kernel: str) -> int:
+    """Bytes a launch must move at least: its operands once and its output once
+    (GEMM1: X, W1, b1, Y; GEMM2: Y, W2, b2, Z; bf16 tensors, fp32 biases)."""
+    if kernel == "gemm1":
+        return 2 * w.M * w.H + 2 * w.H * w.F + 4 * w.F + 2 * w.M * w.F
+    return 2 * w.M * w.F + 2 * w.F * w.H + 4 * w.H + 2 * w.M * w.H
 
 
 def measured_traffic(workload: str, kernel: str):

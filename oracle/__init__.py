@@ -14,6 +14,8 @@ What it computes (the pages' definition of the Megatron MLP block):
                                would (same page, "方案二：按行切分权重矩阵", Z = Y1V1 + Y2V2;
                                大模型分布式并行策略详解 §4.1; AI大模型分布式训练 §2.2)
 with GeLU(a) = a/2 (1 + erf(a/sqrt 2)) (reading: the exact form) and b2 added once.
+The gated variant (gate_up_proj column-parallel, down_proj row-parallel: 大模型分布式优化技术（一）
+§5.1, AI大模型分布式训练 §6.1) replaces GeLU(X W1 + b1) by SiLU(X Wg + bg) * (X Wu + bu).
 
 Pins (tests/test_oracle.py): identity-activation case against numpy float64 matmul,
 GeLU values from the normal-CDF table and scipy's ndtr, the odd-part identity
@@ -57,6 +59,11 @@ class Oracle:
         lib.oracle_tpmlp_f64.restype = ctypes.c_int
         lib.oracle_gelu.argtypes = [ctypes.c_double]
         lib.oracle_gelu.restype = ctypes.c_double
+        lib.oracle_tpmlp_swiglu_f64.argtypes = [vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, i64, i64,
+                                                i32, vp, vp]
+        lib.oracle_tpmlp_swiglu_f64.restype = ctypes.c_int
+        lib.oracle_silu.argtypes = [ctypes.c_double]
+        lib.oracle_silu.restype = ctypes.c_double
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ctypes.c_int
         self.lib = lib
@@ -106,6 +113,34 @@ class Oracle:
         return out
 
 
+    def silu(self, a: float) -> float:
+        return float(self.lib.oracle_silu(float(a)))
+
+    def tpmlp_swiglu(self, X, Wg, bg, Wu, bu, W2, b2, k: int, rows=None, want_y: bool = False):
+        """Gated variant: Y = SiLU(X Wg + bg) * (X Wu + bu), Z = sum_i Y_i W2_i + b2 (fp64).
+        X [x_rows, H]; Wg, Wu [H, F]; bg, bu [F]; W2 [F, H]; b2 [H] (bf16 bit patterns)."""
+        X, Wg, bg, Wu, bu, W2, b2 = (_u16(a) for a in (X, Wg, bg, Wu, bu, W2, b2))
+        x_rows, H = X.shape
+        H1, F = Wg.shape
+        if (H1 != H or Wu.shape != (H, F) or W2.shape != (F, H) or bg.shape != (F,)
+                or bu.shape != (F,) or b2.shape != (H,)):
+            raise ValueError("shape mismatch")
+        rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        R = x_rows if rows_arr is None else len(rows_arr)
+        Z = np.empty((R, H), dtype=np.float64)
+        Y = np.empty((R, F), dtype=np.float64) if want_y else None
+        rc = self.lib.oracle_tpmlp_swiglu_f64(
+            X.ctypes.data, x_rows, None if rows_arr is None else rows_arr.ctypes.data, R,
+            Wg.ctypes.data, bg.ctypes.data, Wu.ctypes.data, bu.ctypes.data, W2.ctypes.data,
+            b2.ctypes.data, H, F, k, Z.ctypes.data, None if Y is None else Y.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments (F % k, rows out of range, ...)")
+        out = {"Z": Z}
+        if want_y:
+            out["Y"] = Y
+        return out
+
+
 def _u16(a) -> np.ndarray:
     a = np.ascontiguousarray(a)
     if a.dtype != np.uint16:
@@ -151,3 +186,11 @@ def tpmlp(X, W1, b1, W2, b2, k: int, rows=None, act: int = ACT_GELU, want_y: boo
           want_partials: bool = False):
     return default().tpmlp(X, W1, b1, W2, b2, k, rows=rows, act=act, want_y=want_y,
                            want_partials=want_partials)
+
+
+def silu(a: float) -> float:
+    return default().silu(a)
+
+
+def tpmlp_swiglu(X, Wg, bg, Wu, bu, W2, b2, k: int, rows=None, want_y: bool = False):
+    return default().tpmlp_swiglu(X, Wg, bg, Wu, bu, W2, b2, k, rows=rows, want_y=want_y)

@@ -139,6 +139,88 @@ int oracle_tpmlp_f64(const uint16_t *X, int64_t x_rows, const int64_t *rows, int
     return failed ? -1 : 0;
 }
 
+/*
+ * Gated variant (the NEXT step the pages point to): the FFN's gate_up_proj is
+ * column-parallel and its down_proj row-parallel (大模型分布式优化技术（一） §5.1;
+ * AI大模型分布式训练 §6.1 gate_proj / up_proj ColwiseParallel, down_proj RowwiseParallel),
+ * with the SwiGLU activation named in §3.3 of the first of those pages.
+ * Reading: Y = SiLU(X Wg + bg) * (X Wu + bu), SiLU(a) = a / (1 + exp(-a)), element by
+ * element; shard i owns columns [i f, (i+1) f) of BOTH Wg and Wu and rows [i f, (i+1) f) of W2.
+ *   Z[m, n] = b2[n] + sum_i sum_{j in shard i} SiLU(ag_j) * au_j * W2[j, n]
+ *   ag_j = bg[j] + sum_h X[m, h] Wg[h, j],   au_j = bu[j] + sum_h X[m, h] Wu[h, j]
+ */
+double oracle_silu(double a) { return a / (1.0 + exp(-a)); }
+
+int oracle_tpmlp_swiglu_f64(const uint16_t *X, int64_t x_rows, const int64_t *rows, int64_t R,
+                            const uint16_t *Wg, const uint16_t *bg, const uint16_t *Wu,
+                            const uint16_t *bu, const uint16_t *W2, const uint16_t *b2, int64_t H,
+                            int64_t F, int32_t k, double *Z, double *Y) {
+    if (!X || !Wg || !bg || !Wu || !bu || !W2 || !b2 || !Z || H <= 0 || F <= 0 || k <= 0 || R < 0)
+        return -1;
+    if (F % k != 0) return -1;
+    const int64_t f = F / k;
+    int failed = 0;
+
+#pragma omp parallel
+    {
+        double *ag = (double *)malloc(sizeof(double) * (size_t)f);
+        double *au = (double *)malloc(sizeof(double) * (size_t)f);
+        double *part = (double *)malloc(sizeof(double) * (size_t)H);
+        double *zsum = (double *)malloc(sizeof(double) * (size_t)H);
+        if (!ag || !au || !part || !zsum) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < R; ++r) {
+                const int64_t m = rows ? rows[r] : r;
+                if (m < 0 || m >= x_rows) {
+#pragma omp atomic write
+                    failed = 1;
+                    continue;
+                }
+                const uint16_t *x = X + m * H;
+                for (int64_t n = 0; n < H; ++n) zsum[n] = 0.0;
+
+                for (int32_t i = 0; i < k; ++i) {
+                    const int64_t j0 = (int64_t)i * f;
+                    /* column shard i of the gate and of the up projection */
+                    for (int64_t jj = 0; jj < f; ++jj) ag[jj] = au[jj] = 0.0;
+                    for (int64_t h = 0; h < H; ++h) {
+                        const double xh = widen_bf16(x[h]);
+                        const uint16_t *wg = Wg + h * F + j0;
+                        const uint16_t *wu = Wu + h * F + j0;
+                        for (int64_t jj = 0; jj < f; ++jj) {
+                            ag[jj] += xh * widen_bf16(wg[jj]);
+                            au[jj] += xh * widen_bf16(wu[jj]);
+                        }
+                    }
+                    for (int64_t jj = 0; jj < f; ++jj) {
+                        const double g = ag[jj] + widen_bf16(bg[j0 + jj]);
+                        const double u = au[jj] + widen_bf16(bu[j0 + jj]);
+                        ag[jj] = oracle_silu(g) * u;
+                        if (Y) Y[r * F + j0 + jj] = ag[jj];
+                    }
+                    /* row shard i of W2, then the all-reduce (shard order) */
+                    for (int64_t n = 0; n < H; ++n) part[n] = 0.0;
+                    for (int64_t jj = 0; jj < f; ++jj) {
+                        const double y = ag[jj];
+                        const uint16_t *w = W2 + (j0 + jj) * H;
+                        for (int64_t n = 0; n < H; ++n) part[n] += y * widen_bf16(w[n]);
+                    }
+                    for (int64_t n = 0; n < H; ++n) zsum[n] += part[n];
+                }
+                for (int64_t n = 0; n < H; ++n) Z[r * H + n] = zsum[n] + widen_bf16(b2[n]);
+            }
+        }
+        free(ag);
+        free(au);
+        free(part);
+        free(zsum);
+    }
+    return failed ? -1 : 0;
+}
+
 int oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -39,6 +40,14 @@ struct tpmlp_ctx {
     void* Xs = nullptr;  // staging for tpmlp_forward_host
     void* Zs = nullptr;
     int64_t stage_rows = 0;
+
+    // activation tensor maps of the last call (re-encoded only when pointer or rows change)
+    const void* x_map_ptr = nullptr;
+    int64_t x_map_rows = -1;
+    CUtensorMap tmX{};
+    const void* y_map_ptr = nullptr;
+    int64_t y_map_rows = -1;
+    CUtensorMap tmY{};
 
     int* status = nullptr;  // device status word
     int64_t launches = 0;
@@ -131,12 +140,23 @@ int pick_bn(int64_t width) {
     return 64;
 }
 
+// Opt a kernel into its dynamic shared memory once per device (bit d of `done`).
+template <typename Kernel>
+int ensure_smem_attr(tpmlp_ctx* c, Kernel kern, uint32_t smem, std::atomic<uint64_t>& done) {
+    const uint64_t bit = uint64_t(1) << (c->device & 63);
+    if (done.load(std::memory_order_acquire) & bit) return TPMLP_OK;
+    TPMLP_CUDA(c, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return TPMLP_OK;
+}
+
 template <int BN, int STAGES, Mode MODE, bool F32>
 int launch_gemm(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                 cudaStream_t s) {
     auto kern = tpmlp::tpmlp_gemm_kernel<BN, STAGES, MODE, F32>;
     constexpr uint32_t smem = tpmlp::GemmSmem<BN, STAGES>::kTotal;
-    TPMLP_CUDA(c, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    static std::atomic<uint64_t> attr_done{0};
+    if (int rc = ensure_smem_attr(c, kern, smem, attr_done)) return rc;
     const int grid = std::min(args.num_tiles, c->num_sms);
     kern<<<grid, tpmlp::kNumThreads, smem, s>>>(a, b, args);
     TPMLP_CUDA(c, cudaGetLastError());
@@ -176,7 +196,8 @@ int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
     auto kern = tpmlp::tpmlp_gemm_pair_kernel<STAGES, NUM_ACC, MODE, F32>;
     constexpr uint32_t smem = tpmlp::PairSmem<STAGES, NUM_ACC>::kTotal;
     static_assert(smem <= 232448, "shared memory per CTA");
-    TPMLP_CUDA(c, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    static std::atomic<uint64_t> attr_done{0};
+    if (int rc = ensure_smem_attr(c, kern, smem, attr_done)) return rc;
     static int resident = 0;  // same for every GB300; looked up on first use
     if (resident <= 0) resident = max_resident_pairs(c, kern, smem);
     const int pairs = std::min(args.num_tiles, resident);
@@ -206,13 +227,26 @@ int check_ctx(const tpmlp_ctx* c) {
     return TPMLP_OK;
 }
 
-int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
-    CUtensorMap tmX;
-    const uint64_t dims[2] = {static_cast<uint64_t>(c->H), static_cast<uint64_t>(M)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(c->H) * 2};
+// Tensor map of a row-major bf16 [rows][cols] activation, box 64 x 128, cached per pointer
+// and row count.
+int activation_map(tpmlp_ctx* c, const void* ptr, int64_t rows, int64_t cols,
+                   const void*& cached_ptr, int64_t& cached_rows, CUtensorMap& map) {
+    if (ptr == cached_ptr && rows == cached_rows) return TPMLP_OK;
+    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(cols) * 2};
     const uint32_t box[2] = {tpmlp::kBK, tpmlp::kBM};
-    int rc = encode_map(c, &tmX, X, 2, dims, strides, box);
+    cached_ptr = nullptr;
+    int rc = encode_map(c, &map, ptr, 2, dims, strides, box);
     if (rc) return rc;
+    cached_ptr = ptr;
+    cached_rows = rows;
+    return TPMLP_OK;
+}
+
+int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
+    int rc = activation_map(c, X, M, c->H, c->x_map_ptr, c->x_map_rows, c->tmX);
+    if (rc) return rc;
+    const CUtensorMap& tmX = c->tmX;
     const bool pair = c->pair1;
     GemmArgs a = base_args(c, M, static_cast<int>(c->F), pair ? tpmlp::kPairBM : tpmlp::kBM,
                            pair ? tpmlp::kPairBN : c->bn1, TPMLP_GROUP_M1);
@@ -227,12 +261,9 @@ int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
 }
 
 int run_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, cudaStream_t s) {
-    CUtensorMap tmY;
-    const uint64_t dims[2] = {static_cast<uint64_t>(c->F), static_cast<uint64_t>(M)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(c->F) * 2};
-    const uint32_t box[2] = {tpmlp::kBK, tpmlp::kBM};
-    int rc = encode_map(c, &tmY, Y, 2, dims, strides, box);
+    int rc = activation_map(c, Y, M, c->F, c->y_map_ptr, c->y_map_rows, c->tmY);
     if (rc) return rc;
+    const CUtensorMap& tmY = c->tmY;
     const bool pair = c->pair2;
     GemmArgs a = base_args(c, M, static_cast<int>(c->H), pair ? tpmlp::kPairBM : tpmlp::kBM,
                            pair ? tpmlp::kPairBN : c->bn2, TPMLP_GROUP_M2);

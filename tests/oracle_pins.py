@@ -193,8 +193,88 @@ def pin_x_linear_without_activation(orc):
     assert np.array_equal(z2, 2.0 * z)
 
 
+# ---------------------------------------------------------------------------------
+# gated (SwiGLU) variant
+def _small_swiglu(seed=17, H=64, F=256, M=29):
+    d = synth.make_inputs(H, F, M, seed)
+    extra = synth.make_inputs(H, F, 1, seed + 1000)  # a second, independent W1 / b1 for "up"
+    d = {"X": d["X"], "Wg": d["W1"], "bg": d["b1"], "Wu": extra["W1"], "bu": extra["b1"],
+         "W2": d["W2"], "b2": d["b2"]}
+    return d, {k: synth.bf16_to_f64(v) for k, v in d.items()}
+
+
+def _swiglu(orc, d, k, **kw):
+    return orc.tpmlp_swiglu(d["X"], d["Wg"], d["bg"], d["Wu"], d["bu"], d["W2"], d["b2"], k, **kw)
+
+
+def pin_silu_table_and_expit(orc):
+    """SiLU(a) = a * sigma(a): textbook logistic values and scipy's expit."""
+    from scipy.special import expit
+    for a_s, sig in _load("logistic_table.json")["sigma"].items():
+        a = float(a_s)
+        assert abs(orc.silu(a) - a * sig) <= 2e-16 * max(1.0, abs(a)), a
+    for a in np.linspace(-30.0, 30.0, 1201):
+        assert abs(orc.silu(float(a)) - float(a * expit(a))) <= 4e-16 * max(1.0, abs(a)), a
+
+
+def pin_silu_odd_part(orc):
+    """sigma(a) + sigma(-a) = 1  =>  SiLU(a) - SiLU(-a) = a."""
+    for a in np.linspace(0.0, 20.0, 401):
+        d = orc.silu(float(a)) - orc.silu(float(-a))
+        assert abs(d - a) <= 4e-16 * max(1.0, a), (a, d)
+
+
+def pin_swiglu_bruteforce_golden(orc):
+    g = _load("bruteforce_swiglu_h2_f4_k2.json")
+    sig = {float(a): v for a, v in _load("logistic_table.json")["sigma"].items()}
+    d = {n: _bits(g[n]) for n in ("X", "Wg", "bg", "Wu", "bu", "W2", "b2")}
+    r = _swiglu(orc, d, g["k"], want_y=True)
+    for j, (a, u) in enumerate(zip(g["gate_by_hand"], g["up_by_hand"])):
+        assert abs(r["Y"][0, j] - a * sig[a] * u) <= 1e-15, j
+    for n, coeff in enumerate(g["Z_coefficients"]):
+        want = coeff["bias"] + sum(c * float(a) * sig[float(a)] for a, c in coeff.items()
+                                   if a != "bias")
+        assert abs(r["Z"][0, n] - want) <= 1e-14, (n, r["Z"][0, n], want)
+
+
+def pin_swiglu_matches_numpy(orc):
+    """Y = SiLU(X Wg + bg) * (X Wu + bu) and Z = Y W2 + b2 against numpy matmul + expit."""
+    from scipy.special import expit
+    d, f = _small_swiglu()
+    for k in (1, 4):
+        r = _swiglu(orc, d, k, want_y=True)
+        G = f["X"] @ f["Wg"] + f["bg"]
+        U = f["X"] @ f["Wu"] + f["bu"]
+        Y = G * expit(G) * U
+        assert _rel_fro(r["Y"], Y) <= 1e-13, (k, _rel_fro(r["Y"], Y))
+        assert _rel_fro(r["Z"], Y @ f["W2"] + f["b2"]) <= 1e-12, k
+
+
+def pin_swiglu_gate_only(orc):
+    """Wu = 0, bu = 1: the up projection is the constant 1, so Y = SiLU(X Wg + bg) exactly,
+    and swapping gate and up would give a different answer."""
+    from scipy.special import expit
+    d, f = _small_swiglu()
+    d = dict(d)
+    d["Wu"] = np.zeros_like(d["Wu"])
+    d["bu"] = synth.round_bf16(np.ones(d["bu"].shape))
+    r = _swiglu(orc, d, 4, want_y=True)
+    G = f["X"] @ f["Wg"] + f["bg"]
+    assert _rel_fro(r["Y"], G * expit(G)) <= 1e-13
+
+
+def pin_swiglu_k_invariance(orc):
+    d, _ = _small_swiglu(seed=23, F=512)
+    z1 = _swiglu(orc, d, 1)["Z"]
+    for k in (2, 4, 8, 16):
+        assert _rel_fro(_swiglu(orc, d, k)["Z"], z1) <= 1e-12, k
+
+
+SWIGLU_PINS = [pin_silu_table_and_expit, pin_silu_odd_part, pin_swiglu_bruteforce_golden,
+               pin_swiglu_matches_numpy, pin_swiglu_gate_only, pin_swiglu_k_invariance]
+
 ALL_PINS = [
     pin_gelu_table, pin_gelu_ndtr, pin_gelu_odd_part, pin_bruteforce_golden,
     pin_identity_matches_numpy, pin_concat_identity, pin_row_split_sum, pin_k_invariance,
     pin_w2_zero, pin_w1_zero, pin_rows_independent, pin_x_linear_without_activation,
-]
+] + SWIGLU_PINS
