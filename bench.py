@@ -44,12 +44,28 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def workload_config(w: synth.Workload, extra=None) -> dict:
+def step_flops(w: synth.Workload, variant: str) -> int:
+    """FLOPs of one forward pass: 2*M*H*F per contraction (the gated block's first GEMM
+    computes the gate and the up projection: twice that)."""
+    return w.flops if variant == "gelu" else 6 * w.M * w.H * w.F
+
+
+def kernel_flops(w: synth.Workload, variant: str, kernel: str) -> int:
+    base = 2 * w.M * w.H * w.F
+    return 2 * base if (variant == "swiglu" and kernel == "gemm1") else base
+
+
+def workload_config(w: synth.Workload, extra=None, variant: str = "gelu") -> dict:
+    if variant == "gelu":
+        desc = (f"{w.name} TP-MLP: X [B={w.B},S={w.S},H={w.H}] bf16, W1 [{w.H},{w.F}], "
+                f"W2 [{w.F},{w.H}], erf GeLU, k={w.k} shards, seeded synthetic")
+    else:
+        desc = (f"{w.name} gated TP-MLP: X [B={w.B},S={w.S},H={w.H}] bf16, Wg and Wu "
+                f"[{w.H},{w.F}], W2 [{w.F},{w.H}], SwiGLU, k={w.k} shards, seeded synthetic")
     cfg = {
-        "workload": f"{w.name} TP-MLP: X [B={w.B},S={w.S},H={w.H}] bf16, W1 [{w.H},{w.F}], "
-                    f"W2 [{w.F},{w.H}], erf GeLU, k={w.k} shards, seeded synthetic",
+        "workload": desc, "variant": variant,
         "B": w.B, "S": w.S, "M": w.M, "H": w.H, "F": w.F, "k": w.k, "seed": w.seed,
-        "flops_per_step": w.flops,
+        "flops_per_step": step_flops(w, variant),
         "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
     }
     if extra:
@@ -128,20 +144,29 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
-def oracle_sample(w: synth.Workload, d: dict, budget_s: float, max_rows: int):
+def run_oracle(w: synth.Workload, d: dict, rows, variant: str):
+    import oracle
+    if variant == "gelu":
+        return oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=rows)
+    return oracle.tpmlp_swiglu(d["X"], d["Wg"], d["bg"], d["Wu"], d["bu"], d["W2"], d["b2"], w.k,
+                               rows=rows)
+
+
+def oracle_sample(w: synth.Workload, d: dict, budget_s: float, max_rows: int,
+                  variant: str = "gelu"):
     """Time the fp64 oracle on a bounded, seeded sample of token rows of the workload."""
     import oracle
     cal_rows = synth.sample_rows(w.M, min(max(oracle.threads(), 4), max_rows))
     t0 = time.perf_counter()
-    oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=cal_rows)
+    run_oracle(w, d, cal_rows, variant)
     t_cal = time.perf_counter() - t0
     per_row = t_cal / len(cal_rows)
     R = int(max(len(cal_rows), min(max_rows, budget_s / max(per_row, 1e-9))))
     rows = synth.sample_rows(w.M, R)
     t0 = time.perf_counter()
-    oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=rows)
+    run_oracle(w, d, rows, variant)
     dt = time.perf_counter() - t0
-    flops = len(rows) * 4 * w.H * w.F
+    flops = len(rows) * step_flops(w, variant) // w.M
     return {"rows": len(rows), "seconds": dt, "tflops": flops / dt / 1e12,
             "tokens_per_s": len(rows) / dt, "cores": oracle.threads()}
 
@@ -152,25 +177,26 @@ def run_reference(args, w: synth.Workload):
     if rank != 0:
         return 0
     import oracle
-    d = synth.workload_inputs(w)
+    v = args.variant
+    d = synth.workload_inputs(w) if v == "gelu" else synth.make_swiglu_inputs(w.H, w.F, w.M, w.seed)
     steps, warm = args.steps, args.warmup
     budget = args.reference_budget_s
     # rows per step so that the whole run stays within the budget
     cal_rows = synth.sample_rows(w.M, max(oracle.threads(), 4))
     t0 = time.perf_counter()
-    oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=cal_rows)
+    run_oracle(w, d, cal_rows, v)
     per_row = (time.perf_counter() - t0) / len(cal_rows)
     R = int(max(1, min(w.M, budget / (steps + warm) / max(per_row, 1e-9))))
     rows = synth.sample_rows(w.M, R)
     for _ in range(warm):
-        oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=rows)
+        run_oracle(w, d, rows, v)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=rows)
+        run_oracle(w, d, rows, v)
         times.append(time.perf_counter() - t0)
     t = statistics.mean(times)
-    flops = len(rows) * 4 * w.H * w.F
+    flops = len(rows) * step_flops(w, v) // w.M
     value = flops / t / 1e12
     sample = (f"{len(rows)} of {w.M} token rows per step (seeded spread incl. first/last), full "
               f"weights, all {w.H} outputs; fp64 oracle, OpenMP over rows")
@@ -179,7 +205,8 @@ def run_reference(args, w: synth.Workload):
         "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "tokens_per_s": len(rows) / t,
-        "config": workload_config(w, {"parallelism": "host cores (oracle)", "rows_per_step": len(rows)}),
+        "config": workload_config(w, {"parallelism": "host cores (oracle)",
+                                      "rows_per_step": len(rows)}, variant=v),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -208,23 +235,25 @@ def run_gpu(args, w: synth.Workload):
         if pg is not None:
             pg.barrier()
 
-    d = synth.workload_inputs(w)
+    variant = args.variant
+    d = synth.workload_inputs(w) if variant == "gelu" else synth.make_swiglu_inputs(w.H, w.F, w.M, w.seed)
 
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
     X = to_dev(d["X"]).view(w.B, w.S, w.H)
-    W1, b1, W2, b2 = (to_dev(d[n]) for n in ("W1", "b1", "W2", "b2"))
     Z = torch.empty((w.B, w.S, w.H), dtype=torch.bfloat16, device=dev)
     Y = torch.empty((w.M, w.F), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    mlp = tp.TPMLP(w.H, w.F, w.k)
-    mlp.pack(W1, b1, W2, b2)
+    mlp = tp.TPMLP(w.H, w.F, w.k, swiglu=(variant == "swiglu"))
+    if variant == "gelu":
+        mlp.pack(*(to_dev(d[n]) for n in ("W1", "b1", "W2", "b2")))
+    else:
+        mlp.pack_swiglu(*(to_dev(d[n]) for n in ("Wg", "bg", "Wu", "bu", "W2", "b2")))
     mlp.reserve(w.M)
-    torch.cuda.synchronize(dev)
-    del W1, W2  # raw weights are not needed after packing
+    torch.cuda.synchronize(dev)  # the raw weights are released: only the packed copies stay
 
     def step(ev=None):
         # one pass of the whole block: GEMM1 (+b1, GeLU) then GEMM2 (sum over shards, +b2)
@@ -293,18 +322,19 @@ def run_gpu(args, w: synth.Workload):
     if rc != tp.TPMLP_OK:
         raise RuntimeError(f"device status after e2e steps: {detail:#x}")
 
-    flops_step = w.flops
+    flops_step = step_flops(w, variant)
     value = world * flops_step / (ms_step * 1e-3) / 1e12
     tokens = world * w.M / (ms_step * 1e-3)
     peaks, peak_src = load_peaks()
     peak_burst = peaks["bf16_tflops"]
     peak_sust = peaks.get("bf16_tflops_sustained", peak_burst)
     kern = {"gemm1": statistics.mean(g1), "gemm2": statistics.mean(g2)}
-    dom = max(kern, key=kern.get)
-    achieved = (flops_step / 2) / (kern[dom] * 1e-3) / 1e12
+    kflops = {kk: kernel_flops(w, variant, kk) for kk in kern}
+    dom = max(kern, key=lambda kk: kern[kk])
+    achieved = kflops[dom] / (kern[dom] * 1e-3) / 1e12
     # the kernels run back to back for the whole timed region (seconds): sustained peak
     peak = peak_sust
-    traffic = measured_traffic(w.name, dom)
+    traffic = measured_traffic(w.name if variant == "gelu" else f"{w.name}-swiglu", dom)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -317,11 +347,11 @@ def run_gpu(args, w: synth.Workload):
         "wall_ms_per_step_incl_l2_flush": t_wall * 1e3 / args.steps,
         "kernel_ms": kern,
         "hbm_gbs_algorithmic": {  # algorithmic bytes of each launch / its mean event time
-            "gemm1": alg_bytes(w, "gemm1") / (kern["gemm1"] * 1e-3) / 1e9,
-            "gemm2": alg_bytes(w, "gemm2") / (kern["gemm2"] * 1e-3) / 1e9,
+            "gemm1": alg_bytes(w, "gemm1", variant) / (kern["gemm1"] * 1e-3) / 1e9,
+            "gemm2": alg_bytes(w, "gemm2", variant) / (kern["gemm2"] * 1e-3) / 1e9,
             "peak_hbm_gbs": peaks["hbm_gbs"]},
         "config": workload_config(w, {"parallelism": "replicas" if world > 1 else "single GPU",
-                                      "output": "bf16"}),
+                                      "output": "bf16"}, variant=variant),
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS bf16 loop under "
@@ -333,7 +363,7 @@ def run_gpu(args, w: synth.Workload):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = oracle_sample(w, d, args.cpu_budget_s, args.cpu_max_rows)
+        cb = oracle_sample(w, d, args.cpu_budget_s, args.cpu_max_rows, variant)
         line["cpu_baseline"] = {
             "value": cb["tflops"], "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
             "sample": f"{cb['rows']} of {w.M} token rows (seeded spread incl. first/last), full "
@@ -349,11 +379,13 @@ def run_gpu(args, w: synth.Workload):
     return 0
 
 
-def alg_bytes(w: synth.Workload, kernel: str) -> int:
+def alg_bytes(w: synth.Workload, kernel: str, variant: str = "gelu") -> int:
     """Bytes a launch must move at least: its operands once and its output once
-    (GEMM1: X, W1, b1, Y; GEMM2: Y, W2, b2, Z; bf16 tensors, fp32 biases)."""
+    (GEMM1: X, W1 (gated: Wg and Wu), biases, Y; GEMM2: Y, W2, b2, Z; bf16 tensors, fp32
+    biases)."""
     if kernel == "gemm1":
-        return 2 * w.M * w.H + 2 * w.H * w.F + 4 * w.F + 2 * w.M * w.F
+        parts = 2 if variant == "swiglu" else 1
+        return 2 * w.M * w.H + parts * (2 * w.H * w.F + 4 * w.F) + 2 * w.M * w.F
     return 2 * w.M * w.F + 2 * w.F * w.H + 4 * w.H + 2 * w.M * w.H
 
 
@@ -386,6 +418,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--k", type=int, default=None, help="override the shard count")
+    ap.add_argument("--variant", default="gelu", choices=["gelu", "swiglu"],
+                    help="gelu: the block of the pages' Megatron figure; swiglu: the gated block")
     ap.add_argument("--impl", default="tpmlp", choices=["tpmlp", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--cpu-max-rows", type=int, default=4096)

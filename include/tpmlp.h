@@ -60,6 +60,8 @@ typedef enum {
 #define TPMLP_FLAG_Z_FP32 0x1u    /* Z is written as fp32 instead of bf16 */
 #define TPMLP_FLAG_SINGLE_SM 0x2u /* use only the single-SM kernel (128-row tiles), never the
                                      CTA-pair kernel (256 x 256 tiles on two SMs); same results */
+#define TPMLP_FLAG_SWIGLU 0x4u    /* gated block: Y_i = SiLU(X Wg_i + bg_i) * (X Wu_i + bu_i);
+                                     weights come from tpmlp_pack_shards_swiglu */
 
 /*
  * Create a context for one block shape on the current CUDA device.
@@ -70,7 +72,7 @@ typedef enum {
  *            parallel degree; shards are contiguous, equal column blocks of W1 and the
  *            matching row blocks of W2 -- AI大模型分布式训练 §2.1 splits W into
  *            [hidden, ffn/k] pieces)
- *   flags    0, or TPMLP_FLAG_Z_FP32 and/or TPMLP_FLAG_SINGLE_SM
+ *   flags    0, or any of TPMLP_FLAG_Z_FP32, TPMLP_FLAG_SINGLE_SM, TPMLP_FLAG_SWIGLU
  * Allocates the packed-weight buffers (2*H*F bf16 + (F+H) fp32) and a device status word;
  * the intermediate activation buffer is allocated by tpmlp_reserve or the first forward.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ARCH (device is not sm_103), OOM, CUDA.
@@ -85,10 +87,29 @@ TPMLP_API int tpmlp_create(tpmlp_ctx **out, int64_t H, int64_t F, int32_t k, uin
  * Writes W1p [k][f][H] (each column shard transposed so that its reduction dimension H is
  * contiguous), W2p [k][H][f] (each row shard transposed likewise), and fp32 copies of b1
  * and b2. The raw weights may be freed once the stream has passed this call.
- * Errors: INVALID_ARG, MISALIGNED, CUDA.
+ * Errors: INVALID_ARG (also: context created with TPMLP_FLAG_SWIGLU), MISALIGNED, CUDA.
  */
 TPMLP_API int tpmlp_pack_shards(tpmlp_ctx *ctx, const void *W1, const void *b1, const void *W2,
                       const void *b2, void *stream);
+
+/*
+ * Pack the weights of the gated block (context created with TPMLP_FLAG_SWIGLU). The pages'
+ * Llama-style feed-forward splits gate_up_proj by columns and down_proj by rows
+ * (大模型分布式优化技术（一） §5.1; AI大模型分布式训练 §6.1: gate_proj / up_proj ColwiseParallel,
+ * down_proj RowwiseParallel); the activation is SwiGLU (same first page, §3.3):
+ *     Y_i = SiLU(X Wg_i + bg_i) * (X Wu_i + bu_i),   Z = sum_i Y_i W2_i + b2,
+ *     SiLU(a) = a / (1 + e^-a), shard i = columns [i f, (i+1) f) of Wg and Wu.
+ *   Wg, Wu device bf16 [H, F]   bg, bu device bf16 [F] (zeros for bias-free models)
+ *   W2 device bf16 [F, H]       b2 device bf16 [H]
+ * Writes one K-major operand holding both projections, interleaved in blocks of G = 128
+ * (64 if f is not a multiple of 128) rows per shard, so that every tile of the first GEMM
+ * holds the gate and up columns of the same outputs; W2 and b2 are packed as in
+ * tpmlp_pack_shards. tpmlp_forward / tpmlp_gemm1 / tpmlp_gemm2 then run the gated block.
+ * Errors: INVALID_ARG (also: context not created with TPMLP_FLAG_SWIGLU), MISALIGNED, CUDA.
+ */
+TPMLP_API int tpmlp_pack_shards_swiglu(tpmlp_ctx *ctx, const void *Wg, const void *bg,
+                                       const void *Wu, const void *bu, const void *W2,
+                                       const void *b2, void *stream);
 
 /*
  * Make sure the intermediate buffer Y [M, F] (bf16) holds at least max_tokens rows.
@@ -149,7 +170,9 @@ TPMLP_API int tpmlp_get_status(tpmlp_ctx *ctx, void *stream, int32_t *detail);
 
 /*
  * Where the packed weights live (for tests that unpack and compare them bit for bit).
- *   which: 0 = W1p bf16 [k][f][H], 1 = W2p bf16 [k][H][f], 2 = b1 fp32 [F], 3 = b2 fp32 [H]
+ *   which: 0 = W1p bf16 [k][f][H], 1 = W2p bf16 [k][H][f], 2 = b1 fp32 [F], 3 = b2 fp32 [H];
+ *   for a TPMLP_FLAG_SWIGLU context W1p is [k][2f][H] and b1 [2F], gate/up interleaved in
+ *   blocks of G rows (see tpmlp_pack_shards_swiglu).
  * *ptr receives a device pointer owned by the context; *bytes its size.
  * Errors: INVALID_ARG, NOT_PACKED.
  */

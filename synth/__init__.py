@@ -24,6 +24,7 @@ _SRC = os.path.join(_HERE, "synth.c")
 _LIB = os.path.join(_HERE, "_synth.so")
 
 STREAM_X, STREAM_W1, STREAM_B1, STREAM_W2, STREAM_B2 = 0, 1, 2, 3, 4
+STREAM_WU, STREAM_BU = 5, 6  # the up projection of the gated (SwiGLU) block
 
 
 def build(force: bool = False) -> str:
@@ -143,6 +144,16 @@ def make_inputs(H: int, F: int, M: int, seed: int, x_rows=None):
     W2 = normal_bf16(seed, STREAM_W2, (F, H), 1.0 / np.sqrt(F))
     b2 = normal_bf16(seed, STREAM_B2, (H,), 0.02)
     return {"X": X, "W1": W1, "b1": b1, "W2": W2, "b2": b2}
+
+
+def make_swiglu_inputs(H: int, F: int, M: int, seed: int, x_rows=None):
+    """Gated block: X, Wg = the W1 draw, bg = the b1 draw, Wu [H,F] and bu [F] from streams of
+    their own (same distributions as W1, b1), W2, b2."""
+    d = make_inputs(H, F, M, seed, x_rows=x_rows)
+    return {"X": d["X"], "Wg": d["W1"], "bg": d["b1"],
+            "Wu": normal_bf16(seed, STREAM_WU, (H, F), 1.0 / np.sqrt(H)),
+            "bu": normal_bf16(seed, STREAM_BU, (F,), 0.02),
+            "W2": d["W2"], "b2": d["b2"]}
 
 
 def workload_inputs(w: Workload, x_rows=None):

@@ -22,7 +22,7 @@ __all__ = [
     "tpmlp_strerror", "tpmlp_last_error", "tpmlp_launch_count",
     "TPMLP_OK", "TPMLP_ERR_INVALID_ARG", "TPMLP_ERR_UNSUPPORTED_SHAPE", "TPMLP_ERR_NOT_PACKED",
     "TPMLP_ERR_CUDA", "TPMLP_ERR_OOM", "TPMLP_ERR_DEVICE_TIMEOUT", "TPMLP_ERR_ARCH",
-    "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM",
+    "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM", "TPMLP_FLAG_SWIGLU", "tpmlp_pack_shards_swiglu",
 ]
 
 TPMLP_OK = 0
@@ -36,6 +36,7 @@ TPMLP_ERR_ARCH = -7
 TPMLP_ERR_MISALIGNED = -8
 TPMLP_FLAG_Z_FP32 = 0x1
 TPMLP_FLAG_SINGLE_SM = 0x2
+TPMLP_FLAG_SWIGLU = 0x4
 TPMLP_NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's fixed scratch for tpmlp_forward_noalloc
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -71,6 +72,7 @@ def load_library() -> ctypes.CDLL:
     sig = {
         "tpmlp_create": ([ctypes.POINTER(vp), i64, i64, i32, u32], ctypes.c_int),
         "tpmlp_pack_shards": ([vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "tpmlp_pack_shards_swiglu": ([vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "tpmlp_reserve": ([vp, i64], ctypes.c_int),
         "tpmlp_forward": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_forward_host": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
@@ -140,6 +142,12 @@ def tpmlp_create(H: int, F: int, k: int, flags: int = 0) -> int:
 def tpmlp_pack_shards(ctx: int, W1, b1, W2, b2, stream=None) -> None:
     _check(load_library().tpmlp_pack_shards(ctx, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
                                             _stream(stream)), "tpmlp_pack_shards", ctx)
+
+
+def tpmlp_pack_shards_swiglu(ctx: int, Wg, bg, Wu, bu, W2, b2, stream=None) -> None:
+    _check(load_library().tpmlp_pack_shards_swiglu(ctx, _ptr(Wg), _ptr(bg), _ptr(Wu), _ptr(bu),
+                                                   _ptr(W2), _ptr(b2), _stream(stream)),
+           "tpmlp_pack_shards_swiglu", ctx)
 
 
 def tpmlp_reserve(ctx: int, max_tokens: int) -> None:
@@ -217,10 +225,13 @@ class TPMLP:
         Z = mlp(X)                     # X bf16 [B, S, H] -> Z [B, S, H]
     """
 
-    def __init__(self, H: int, F: int, k: int, z_fp32: bool = False, single_sm: bool = False):
+    def __init__(self, H: int, F: int, k: int, z_fp32: bool = False, single_sm: bool = False,
+                 swiglu: bool = False):
         self.H, self.F, self.k = H, F, k
         self.z_fp32 = z_fp32
-        flags = (TPMLP_FLAG_Z_FP32 if z_fp32 else 0) | (TPMLP_FLAG_SINGLE_SM if single_sm else 0)
+        self.swiglu = swiglu
+        flags = ((TPMLP_FLAG_Z_FP32 if z_fp32 else 0) | (TPMLP_FLAG_SINGLE_SM if single_sm else 0)
+                 | (TPMLP_FLAG_SWIGLU if swiglu else 0))
         self.ctx = tpmlp_create(H, F, k, flags)
 
     def close(self):
@@ -257,6 +268,16 @@ class TPMLP:
         self._require(W2, bf, (self.F, self.H), "W2")
         self._require(b2, bf, (self.H,), "b2")
         tpmlp_pack_shards(self.ctx, W1, b1, W2, b2, stream)
+
+    def pack_swiglu(self, Wg, bg, Wu, bu, W2, b2, stream=None):
+        """Gated block: Y = SiLU(X Wg + bg) * (X Wu + bu), then the row-parallel W2."""
+        import torch
+        bf = torch.bfloat16
+        for t, shape, name in ((Wg, (self.H, self.F), "Wg"), (bg, (self.F,), "bg"),
+                               (Wu, (self.H, self.F), "Wu"), (bu, (self.F,), "bu"),
+                               (W2, (self.F, self.H), "W2"), (b2, (self.H,), "b2")):
+            self._require(t, bf, shape, name)
+        tpmlp_pack_shards_swiglu(self.ctx, Wg, bg, Wu, bu, W2, b2, stream)
 
     def reserve(self, max_tokens: int):
         tpmlp_reserve(self.ctx, max_tokens)

@@ -26,14 +26,16 @@ struct tpmlp_ctx {
     uint32_t flags = 0;
     int bn1 = 0, bn2 = 0;  // output tile widths of GEMM1 / GEMM2
 
-    uint16_t* W1p = nullptr;  // [k][f][H]
+    uint16_t* W1p = nullptr;  // [k][f][H]  (gated: [k][2f][H])
     uint16_t* W2p = nullptr;  // [k][H][f]
-    float* b1 = nullptr;      // [F]
+    float* b1 = nullptr;      // [F]        (gated: [2F])
     float* b2 = nullptr;      // [H]
     bool packed = false;
     CUtensorMap tmW1{}, tmW2{};            // B boxes for the single-SM kernel (BN rows)
     CUtensorMap tmW1_pair{}, tmW2_pair{};  // B boxes for the CTA-pair kernel (128 rows)
     bool pair1 = false, pair2 = false;     // GEMM1 / GEMM2 run on CTA pairs
+    bool gated = false;  // SwiGLU block: W1p holds gate and up rows interleaved
+    int gate_block = 0;  // G: gate/up interleave block (output columns per half-tile)
 
     uint16_t* Y = nullptr;  // [y_rows][F] intermediate activations
     int64_t y_rows = 0;
@@ -248,12 +250,23 @@ int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
     if (rc) return rc;
     const CUtensorMap& tmX = c->tmX;
     const bool pair = c->pair1;
+    const int tile_rows_b = pair ? tpmlp::kPairBN : c->bn1;  // B rows (output columns) per tile
     GemmArgs a = base_args(c, M, static_cast<int>(c->F), pair ? tpmlp::kPairBM : tpmlp::kBM,
-                           pair ? tpmlp::kPairBN : c->bn1, TPMLP_GROUP_M1);
+                           tile_rows_b, TPMLP_GROUP_M1);
     a.kb_tile = static_cast<int>(c->H / tpmlp::kBK);
     a.kb_shard = a.kb_tile;
     a.bias = c->b1;
     a.out = Y;
+    if (c->gated) {
+        // tiles walk the 2F packed rows; each yields half as many output columns
+        a.f = static_cast<int>(2 * c->f);
+        a.n_blocks = static_cast<int>(2 * c->F / tile_rows_b);
+        a.num_tiles = a.m_blocks * a.n_blocks;
+        if (pair)
+            return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1Gated, false>(
+                c, tmX, c->tmW1_pair, a, s);
+        return dispatch_gemm<Mode::kGemm1Gated, false>(c, c->bn1, tmX, c->tmW1, a, s);
+    }
     if (pair)
         return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1, false>(c, tmX,
                                                                                    c->tmW1_pair, a, s);
@@ -303,96 +316,31 @@ int check_tokens(int64_t B, int64_t S) {
 
 int z_elem_bytes(const tpmlp_ctx* c) { return (c->flags & TPMLP_FLAG_Z_FP32) ? 4 : 2; }
 
-}  // namespace
-
-extern "C" {
-
-int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flags) {
-    if (!out) return TPMLP_ERR_INVALID_ARG;
-    *out = nullptr;
-    if (H <= 0 || F <= 0 || k <= 0) return TPMLP_ERR_INVALID_ARG;
-    if (flags & ~(TPMLP_FLAG_Z_FP32 | TPMLP_FLAG_SINGLE_SM)) return TPMLP_ERR_INVALID_ARG;
-    if (H % 64 || F % 64 || F % k || (F / k) % 64) return TPMLP_ERR_UNSUPPORTED_SHAPE;
-    if (H > (int64_t(1) << 20) || F > (int64_t(1) << 22)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
-
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return TPMLP_ERR_CUDA;
-    cudaDeviceProp prop;
-    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return TPMLP_ERR_CUDA;
-    if (prop.major != 10 || prop.minor != 3) return TPMLP_ERR_ARCH;
-
-    tpmlp_ctx* c = new (std::nothrow) tpmlp_ctx();
-    if (!c) return TPMLP_ERR_OOM;
-    c->device = dev;
-    c->num_sms = prop.multiProcessorCount;
-    c->H = H;
-    c->F = F;
-    c->k = k;
-    c->f = F / k;
-    c->flags = flags;
-    c->bn1 = pick_bn(c->f);
-    c->bn2 = pick_bn(H);
-    // 256 x 256 tiles on CTA pairs wherever the output width allows it
-    c->pair1 = c->bn1 == 256 && !(flags & TPMLP_FLAG_SINGLE_SM);
-    c->pair2 = c->bn2 == 256 && !(flags & TPMLP_FLAG_SINGLE_SM);
-    int rc = TPMLP_OK;
-    cudaError_t e;
-    if ((e = cudaMalloc(&c->W1p, static_cast<size_t>(H) * F * 2)) != cudaSuccess ||
-        (e = cudaMalloc(&c->W2p, static_cast<size_t>(H) * F * 2)) != cudaSuccess ||
-        (e = cudaMalloc(&c->b1, static_cast<size_t>(F) * 4)) != cudaSuccess ||
-        (e = cudaMalloc(&c->b2, static_cast<size_t>(H) * 4)) != cudaSuccess ||
-        (e = cudaMalloc(&c->status, sizeof(int))) != cudaSuccess ||
-        (e = cudaMemset(c->status, 0, sizeof(int))) != cudaSuccess) {
-        rc = (e == cudaErrorMemoryAllocation) ? TPMLP_ERR_OOM : TPMLP_ERR_CUDA;
-        tpmlp_destroy(c);
-        return rc;
-    }
-    *out = c;
-    return TPMLP_OK;
-}
-
-int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* W2, const void* b2,
-                      void* stream) {
-    if (!c || !W1 || !b1 || !W2 || !b2) return TPMLP_ERR_INVALID_ARG;
-    if (!aligned16(W1) || !aligned16(W2) || (reinterpret_cast<uintptr_t>(b1) & 1) ||
-        (reinterpret_cast<uintptr_t>(b2) & 1))
-        return TPMLP_ERR_MISALIGNED;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// W2 [F][H] = k blocks [f][H] -> W2p [k][H][f]; b2 -> fp32.
+int pack_second_layer(tpmlp_ctx* c, const void* W2, const void* b2, cudaStream_t s) {
     const int T = tpmlp::kTransposeTile;
-    {
-        // W1 [H][F] -> W1p [F][H] (= [k][f][H]: shard i is rows [i f, (i+1) f))
-        dim3 grid(static_cast<unsigned>(c->F / T), static_cast<unsigned>(c->H / T), 1);
-        tpmlp::transpose_bf16_kernel<<<grid, dim3(64, 4), 0, s>>>(
-            static_cast<const uint16_t*>(W1), c->W1p, static_cast<int>(c->H),
-            static_cast<int>(c->F), 0, 0);
-        TPMLP_CUDA(c, cudaGetLastError());
-        ++c->launches;
-    }
-    {
-        // W2 [F][H] = k blocks [f][H] -> W2p [k][H][f]
-        dim3 grid(static_cast<unsigned>(c->H / T), static_cast<unsigned>(c->f / T),
-                  static_cast<unsigned>(c->k));
-        tpmlp::transpose_bf16_kernel<<<grid, dim3(64, 4), 0, s>>>(
-            static_cast<const uint16_t*>(W2), c->W2p, static_cast<int>(c->f),
-            static_cast<int>(c->H), static_cast<long long>(c->f) * c->H,
-            static_cast<long long>(c->f) * c->H);
-        TPMLP_CUDA(c, cudaGetLastError());
-        ++c->launches;
-    }
-    tpmlp::bf16_to_f32_kernel<<<static_cast<unsigned>((c->F + 255) / 256), 256, 0, s>>>(
-        static_cast<const uint16_t*>(b1), c->b1, c->F);
+    dim3 grid(static_cast<unsigned>(c->H / T), static_cast<unsigned>(c->f / T),
+              static_cast<unsigned>(c->k));
+    tpmlp::transpose_bf16_kernel<<<grid, dim3(64, 4), 0, s>>>(
+        static_cast<const uint16_t*>(W2), c->W2p, static_cast<int>(c->f), static_cast<int>(c->H),
+        static_cast<long long>(c->f) * c->H, static_cast<long long>(c->f) * c->H);
     TPMLP_CUDA(c, cudaGetLastError());
     tpmlp::bf16_to_f32_kernel<<<static_cast<unsigned>((c->H + 255) / 256), 256, 0, s>>>(
         static_cast<const uint16_t*>(b2), c->b2, c->H);
     TPMLP_CUDA(c, cudaGetLastError());
     c->launches += 2;
+    return TPMLP_OK;
+}
 
-    // tensor maps of the packed shards: box 64 (reduction) x BN (output columns) x 1 shard
+// Tensor maps of the packed shards: box 64 (reduction) x rows x 1 shard, for the single-SM
+// kernel (rows = its tile width) and for the CTA-pair kernel (rows = 128 per CTA).
+int encode_weight_maps(tpmlp_ctx* c) {
     {
-        const uint64_t dims[3] = {static_cast<uint64_t>(c->H), static_cast<uint64_t>(c->f),
+        const int64_t rows1 = c->gated ? 2 * c->f : c->f;  // packed rows per shard
+        const uint64_t dims[3] = {static_cast<uint64_t>(c->H), static_cast<uint64_t>(rows1),
                                   static_cast<uint64_t>(c->k)};
         const uint64_t strides[2] = {static_cast<uint64_t>(c->H) * 2,
-                                     static_cast<uint64_t>(c->f) * c->H * 2};
+                                     static_cast<uint64_t>(rows1) * c->H * 2};
         const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(c->bn1), 1};
         int rc = encode_map(c, &c->tmW1, c->W1p, 3, dims, strides, box);
         if (rc) return rc;
@@ -412,6 +360,119 @@ int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* 
         rc = encode_map(c, &c->tmW2_pair, c->W2p, 3, dims, strides, box_pair);
         if (rc) return rc;
     }
+    return TPMLP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flags) {
+    if (!out) return TPMLP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (H <= 0 || F <= 0 || k <= 0) return TPMLP_ERR_INVALID_ARG;
+    if (flags & ~(TPMLP_FLAG_Z_FP32 | TPMLP_FLAG_SINGLE_SM | TPMLP_FLAG_SWIGLU))
+        return TPMLP_ERR_INVALID_ARG;
+    if (H % 64 || F % 64 || F % k || (F / k) % 64) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (H > (int64_t(1) << 20) || F > (int64_t(1) << 22)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TPMLP_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return TPMLP_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return TPMLP_ERR_ARCH;
+
+    tpmlp_ctx* c = new (std::nothrow) tpmlp_ctx();
+    if (!c) return TPMLP_ERR_OOM;
+    c->device = dev;
+    c->num_sms = prop.multiProcessorCount;
+    c->H = H;
+    c->F = F;
+    c->k = k;
+    c->f = F / k;
+    c->flags = flags;
+    c->gated = (flags & TPMLP_FLAG_SWIGLU) != 0;
+    // gated: each first-GEMM tile holds G gate + G up columns of the same G outputs
+    c->gate_block = (c->f % 128 == 0) ? 128 : 64;
+    c->bn1 = c->gated ? 2 * c->gate_block : pick_bn(c->f);
+    c->bn2 = pick_bn(H);
+    // 256 x 256 tiles on CTA pairs wherever the output width allows it
+    c->pair1 = c->bn1 == 256 && !(flags & TPMLP_FLAG_SINGLE_SM);
+    c->pair2 = c->bn2 == 256 && !(flags & TPMLP_FLAG_SINGLE_SM);
+    int rc = TPMLP_OK;
+    cudaError_t e;
+    const size_t parts1 = c->gated ? 2 : 1;  // gate and up packed together
+    if ((e = cudaMalloc(&c->W1p, parts1 * H * F * 2)) != cudaSuccess ||
+        (e = cudaMalloc(&c->W2p, static_cast<size_t>(H) * F * 2)) != cudaSuccess ||
+        (e = cudaMalloc(&c->b1, parts1 * F * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&c->b2, static_cast<size_t>(H) * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&c->status, sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(c->status, 0, sizeof(int))) != cudaSuccess) {
+        rc = (e == cudaErrorMemoryAllocation) ? TPMLP_ERR_OOM : TPMLP_ERR_CUDA;
+        tpmlp_destroy(c);
+        return rc;
+    }
+    *out = c;
+    return TPMLP_OK;
+}
+
+int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* W2, const void* b2,
+                      void* stream) {
+    if (!c || !W1 || !b1 || !W2 || !b2 || c->gated) return TPMLP_ERR_INVALID_ARG;
+    if (!aligned16(W1) || !aligned16(W2) || (reinterpret_cast<uintptr_t>(b1) & 1) ||
+        (reinterpret_cast<uintptr_t>(b2) & 1))
+        return TPMLP_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int T = tpmlp::kTransposeTile;
+    c->packed = false;
+    {
+        // W1 [H][F] -> W1p [F][H] (= [k][f][H]: shard i is rows [i f, (i+1) f))
+        dim3 grid(static_cast<unsigned>(c->F / T), static_cast<unsigned>(c->H / T), 1);
+        tpmlp::transpose_bf16_kernel<<<grid, dim3(64, 4), 0, s>>>(
+            static_cast<const uint16_t*>(W1), c->W1p, static_cast<int>(c->H),
+            static_cast<int>(c->F), 0, 0);
+        TPMLP_CUDA(c, cudaGetLastError());
+        ++c->launches;
+    }
+    tpmlp::bf16_to_f32_kernel<<<static_cast<unsigned>((c->F + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint16_t*>(b1), c->b1, c->F);
+    TPMLP_CUDA(c, cudaGetLastError());
+    ++c->launches;
+    int rc = pack_second_layer(c, W2, b2, s);
+    if (rc) return rc;
+    if ((rc = encode_weight_maps(c))) return rc;
+    c->packed = true;
+    return TPMLP_OK;
+}
+
+int tpmlp_pack_shards_swiglu(tpmlp_ctx* c, const void* Wg, const void* bg, const void* Wu,
+                             const void* bu, const void* W2, const void* b2, void* stream) {
+    if (!c || !Wg || !bg || !Wu || !bu || !W2 || !b2 || !c->gated) return TPMLP_ERR_INVALID_ARG;
+    if (!aligned16(Wg) || !aligned16(Wu) || !aligned16(W2) ||
+        ((reinterpret_cast<uintptr_t>(bg) | reinterpret_cast<uintptr_t>(bu) |
+          reinterpret_cast<uintptr_t>(b2)) & 1))
+        return TPMLP_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int T = tpmlp::kTransposeTile;
+    c->packed = false;
+    const void* parts[2] = {Wg, Wu};
+    const void* biases[2] = {bg, bu};
+    for (int part = 0; part < 2; ++part) {
+        // gate (part 0) / up (part 1) [H][F] -> interleaved rows of W1p [k][2f][H]
+        dim3 grid(static_cast<unsigned>(c->F / T), static_cast<unsigned>(c->H / T), 1);
+        tpmlp::transpose_interleave_bf16_kernel<<<grid, dim3(64, 4), 0, s>>>(
+            static_cast<const uint16_t*>(parts[part]), c->W1p, static_cast<int>(c->H),
+            static_cast<int>(c->F), c->gate_block, part);
+        TPMLP_CUDA(c, cudaGetLastError());
+        tpmlp::interleave_bias_kernel<<<static_cast<unsigned>((c->F + 255) / 256), 256, 0, s>>>(
+            static_cast<const uint16_t*>(biases[part]), c->b1, static_cast<int>(c->F),
+            c->gate_block, part);
+        TPMLP_CUDA(c, cudaGetLastError());
+        c->launches += 2;
+    }
+    int rc = pack_second_layer(c, W2, b2, s);
+    if (rc) return rc;
+    if ((rc = encode_weight_maps(c))) return rc;
     c->packed = true;
     return TPMLP_OK;
 }
@@ -501,9 +562,9 @@ int tpmlp_packed_buffer(const tpmlp_ctx* c, int32_t which, const void** ptr, int
     if (!c || !ptr || !bytes) return TPMLP_ERR_INVALID_ARG;
     if (!c->packed) return TPMLP_ERR_NOT_PACKED;
     switch (which) {
-        case 0: *ptr = c->W1p; *bytes = c->H * c->F * 2; return TPMLP_OK;
+        case 0: *ptr = c->W1p; *bytes = (c->gated ? 2 : 1) * c->H * c->F * 2; return TPMLP_OK;
         case 1: *ptr = c->W2p; *bytes = c->H * c->F * 2; return TPMLP_OK;
-        case 2: *ptr = c->b1; *bytes = c->F * 4; return TPMLP_OK;
+        case 2: *ptr = c->b1; *bytes = (c->gated ? 2 : 1) * c->F * 4; return TPMLP_OK;
         case 3: *ptr = c->b2; *bytes = c->H * 4; return TPMLP_OK;
         default: return TPMLP_ERR_INVALID_ARG;
     }

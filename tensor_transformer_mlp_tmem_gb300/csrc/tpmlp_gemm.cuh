@@ -38,7 +38,11 @@ constexpr int kUmmaK = 16;      // reduction depth of one kind::f16 MMA
 constexpr int kNumThreads = 192;
 constexpr int kEpiWarps = 4;
 
-enum class Mode : int { kGemm1 = 1, kGemm2 = 2 };
+// kGemm1: Y = GeLU(acc + b1).  kGemm1Gated: the accumulator's column halves hold the gate and
+// the up projection of the same outputs, Y = SiLU(gate + bg) * (up + bu).  kGemm2: Z = acc + b2.
+enum class Mode : int { kGemm1 = 1, kGemm2 = 2, kGemm1Gated = 3 };
+
+__host__ __device__ constexpr bool is_gemm1(Mode m) { return m != Mode::kGemm2; }
 
 // Wait sites recorded in the status word when a bounded wait gives up: (mode << 8) | site.
 enum : int { kSiteProducer = 1, kSiteMmaAccum = 2, kSiteMmaFull = 3, kSiteEpilogue = 4 };
@@ -96,6 +100,9 @@ __device__ __forceinline__ float gelu_erf(float a) {
     return 0.5f * a * (1.0f + erff(a * 0.70710678118654752440f));
 }
 
+// SiLU(a) = a * sigma(a) = a / (1 + e^-a), with CUDA's expf.
+__device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // round to nearest even
     return *reinterpret_cast<uint32_t*>(&p);
@@ -136,6 +143,67 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const fl
                                 pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
                                 pack_bf16x2(x[8 * j + 4], x[8 * j + 5]),
                                 pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+    }
+}
+
+// One 32-column slice of one output row of the gated first layer: the gate values g and the up
+// values u of the same 32 outputs; Y = SiLU(g + bias_g) * (u + bias_u), rounded to bf16.
+__device__ __forceinline__ void epilogue_gated_slice(const uint32_t (&g)[32], const uint32_t (&u)[32],
+                                                     const float* __restrict__ bias_g,
+                                                     const float* __restrict__ bias_u,
+                                                     void* __restrict__ out, int row, int M, int ldo,
+                                                     int col) {
+    float x[32];
+    const float4* bg4 = reinterpret_cast<const float4*>(bias_g);
+    const float4* bu4 = reinterpret_cast<const float4*>(bias_u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float4 bg = __ldg(bg4 + j);
+        const float4 bu = __ldg(bu4 + j);
+        x[4 * j + 0] = silu(__uint_as_float(g[4 * j + 0]) + bg.x) * (__uint_as_float(u[4 * j + 0]) + bu.x);
+        x[4 * j + 1] = silu(__uint_as_float(g[4 * j + 1]) + bg.y) * (__uint_as_float(u[4 * j + 1]) + bu.y);
+        x[4 * j + 2] = silu(__uint_as_float(g[4 * j + 2]) + bg.z) * (__uint_as_float(u[4 * j + 2]) + bu.z);
+        x[4 * j + 3] = silu(__uint_as_float(g[4 * j + 3]) + bg.w) * (__uint_as_float(u[4 * j + 3]) + bu.w);
+    }
+    if (row >= M) return;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) +
+                                          static_cast<size_t>(row) * ldo + col);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        dst[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
+                            pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+}
+
+// Drain the accumulator columns [base, base + width) of this warp's 32 rows through the
+// epilogue. Releases the accumulator (arrive on `release_bar`, via `arrive`) once the last
+// columns are in registers. n0 is the tile's first column in B-row space; for the gated
+// layer the first half of the columns is the gate and the second half the up projection of
+// outputs [n0 / 2, n0 / 2 + width / 2).
+template <Mode MODE, bool OUT_F32, int WIDTH, typename Release>
+__device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs& args, int row,
+                                                  int n0, Release release) {
+    if constexpr (MODE == Mode::kGemm1Gated) {
+        constexpr int G = WIDTH / 2;
+#pragma unroll 1
+        for (int c = 0; c < G; c += 32) {
+            uint32_t g[32], u[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c, g);
+            ptx::tmem_ld_32x32b_x32(taddr + G + c, u);
+            ptx::tmem_wait_ld(g);
+            ptx::tmem_wait_ld(u);
+            if (c + 32 == G) release();
+            epilogue_gated_slice(g, u, args.bias + n0 + c, args.bias + n0 + G + c, args.out, row,
+                                 args.M, args.ldo, n0 / 2 + c);
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < WIDTH; c += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c, v);
+            ptx::tmem_wait_ld(v);
+            if (c + 32 == WIDTH) release();
+            epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo, n0 + c);
+        }
     }
 }
 
@@ -214,7 +282,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 decode_tile(args, t, m_blk, n_blk);
                 const int m0 = m_blk * kBM;
                 const int n0 = n_blk * BN;
-                const int shard1 = (MODE == Mode::kGemm1) ? n0 / args.f : 0;
+                const int shard1 = is_gemm1(MODE) ? n0 / args.f : 0;
                 const int n_in_shard1 = n0 - shard1 * args.f;
                 for (int kb = 0; kb < args.kb_tile; ++kb) {
                     if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status,
@@ -225,7 +293,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t sa = base + stage * L::kStageBytes;
                     const uint32_t sb = sa + L::kABytes;
                     ptx::mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
-                    if constexpr (MODE == Mode::kGemm1) {
+                    if constexpr (is_gemm1(MODE)) {
                         ptx::tma_load_2d(sa, &tmA, full_bar(stage), kb * kBK, m0);
                         ptx::tma_load_3d(sb, &tmB, full_bar(stage), kb * kBK, n_in_shard1, shard1);
                     } else {
@@ -310,20 +378,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::tc_fence_after();
             const int row = m0 + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(taddr + c, v);
-                ptx::tmem_wait_ld(v);
-                if (c + 32 == BN) {
-                    // all of this warp's accumulator columns are in registers: hand it back
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
-                }
-                epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo,
-                                              n0 + c);
-            }
+            const uint32_t empty = tempty_bar(acc);
+            drain_accumulator<MODE, OUT_F32, BN>(taddr, args, row, n0, [&] {
+                // all of this warp's accumulator columns are in registers: hand it back
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(empty);
+            });
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }

@@ -106,7 +106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;  // this CTA's A rows
                 const int n0 = n_blk * kPairBN;
                 const int nb = n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
-                const int shard1 = (MODE == Mode::kGemm1) ? n0 / args.f : 0;
+                const int shard1 = is_gemm1(MODE) ? n0 / args.f : 0;
                 const int nb_in_shard1 = nb - shard1 * args.f;
                 for (int kb = 0; kb < args.kb_tile; ++kb) {
                     if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status,
@@ -118,7 +118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     const uint32_t sb = sa + L::kABytes;
                     const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // rank 0's barrier
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
-                    if constexpr (MODE == Mode::kGemm1) {
+                    if constexpr (is_gemm1(MODE)) {
                         ptx::tma_load_2d_pair(sa, &tmA, fb, kb * kBK, m0);
                         ptx::tma_load_3d_pair(sb, &tmB, fb, kb * kBK, nb_in_shard1, shard1);
                     } else {
@@ -209,19 +209,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             const int row = m0 + q * 32 + lane;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kPairBN;
-#pragma unroll 1
-            for (int c = 0; c < kPairBN; c += 32) {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(taddr + c, v);
-                ptx::tmem_wait_ld(v);
-                if (c + 32 == kPairBN) {
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
-                }
-                epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo,
-                                              n0 + c);
-            }
+            const uint32_t empty = ptx::mapa_shared(tempty_bar(acc), 0);  // rank 0's barrier
+            drain_accumulator<MODE, OUT_F32, kPairBN>(taddr, args, row, n0, [&] {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(empty);
+            });
             if (++acc == NUM_ACC) {
                 acc = 0;
                 acc_phase ^= 1u;

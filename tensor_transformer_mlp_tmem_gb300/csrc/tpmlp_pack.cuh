@@ -41,6 +41,41 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Gated first layer: the gate and the up projection are packed into one K-major operand whose
+// rows alternate in blocks of G: for output column j (0 <= j < F) of part p (0 = gate,
+// 1 = up), the packed row is (j / G) * 2G + p * G + (j % G). With G dividing the shard width
+// f, shard i's 2f packed rows are [2 i f, 2 (i+1) f) and every 2G-row tile holds the gate and
+// the up columns of the same G outputs.
+//   out[(j / G) * 2G + p * G + (j % G)][r] = in[r][j]      (in: [R][C] bf16, out rows of R)
+__global__ void __launch_bounds__(256)
+    transpose_interleave_bf16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
+                                     int R, int C, int G, int part) {
+    __shared__ uint16_t tile[kTransposeTile][kTransposeTile + 2];
+    const int r0 = blockIdx.y * kTransposeTile;
+    const int c0 = blockIdx.x * kTransposeTile;
+    const int tx = threadIdx.x;  // 0..63
+    for (int i = threadIdx.y; i < kTransposeTile; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + tx;
+        if (r < R && c < C) tile[i][tx] = in[static_cast<size_t>(r) * C + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < kTransposeTile; i += blockDim.y) {
+        const int j = c0 + i, r = r0 + tx;
+        if (j < C && r < R) {
+            const size_t row = static_cast<size_t>(j / G) * 2 * G + static_cast<size_t>(part) * G + j % G;
+            out[row * R + r] = tile[tx][i];
+        }
+    }
+}
+
+// The biases of the gated layer in the same interleaved order (widened to fp32).
+__global__ void interleave_bias_kernel(const uint16_t* __restrict__ in, float* __restrict__ out,
+                                       int C, int G, int part) {
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < C; j += gridDim.x * blockDim.x)
+        out[static_cast<size_t>(j / G) * 2 * G + static_cast<size_t>(part) * G + j % G] =
+            __uint_as_float(static_cast<uint32_t>(in[j]) << 16);
+}
+
 __global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ in, float* __restrict__ out,
                                    long long n) {
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;

@@ -196,10 +196,7 @@ def pin_x_linear_without_activation(orc):
 # ---------------------------------------------------------------------------------
 # gated (SwiGLU) variant
 def _small_swiglu(seed=17, H=64, F=256, M=29):
-    d = synth.make_inputs(H, F, M, seed)
-    extra = synth.make_inputs(H, F, 1, seed + 1000)  # a second, independent W1 / b1 for "up"
-    d = {"X": d["X"], "Wg": d["W1"], "bg": d["b1"], "Wu": extra["W1"], "bu": extra["b1"],
-         "W2": d["W2"], "b2": d["b2"]}
+    d = synth.make_swiglu_inputs(H, F, M, seed)
     return d, {k: synth.bf16_to_f64(v) for k, v in d.items()}
 
 
