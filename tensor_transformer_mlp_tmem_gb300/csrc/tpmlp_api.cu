@@ -173,7 +173,10 @@ int dispatch_gemm(tpmlp_ctx* c, int bn, const CUtensorMap& a, const CUtensorMap&
     switch (bn) {
         case 256: return launch_gemm<256, TPMLP_STAGES_256, MODE, F32>(c, a, b, args, s);
         case 128: return launch_gemm<128, 6, MODE, F32>(c, a, b, args, s);
-        default: return launch_gemm<64, 8, MODE, F32>(c, a, b, args, s);
+        default:
+            // the gated layer's tiles hold 2 x 64 columns at least
+            if constexpr (MODE == Mode::kGemm1Gated) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+            else return launch_gemm<64, 8, MODE, F32>(c, a, b, args, s);
     }
 }
 

@@ -11,8 +11,9 @@
 //               K-major, 128-byte swizzled) into a STAGES-deep shared-memory ring.
 //   warp 1      allocates tensor memory (2 x BN fp32 columns: two accumulators) and, from
 //               one lane, issues tcgen05.mma (M = 128, N = BN, K = 16 per instruction).
-//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (each warp owns the 32
-//               TMEM lanes = output rows its warp rank may access), bias, GeLU (GEMM1),
+//   warps 2..   epilogue (4 or 8 warps): tcgen05.ld of the finished accumulator (each warp
+//               owns the 32 TMEM lanes = output rows its warp rank may access; with 8 warps
+//               two share a lane quadrant and split its columns), bias, GeLU (GEMM1),
 //               conversion and stores. The accumulator is handed back to the MMA warp as
 //               soon as it has been read, so the next tile's MMAs overlap this epilogue.
 //
@@ -35,8 +36,15 @@ namespace tpmlp {
 constexpr int kBM = 128;        // output rows per tile = TMEM lanes
 constexpr int kBK = 64;         // reduction depth per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;      // reduction depth of one kind::f16 MMA
-constexpr int kNumThreads = 192;
-constexpr int kEpiWarps = 4;
+// Epilogue warps: 4 (one per TMEM lane quadrant) or 8 (two per quadrant, each draining half
+// of the accumulator's columns).
+#ifndef TPMLP_EPI_WARPS
+#define TPMLP_EPI_WARPS 8
+#endif
+constexpr int kEpiWarps = TPMLP_EPI_WARPS;
+constexpr int kEpiParts = kEpiWarps / 4;  // column parts per lane quadrant
+constexpr int kNumThreads = 64 + 32 * kEpiWarps;
+static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
 
 // kGemm1: Y = GeLU(acc + b1).  kGemm1Gated: the accumulator's column halves hold the gate and
 // the up projection of the same outputs, Y = SiLU(gate + bg) * (up + bu).  kGemm2: Z = acc + b2.
@@ -179,29 +187,36 @@ __device__ __forceinline__ void epilogue_gated_slice(const uint32_t (&g)[32], co
 // columns are in registers. n0 is the tile's first column in B-row space; for the gated
 // layer the first half of the columns is the gate and the second half the up projection of
 // outputs [n0 / 2, n0 / 2 + width / 2).
+// `part` (0 .. kEpiParts-1) selects which share of the columns this warp drains.
 template <Mode MODE, bool OUT_F32, int WIDTH, typename Release>
 __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs& args, int row,
-                                                  int n0, Release release) {
+                                                  int n0, int part, Release release) {
     if constexpr (MODE == Mode::kGemm1Gated) {
         constexpr int G = WIDTH / 2;
+        constexpr int kCols = G / kEpiParts;
+        static_assert(kCols % 32 == 0, "gated epilogue slice");
+        const int c0 = part * kCols;
 #pragma unroll 1
-        for (int c = 0; c < G; c += 32) {
+        for (int c = c0; c < c0 + kCols; c += 32) {
             uint32_t g[32], u[32];
             ptx::tmem_ld_32x32b_x32(taddr + c, g);
             ptx::tmem_ld_32x32b_x32(taddr + G + c, u);
             ptx::tmem_wait_ld(g);
             ptx::tmem_wait_ld(u);
-            if (c + 32 == G) release();
+            if (c + 32 == c0 + kCols) release();
             epilogue_gated_slice(g, u, args.bias + n0 + c, args.bias + n0 + G + c, args.out, row,
                                  args.M, args.ldo, n0 / 2 + c);
         }
     } else {
+        constexpr int kCols = WIDTH / kEpiParts;
+        static_assert(kCols % 32 == 0, "epilogue slice");
+        const int c0 = part * kCols;
 #pragma unroll 1
-        for (int c = 0; c < WIDTH; c += 32) {
+        for (int c = c0; c < c0 + kCols; c += 32) {
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(taddr + c, v);
             ptx::tmem_wait_ld(v);
-            if (c + 32 == WIDTH) release();
+            if (c + 32 == c0 + kCols) release();
             epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo, n0 + c);
         }
     }
@@ -366,6 +381,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     } else {
         // ------------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lanes [32q, 32q+32) = tile rows this warp may read
+        const int part = (warp - 2) >> 2;  // which share of the columns
         uint32_t acc = 0, acc_phase = 0;
         for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
             int m_blk, n_blk;
@@ -379,7 +395,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int row = m0 + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             const uint32_t empty = tempty_bar(acc);
-            drain_accumulator<MODE, OUT_F32, BN>(taddr, args, row, n0, [&] {
+            drain_accumulator<MODE, OUT_F32, BN>(taddr, args, row, n0, part, [&] {
                 // all of this warp's accumulator columns are in registers: hand it back
                 ptx::tc_fence_before();
                 __syncwarp();

@@ -18,7 +18,7 @@
 //   full[s]   (rank 0)  rank 0 arms it with both CTAs' bytes; both CTAs' TMA loads complete on it
 //   empty[s]  (both)    the MMA thread's multicast commit frees stage s in both CTAs
 //   tfull[a]  (both)    multicast commit: accumulator a is complete in both CTAs
-//   tempty[a] (rank 0)  8 arrivals (4 epilogue warps per CTA): accumulator a has been read
+//   tempty[a] (rank 0)  one arrival per epilogue warp of both CTAs: accumulator a has been read
 // All waits are bounded (ptx::mbar_wait); see tpmlp_gemm.cuh for the abort protocol.
 #pragma once
 
@@ -196,6 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     } else {
         // ------------------------------------------------------------- epilogue (both CTAs)
         const int q = warp & 3;
+        const int part = (warp - 2) >> 2;
         uint32_t acc = 0, acc_phase = 0;
         for (int t = pair; t < args.num_tiles; t += num_pairs) {
             int m_blk, n_blk;
@@ -210,7 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kPairBN;
             const uint32_t empty = ptx::mapa_shared(tempty_bar(acc), 0);  // rank 0's barrier
-            drain_accumulator<MODE, OUT_F32, kPairBN>(taddr, args, row, n0, [&] {
+            drain_accumulator<MODE, OUT_F32, kPairBN>(taddr, args, row, n0, part, [&] {
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive_cluster(empty);
