@@ -14,6 +14,8 @@ What it computes (the pages' definition of the Megatron MLP block):
                                would (same page, "方案二：按行切分权重矩阵", Z = Y1V1 + Y2V2;
                                大模型分布式并行策略详解 §4.1; AI大模型分布式训练 §2.2)
 with GeLU(a) = a/2 (1 + erf(a/sqrt 2)) (reading: the exact form) and b2 added once.
+The layer around the block: Z = X + MLP(LayerNorm(X)) (residual of AI大模型分布式训练 §3.4,
+LayerNorm on the full hidden vector before the block, 大模型分布式并行策略详解 §4.2).
 The gated variant (gate_up_proj column-parallel, down_proj row-parallel: 大模型分布式优化技术（一）
 §5.1, AI大模型分布式训练 §6.1) replaces GeLU(X W1 + b1) by SiLU(X Wg + bg) * (X Wu + bu).
 
@@ -64,6 +66,9 @@ class Oracle:
         lib.oracle_tpmlp_swiglu_f64.restype = ctypes.c_int
         lib.oracle_silu.argtypes = [ctypes.c_double]
         lib.oracle_silu.restype = ctypes.c_double
+        lib.oracle_block_f64.argtypes = [vp, i64, vp, i64, vp, vp, ctypes.c_double, vp, vp, vp, vp,
+                                         i64, i64, i32, vp, vp]
+        lib.oracle_block_f64.restype = ctypes.c_int
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ctypes.c_int
         self.lib = lib
@@ -141,6 +146,32 @@ class Oracle:
         return out
 
 
+    def block(self, X, gamma, beta, eps: float, W1, b1, W2, b2, k: int, rows=None,
+              want_xn: bool = False):
+        """Pre-LayerNorm sub-layer Z = X + MLP(LN(X)) in fp64 (gamma, beta [H] bf16)."""
+        X, gamma, beta, W1, b1, W2, b2 = (_u16(a) for a in (X, gamma, beta, W1, b1, W2, b2))
+        x_rows, H = X.shape
+        F = W1.shape[1]
+        if (W1.shape != (H, F) or W2.shape != (F, H) or gamma.shape != (H,) or beta.shape != (H,)
+                or b1.shape != (F,) or b2.shape != (H,)):
+            raise ValueError("shape mismatch")
+        rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        R = x_rows if rows_arr is None else len(rows_arr)
+        Z = np.empty((R, H), dtype=np.float64)
+        Xn = np.empty((R, H), dtype=np.float64) if want_xn else None
+        rc = self.lib.oracle_block_f64(
+            X.ctypes.data, x_rows, None if rows_arr is None else rows_arr.ctypes.data, R,
+            gamma.ctypes.data, beta.ctypes.data, float(eps), W1.ctypes.data, b1.ctypes.data,
+            W2.ctypes.data, b2.ctypes.data, H, F, k, Z.ctypes.data,
+            None if Xn is None else Xn.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        out = {"Z": Z}
+        if want_xn:
+            out["Xn"] = Xn
+        return out
+
+
 def _u16(a) -> np.ndarray:
     a = np.ascontiguousarray(a)
     if a.dtype != np.uint16:
@@ -194,3 +225,7 @@ def silu(a: float) -> float:
 
 def tpmlp_swiglu(X, Wg, bg, Wu, bu, W2, b2, k: int, rows=None, want_y: bool = False):
     return default().tpmlp_swiglu(X, Wg, bg, Wu, bu, W2, b2, k, rows=rows, want_y=want_y)
+
+
+def block(X, gamma, beta, eps, W1, b1, W2, b2, k: int, rows=None, want_xn: bool = False):
+    return default().block(X, gamma, beta, eps, W1, b1, W2, b2, k, rows=rows, want_xn=want_xn)

@@ -221,6 +221,98 @@ int oracle_tpmlp_swiglu_f64(const uint16_t *X, int64_t x_rows, const int64_t *ro
     return failed ? -1 : 0;
 }
 
+/*
+ * The steps either side of the block inside a Transformer layer: the layer adds the MLP's
+ * output to its input, x = x + mlp(x) (AI大模型分布式训练 §3.4, TransformerBlock.forward), and
+ * LayerNorm normalises each token's full hidden vector before the block (大模型分布式并行策略详解
+ * §4.2: LayerNorm needs the whole hidden state; AI大模型分布式训练 §4.2: sequence parallelism
+ * splits LayerNorm along the tokens, which are independent).
+ * Reading: the pre-LayerNorm sub-layer Z = X + MLP(LN(X)) with the standard LayerNorm
+ *   LN(x)_h = (x_h - mu) / sqrt(var + eps) * gamma_h + beta_h,
+ *   mu = (1/H) sum_h x_h,  var = (1/H) sum_h (x_h - mu)^2   (biased variance)
+ * and MLP = the GeLU block above (k shards, sum over shards, + b2).
+ *   Xn  out or NULL, double [R][H]: LN(X) of the selected rows
+ */
+int oracle_block_f64(const uint16_t *X, int64_t x_rows, const int64_t *rows, int64_t R,
+                     const uint16_t *gamma, const uint16_t *beta, double eps,
+                     const uint16_t *W1, const uint16_t *b1, const uint16_t *W2,
+                     const uint16_t *b2, int64_t H, int64_t F, int32_t k, double *Z, double *Xn) {
+    if (!X || !gamma || !beta || !W1 || !b1 || !W2 || !b2 || !Z || H <= 0 || F <= 0 || k <= 0 ||
+        R < 0 || eps < 0.0)
+        return -1;
+    if (F % k != 0) return -1;
+    const int64_t f = F / k;
+    int failed = 0;
+
+#pragma omp parallel
+    {
+        double *xn = (double *)malloc(sizeof(double) * (size_t)H);
+        double *acc = (double *)malloc(sizeof(double) * (size_t)f);
+        double *part = (double *)malloc(sizeof(double) * (size_t)H);
+        double *zsum = (double *)malloc(sizeof(double) * (size_t)H);
+        if (!xn || !acc || !part || !zsum) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < R; ++r) {
+                const int64_t m = rows ? rows[r] : r;
+                if (m < 0 || m >= x_rows) {
+#pragma omp atomic write
+                    failed = 1;
+                    continue;
+                }
+                const uint16_t *x = X + m * H;
+
+                /* LayerNorm of the token's hidden vector */
+                double mu = 0.0;
+                for (int64_t h = 0; h < H; ++h) mu += widen_bf16(x[h]);
+                mu /= (double)H;
+                double var = 0.0;
+                for (int64_t h = 0; h < H; ++h) {
+                    const double d = widen_bf16(x[h]) - mu;
+                    var += d * d;
+                }
+                var /= (double)H;
+                const double inv = 1.0 / sqrt(var + eps);
+                for (int64_t h = 0; h < H; ++h) {
+                    xn[h] = (widen_bf16(x[h]) - mu) * inv * widen_bf16(gamma[h]) + widen_bf16(beta[h]);
+                    if (Xn) Xn[r * H + h] = xn[h];
+                }
+
+                /* the block on LN(x) */
+                for (int64_t n = 0; n < H; ++n) zsum[n] = 0.0;
+                for (int32_t i = 0; i < k; ++i) {
+                    const int64_t j0 = (int64_t)i * f;
+                    for (int64_t jj = 0; jj < f; ++jj) acc[jj] = 0.0;
+                    for (int64_t h = 0; h < H; ++h) {
+                        const double xh = xn[h];
+                        const uint16_t *w = W1 + h * F + j0;
+                        for (int64_t jj = 0; jj < f; ++jj) acc[jj] += xh * widen_bf16(w[jj]);
+                    }
+                    for (int64_t jj = 0; jj < f; ++jj)
+                        acc[jj] = oracle_gelu(acc[jj] + widen_bf16(b1[j0 + jj]));
+                    for (int64_t n = 0; n < H; ++n) part[n] = 0.0;
+                    for (int64_t jj = 0; jj < f; ++jj) {
+                        const double y = acc[jj];
+                        const uint16_t *w = W2 + (j0 + jj) * H;
+                        for (int64_t n = 0; n < H; ++n) part[n] += y * widen_bf16(w[n]);
+                    }
+                    for (int64_t n = 0; n < H; ++n) zsum[n] += part[n];
+                }
+                /* residual: the sub-layer's input plus the block's output */
+                for (int64_t n = 0; n < H; ++n)
+                    Z[r * H + n] = widen_bf16(x[n]) + (zsum[n] + widen_bf16(b2[n]));
+            }
+        }
+        free(xn);
+        free(acc);
+        free(part);
+        free(zsum);
+    }
+    return failed ? -1 : 0;
+}
+
 int oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -267,6 +267,75 @@ def pin_swiglu_k_invariance(orc):
         assert _rel_fro(_swiglu(orc, d, k)["Z"], z1) <= 1e-12, k
 
 
+# ---------------------------------------------------------------------------------
+# the sub-layer around the block: Z = X + MLP(LayerNorm(X))
+def _ln_params(H, seed=5):
+    g = synth.normal_bf16(seed, 40, (H,), 0.5, mean=1.0)
+    b = synth.normal_bf16(seed, 41, (H,), 0.1)
+    return g, b
+
+
+def pin_layernorm_golden(orc):
+    t = _load("layernorm_h4.json")
+    X = _bits([t["x"]])
+    zeros4 = _bits([0.0] * 4)
+    W = _bits(np.zeros((4, 4)))
+    r = orc.block(X, _bits(t["gamma"]), _bits(t["beta"]), 0.0, W, zeros4, W, zeros4, 2,
+                  want_xn=True)
+    s = t["inv_sqrt5"]
+    for h, (a, b) in enumerate(t["xn_in_units_of_inv_sqrt5"]):
+        assert abs(r["Xn"][0, h] - (a * s + b)) <= 1e-15, h
+    assert np.array_equal(r["Z"], synth.bf16_to_f64(X))  # W2 = 0, b2 = 0: Z = X
+
+
+def pin_layernorm_matches_torch(orc):
+    """LN(X) against torch.nn.functional.layer_norm in float64 (an independent routine)."""
+    import torch
+    d, f = _small(H=256, F=512, M=21)
+    g, b = _ln_params(256)
+    r = orc.block(d["X"], g, b, 1e-5, d["W1"], d["b1"], d["W2"], d["b2"], 4, want_xn=True)
+    ref = torch.nn.functional.layer_norm(
+        torch.from_numpy(f["X"]), (256,), torch.from_numpy(synth.bf16_to_f64(g)),
+        torch.from_numpy(synth.bf16_to_f64(b)), eps=1e-5).numpy()
+    assert np.max(np.abs(r["Xn"] - ref)) <= 1e-12
+
+
+def pin_layernorm_scale_invariance(orc):
+    """With eps = 0, LN(2x) = LN(x) (doubling is exact)."""
+    d, _ = _small(H=128, F=256, M=9)
+    g, b = _ln_params(128)
+    X2 = synth.round_bf16(2.0 * synth.bf16_to_f64(d["X"]))
+    r1 = orc.block(d["X"], g, b, 0.0, d["W1"], d["b1"], d["W2"], d["b2"], 2, want_xn=True)
+    r2 = orc.block(X2, g, b, 0.0, d["W1"], d["b1"], d["W2"], d["b2"], 2, want_xn=True)
+    assert np.max(np.abs(r1["Xn"] - r2["Xn"])) <= 1e-13
+
+
+def pin_block_is_residual_plus_mlp(orc):
+    """Z - X = GeLU(LN(X) W1 + b1) W2 + b2 (torch LayerNorm, numpy matmul, scipy ndtr)."""
+    import torch
+    from scipy.special import ndtr
+    d, f = _small(H=128, F=512, M=17)
+    g, b = _ln_params(128)
+    r = orc.block(d["X"], g, b, 1e-5, d["W1"], d["b1"], d["W2"], d["b2"], 4)
+    xn = torch.nn.functional.layer_norm(
+        torch.from_numpy(f["X"]), (128,), torch.from_numpy(synth.bf16_to_f64(g)),
+        torch.from_numpy(synth.bf16_to_f64(b)), eps=1e-5).numpy()
+    A = xn @ f["W1"] + f["b1"]
+    mlp = (A * ndtr(A)) @ f["W2"] + f["b2"]
+    assert _rel_fro(r["Z"] - f["X"], mlp) <= 1e-12
+
+
+def pin_block_zero_mlp_is_identity(orc):
+    d, f = _small()
+    g, b = _ln_params(64)
+    r = orc.block(d["X"], g, b, 1e-5, d["W1"], d["b1"], np.zeros_like(d["W2"]),
+                  np.zeros_like(d["b2"]), 4)
+    assert np.array_equal(r["Z"], f["X"])
+
+
+BLOCK_PINS = [pin_layernorm_golden, pin_layernorm_matches_torch, pin_layernorm_scale_invariance,
+              pin_block_is_residual_plus_mlp, pin_block_zero_mlp_is_identity]
+
 SWIGLU_PINS = [pin_silu_table_and_expit, pin_silu_odd_part, pin_swiglu_bruteforce_golden,
                pin_swiglu_matches_numpy, pin_swiglu_gate_only, pin_swiglu_k_invariance]
 
@@ -274,4 +343,4 @@ ALL_PINS = [
     pin_gelu_table, pin_gelu_ndtr, pin_gelu_odd_part, pin_bruteforce_golden,
     pin_identity_matches_numpy, pin_concat_identity, pin_row_split_sum, pin_k_invariance,
     pin_w2_zero, pin_w1_zero, pin_rows_independent, pin_x_linear_without_activation,
-] + SWIGLU_PINS
+] + SWIGLU_PINS + BLOCK_PINS

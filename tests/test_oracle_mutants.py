@@ -40,6 +40,16 @@ MUTANTS = {
                                "const double u = au[jj];"),
     "swiglu_up_without_shard_offset": ("const uint16_t *wu = Wu + h * F + j0;",
                                        "const uint16_t *wu = Wu + h * F;"),
+    "ln_unbiased_variance": ("var /= (double)H;", "var /= (double)(H - 1);"),
+    "ln_no_mean_subtraction": ("xn[h] = (widen_bf16(x[h]) - mu) * inv", "xn[h] = widen_bf16(x[h]) * inv"),
+    "ln_gamma_dropped": ("* inv * widen_bf16(gamma[h]) + widen_bf16(beta[h]);",
+                         "* inv + widen_bf16(beta[h]);"),
+    "ln_eps_outside_sqrt": ("const double inv = 1.0 / sqrt(var + eps);",
+                            "const double inv = 1.0 / (sqrt(var) + eps);"),
+    "residual_dropped": ("Z[r * H + n] = widen_bf16(x[n]) + (zsum[n] + widen_bf16(b2[n]));",
+                         "Z[r * H + n] = (zsum[n] + widen_bf16(b2[n]));"),
+    "residual_of_normalised_input": ("Z[r * H + n] = widen_bf16(x[n]) + (zsum[n]",
+                                     "Z[r * H + n] = xn[n] + (zsum[n]"),
     "activation_dropped": ("acc[jj] = (act == ORACLE_ACT_GELU) ? oracle_gelu(a) : a;",
                               "acc[jj] = a;"),
 }
