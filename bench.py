@@ -46,8 +46,9 @@ def log(*a):
 
 def step_flops(w: synth.Workload, variant: str) -> int:
     """FLOPs of one forward pass: 2*M*H*F per contraction (the gated block's first GEMM
-    computes the gate and the up projection: twice that)."""
-    return w.flops if variant == "gelu" else 6 * w.M * w.H * w.F
+    computes the gate and the up projection: twice that). LayerNorm and the residual add
+    are O(M*H) and not counted."""
+    return 6 * w.M * w.H * w.F if variant == "swiglu" else w.flops
 
 
 def kernel_flops(w: synth.Workload, variant: str, kernel: str) -> int:
@@ -59,6 +60,10 @@ def workload_config(w: synth.Workload, extra=None, variant: str = "gelu") -> dic
     if variant == "gelu":
         desc = (f"{w.name} TP-MLP: X [B={w.B},S={w.S},H={w.H}] bf16, W1 [{w.H},{w.F}], "
                 f"W2 [{w.F},{w.H}], erf GeLU, k={w.k} shards, seeded synthetic")
+    elif variant == "block":
+        desc = (f"{w.name} TP-MLP layer Z = X + MLP(LayerNorm(X)): X [B={w.B},S={w.S},H={w.H}] "
+                f"bf16, W1 [{w.H},{w.F}], W2 [{w.F},{w.H}], erf GeLU, k={w.k} shards, seeded "
+                f"synthetic")
     else:
         desc = (f"{w.name} gated TP-MLP: X [B={w.B},S={w.S},H={w.H}] bf16, Wg and Wu "
                 f"[{w.H},{w.F}], W2 [{w.F},{w.H}], SwiGLU, k={w.k} shards, seeded synthetic")
@@ -144,10 +149,18 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
+def ln_params(H: int):
+    return (synth.normal_bf16(5, 40, (H,), 0.5, mean=1.0), synth.normal_bf16(5, 41, (H,), 0.1))
+
+
 def run_oracle(w: synth.Workload, d: dict, rows, variant: str):
     import oracle
     if variant == "gelu":
         return oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=rows)
+    if variant == "block":
+        g, b = ln_params(w.H)
+        return oracle.block(d["X"], g, b, 1e-5, d["W1"], d["b1"], d["W2"], d["b2"], w.k,
+                            rows=rows)
     return oracle.tpmlp_swiglu(d["X"], d["Wg"], d["bg"], d["Wu"], d["bu"], d["W2"], d["b2"], w.k,
                                rows=rows)
 
@@ -178,7 +191,7 @@ def run_reference(args, w: synth.Workload):
         return 0
     import oracle
     v = args.variant
-    d = synth.workload_inputs(w) if v == "gelu" else synth.make_swiglu_inputs(w.H, w.F, w.M, w.seed)
+    d = synth.make_swiglu_inputs(w.H, w.F, w.M, w.seed) if v == "swiglu" else synth.workload_inputs(w)
     steps, warm = args.steps, args.warmup
     budget = args.reference_budget_s
     # rows per step so that the whole run stays within the budget
@@ -236,7 +249,8 @@ def run_gpu(args, w: synth.Workload):
             pg.barrier()
 
     variant = args.variant
-    d = synth.workload_inputs(w) if variant == "gelu" else synth.make_swiglu_inputs(w.H, w.F, w.M, w.seed)
+    d = (synth.make_swiglu_inputs(w.H, w.F, w.M, w.seed) if variant == "swiglu"
+         else synth.workload_inputs(w))
 
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -248,21 +262,35 @@ def run_gpu(args, w: synth.Workload):
     stream = torch.cuda.current_stream(dev)
 
     mlp = tp.TPMLP(w.H, w.F, w.k, swiglu=(variant == "swiglu"))
-    if variant == "gelu":
-        mlp.pack(*(to_dev(d[n]) for n in ("W1", "b1", "W2", "b2")))
-    else:
+    if variant == "swiglu":
         mlp.pack_swiglu(*(to_dev(d[n]) for n in ("Wg", "bg", "Wu", "bu", "W2", "b2")))
+    else:
+        mlp.pack(*(to_dev(d[n]) for n in ("W1", "b1", "W2", "b2")))
+    if variant == "block":
+        g, b = ln_params(w.H)
+        mlp.set_layernorm(to_dev(g), to_dev(b), 1e-5)
+        Xn = torch.empty((w.M, w.H), dtype=torch.bfloat16, device=dev)
     mlp.reserve(w.M)
     torch.cuda.synchronize(dev)  # the raw weights are released: only the packed copies stay
 
     def step(ev=None):
-        # one pass of the whole block: GEMM1 (+b1, GeLU) then GEMM2 (sum over shards, +b2)
+        # one pass of the whole block: GEMM1 (+b1, GeLU) then GEMM2 (sum over shards, +b2);
+        # the "block" variant is tpmlp_block_forward's three launches with events between them
         if ev is not None:
             ev[0].record(stream)
-        tp.tpmlp_gemm1(mlp.ctx, X, w.M, Y, stream)
+        if variant == "block":
+            tp.tpmlp_layernorm(mlp.ctx, X, w.M, Xn, stream)
+            if ev is not None:
+                ev[3].record(stream)
+            tp.tpmlp_gemm1(mlp.ctx, Xn, w.M, Y, stream)
+        else:
+            tp.tpmlp_gemm1(mlp.ctx, X, w.M, Y, stream)
         if ev is not None:
             ev[1].record(stream)
-        tp.tpmlp_gemm2(mlp.ctx, Y, w.M, Z, stream)
+        if variant == "block":
+            tp.tpmlp_gemm2_residual(mlp.ctx, Y, w.M, Z, X, stream)
+        else:
+            tp.tpmlp_gemm2(mlp.ctx, Y, w.M, Z, stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -274,7 +302,7 @@ def run_gpu(args, w: synth.Workload):
     if rc != tp.TPMLP_OK:
         raise RuntimeError(f"device status after warm-up: {detail:#x}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
@@ -294,9 +322,14 @@ def run_gpu(args, w: synth.Workload):
     if rc != tp.TPMLP_OK:
         raise RuntimeError(f"device status after timed steps: {detail:#x}")
 
-    g1 = [e[0].elapsed_time(e[1]) for e in evs]
+    if variant == "block":
+        ln = [e[0].elapsed_time(e[3]) for e in evs]
+        g1 = [e[3].elapsed_time(e[1]) for e in evs]
+    else:
+        ln = []
+        g1 = [e[0].elapsed_time(e[1]) for e in evs]
     g2 = [e[1].elapsed_time(e[2]) for e in evs]
-    st = [a + b for a, b in zip(g1, g2)]
+    st = [e[0].elapsed_time(e[2]) for e in evs]
     ms_step = statistics.mean(st)
     if pg is not None:
         t = torch.tensor([ms_step, t_wall], dtype=torch.float64, device=dev)
@@ -306,13 +339,25 @@ def run_gpu(args, w: synth.Workload):
     # ---- end to end through the host-buffer entry point (pinned host memory)
     Xh = torch.from_numpy(np.ascontiguousarray(d["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
     Zh = torch.empty((w.M, w.H), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        if variant == "block":
+            # host X -> device, the layer, device Z -> host (pinned buffers, one stream)
+            Xd = X.view(w.M, w.H)
+            Xd.copy_(Xh, non_blocking=True)
+            tp.tpmlp_block_forward(mlp.ctx, Xd, w.B, w.S, Z, stream)
+            Zh.copy_(Z.view(w.M, w.H), non_blocking=True)
+            stream.synchronize()
+        else:
+            tp.tpmlp_forward_host(mlp.ctx, Xh, w.B, w.S, Zh, stream)
+
     for _ in range(max(1, args.warmup)):
-        tp.tpmlp_forward_host(mlp.ctx, Xh, w.B, w.S, Zh, stream)
+        e2e_step()
     e2e_steps = max(3, min(args.steps, 20))
     barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        tp.tpmlp_forward_host(mlp.ctx, Xh, w.B, w.S, Zh, stream)
+        e2e_step()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     if pg is not None:
         t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
@@ -329,6 +374,7 @@ def run_gpu(args, w: synth.Workload):
     peak_burst = peaks["bf16_tflops"]
     peak_sust = peaks.get("bf16_tflops_sustained", peak_burst)
     kern = {"gemm1": statistics.mean(g1), "gemm2": statistics.mean(g2)}
+    ln_ms = statistics.mean(ln) if ln else None
     kflops = {kk: kernel_flops(w, variant, kk) for kk in kern}
     dom = max(kern, key=lambda kk: kern[kk])
     achieved = kflops[dom] / (kern[dom] * 1e-3) / 1e12
@@ -345,10 +391,11 @@ def run_gpu(args, w: synth.Workload):
         "pct_of_dense_bf16_peak": 100.0 * (value / world) / peak,
         "pct_of_dense_bf16_peak_burst": 100.0 * (value / world) / peak_burst,
         "wall_ms_per_step_incl_l2_flush": t_wall * 1e3 / args.steps,
-        "kernel_ms": kern,
+        "kernel_ms": dict(kern, **({"layernorm": ln_ms} if ln_ms else {})),
         "hbm_gbs_algorithmic": {  # algorithmic bytes of each launch / its mean event time
             "gemm1": alg_bytes(w, "gemm1", variant) / (kern["gemm1"] * 1e-3) / 1e9,
             "gemm2": alg_bytes(w, "gemm2", variant) / (kern["gemm2"] * 1e-3) / 1e9,
+            **({"layernorm": (4 * w.M * w.H + 8 * w.H) / (ln_ms * 1e-3) / 1e9} if ln_ms else {}),
             "peak_hbm_gbs": peaks["hbm_gbs"]},
         "config": workload_config(w, {"parallelism": "replicas" if world > 1 else "single GPU",
                                       "output": "bf16"}, variant=variant),
@@ -358,7 +405,9 @@ def run_gpu(args, w: synth.Workload):
                                     f"the power cap)", "traffic": traffic},
         "e2e": {"value": world * flops_step / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": w.M * w.H * 2, "d2h_bytes_per_step": w.M * w.H * 2,
-                "ms_per_step": e2e_s * 1e3, "api": "tpmlp_forward_host (pinned host X, Z)"},
+                "ms_per_step": e2e_s * 1e3,
+                "api": ("pinned host X -> tpmlp_block_forward -> pinned host Z" if variant == "block"
+                        else "tpmlp_forward_host (pinned host X, Z)")},
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -386,7 +435,8 @@ def alg_bytes(w: synth.Workload, kernel: str, variant: str = "gelu") -> int:
     if kernel == "gemm1":
         parts = 2 if variant == "swiglu" else 1
         return 2 * w.M * w.H + parts * (2 * w.H * w.F + 4 * w.F) + 2 * w.M * w.F
-    return 2 * w.M * w.F + 2 * w.F * w.H + 4 * w.H + 2 * w.M * w.H
+    residual = 2 * w.M * w.H if variant == "block" else 0
+    return 2 * w.M * w.F + 2 * w.F * w.H + 4 * w.H + 2 * w.M * w.H + residual
 
 
 def measured_traffic(workload: str, kernel: str):
@@ -418,8 +468,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--k", type=int, default=None, help="override the shard count")
-    ap.add_argument("--variant", default="gelu", choices=["gelu", "swiglu"],
-                    help="gelu: the block of the pages' Megatron figure; swiglu: the gated block")
+    ap.add_argument("--variant", default="gelu", choices=["gelu", "swiglu", "block"],
+                    help="gelu: the block of the pages' Megatron figure; swiglu: the gated block; "
+                         "block: Z = X + MLP(LayerNorm(X)) (LayerNorm kernel + the GeLU block "
+                         "with the residual add in the second GEMM's epilogue)")
     ap.add_argument("--impl", default="tpmlp", choices=["tpmlp", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--cpu-max-rows", type=int, default=4096)

@@ -162,6 +162,53 @@ TPMLP_API int tpmlp_gemm1(tpmlp_ctx *ctx, const void *X, int64_t M, void *Y, voi
 TPMLP_API int tpmlp_gemm2(tpmlp_ctx *ctx, const void *Y, int64_t M, void *Z, void *stream);
 
 /*
+ * LayerNorm parameters for the layer around the block (see tpmlp_block_forward).
+ *   gamma, beta  device bf16 [H] (copied; may be freed once the stream has passed this call)
+ *   eps          0 <= eps <= 1, added to the variance inside the square root
+ * H must be at most 16384 for the LayerNorm kernel.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, OOM, CUDA.
+ */
+TPMLP_API int tpmlp_set_layernorm(tpmlp_ctx *ctx, const void *gamma, const void *beta, float eps,
+                                  void *stream);
+
+/*
+ * LayerNorm of each token's full hidden vector (the step in front of the block:
+ * 大模型分布式并行策略详解 §4.2 -- LayerNorm needs the whole hidden state; sequence parallelism
+ * splits it along the independent tokens, AI大模型分布式训练 §4.2):
+ *   Xn[m, h] = (X[m, h] - mu_m) / sqrt(var_m + eps) * gamma[h] + beta[h]
+ *   mu_m = mean_h X[m, h], var_m = mean_h (X[m, h] - mu_m)^2 (biased); fp32 statistics.
+ *   X, Xn device bf16 [M, H]; M == 0 is a no-op.
+ * Errors: INVALID_ARG, NOT_PACKED (parameters not set), MISALIGNED, CUDA.
+ */
+TPMLP_API int tpmlp_layernorm(tpmlp_ctx *ctx, const void *X, int64_t M, void *Xn, void *stream);
+
+/*
+ * The block inside its Transformer layer: Z = X + MLP(LayerNorm(X)) -- the residual add of the
+ * pages' TransformerBlock (x = x + mlp(x), AI大模型分布式训练 §3.4) with LayerNorm in front.
+ * MLP is the context's block (GeLU, or gated with TPMLP_FLAG_SWIGLU). Three launches: the
+ * LayerNorm kernel, the first GEMM on the normalised input, and the second GEMM whose
+ * epilogue adds X (Z = X + (sum_i Y_i W2_i + b2), in fp32, rounded once).
+ *   X device bf16 [B, S, H]; Z device [B, S, H] (bf16, or fp32 with TPMLP_FLAG_Z_FP32).
+ *   Z may be X itself (in-place update of the residual stream, bf16 output); no other
+ *   overlap is allowed. The normalised input lives in a context buffer (grows on demand,
+ *   synchronising the device when it does).
+ * Errors: INVALID_ARG, NOT_PACKED (weights or LayerNorm parameters not set), MISALIGNED,
+ * UNSUPPORTED_SHAPE, OOM, CUDA.
+ */
+TPMLP_API int tpmlp_block_forward(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z,
+                                  void *stream);
+
+/*
+ * The second step with the residual add (the last launch of tpmlp_block_forward):
+ *   Z[m, n] = R[m, n] + (b2[n] + sum_i sum_{j<f} Y[m, i f + j] W2[i f + j, n])
+ *   Y device bf16 [M, F]; R device bf16 [M, H]; Z device [M, H] (bf16, or fp32 with
+ *   TPMLP_FLAG_Z_FP32). Z may be R itself. M == 0 is a no-op.
+ * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, CUDA.
+ */
+TPMLP_API int tpmlp_gemm2_residual(tpmlp_ctx *ctx, const void *Y, int64_t M, void *Z,
+                                   const void *R, void *stream);
+
+/*
  * Read and clear the device status word that the kernels set when a bounded wait gives up
  * (synchronises `stream`). Returns TPMLP_OK, TPMLP_ERR_DEVICE_TIMEOUT or TPMLP_ERR_CUDA.
  * *detail (optional) receives the raw word: which barrier wait gave up.

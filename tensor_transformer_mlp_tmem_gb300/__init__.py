@@ -23,6 +23,7 @@ __all__ = [
     "TPMLP_OK", "TPMLP_ERR_INVALID_ARG", "TPMLP_ERR_UNSUPPORTED_SHAPE", "TPMLP_ERR_NOT_PACKED",
     "TPMLP_ERR_CUDA", "TPMLP_ERR_OOM", "TPMLP_ERR_DEVICE_TIMEOUT", "TPMLP_ERR_ARCH",
     "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM", "TPMLP_FLAG_SWIGLU", "tpmlp_pack_shards_swiglu",
+    "tpmlp_set_layernorm", "tpmlp_layernorm", "tpmlp_block_forward", "tpmlp_gemm2_residual",
 ]
 
 TPMLP_OK = 0
@@ -77,8 +78,12 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_forward": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_forward_host": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_forward_noalloc": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_set_layernorm": ([vp, vp, vp, ctypes.c_float, vp], ctypes.c_int),
+        "tpmlp_layernorm": ([vp, vp, i64, vp, vp], ctypes.c_int),
+        "tpmlp_block_forward": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_gemm1": ([vp, vp, i64, vp, vp], ctypes.c_int),
         "tpmlp_gemm2": ([vp, vp, i64, vp, vp], ctypes.c_int),
+        "tpmlp_gemm2_residual": ([vp, vp, i64, vp, vp, vp], ctypes.c_int),
         "tpmlp_get_status": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
         "tpmlp_packed_buffer": ([vp, i32, ctypes.POINTER(vp), ctypes.POINTER(i64)], ctypes.c_int),
         "tpmlp_destroy": ([vp], None),
@@ -172,6 +177,21 @@ def tpmlp_forward_noalloc(ctx: int, X, B: int, S: int, Z, stream=None) -> None:
            "tpmlp_forward_noalloc", ctx)
 
 
+def tpmlp_set_layernorm(ctx: int, gamma, beta, eps: float, stream=None) -> None:
+    _check(load_library().tpmlp_set_layernorm(ctx, _ptr(gamma), _ptr(beta), eps, _stream(stream)),
+           "tpmlp_set_layernorm", ctx)
+
+
+def tpmlp_layernorm(ctx: int, X, M: int, Xn, stream=None) -> None:
+    _check(load_library().tpmlp_layernorm(ctx, _ptr(X), M, _ptr(Xn), _stream(stream)),
+           "tpmlp_layernorm", ctx)
+
+
+def tpmlp_block_forward(ctx: int, X, B: int, S: int, Z, stream=None) -> None:
+    _check(load_library().tpmlp_block_forward(ctx, _ptr(X), B, S, _ptr(Z), _stream(stream)),
+           "tpmlp_block_forward", ctx)
+
+
 def tpmlp_gemm1(ctx: int, X, M: int, Y, stream=None) -> None:
     _check(load_library().tpmlp_gemm1(ctx, _ptr(X), M, _ptr(Y), _stream(stream)), "tpmlp_gemm1",
            ctx)
@@ -180,6 +200,11 @@ def tpmlp_gemm1(ctx: int, X, M: int, Y, stream=None) -> None:
 def tpmlp_gemm2(ctx: int, Y, M: int, Z, stream=None) -> None:
     _check(load_library().tpmlp_gemm2(ctx, _ptr(Y), M, _ptr(Z), _stream(stream)), "tpmlp_gemm2",
            ctx)
+
+
+def tpmlp_gemm2_residual(ctx: int, Y, M: int, Z, R, stream=None) -> None:
+    _check(load_library().tpmlp_gemm2_residual(ctx, _ptr(Y), M, _ptr(Z), _ptr(R), _stream(stream)),
+           "tpmlp_gemm2_residual", ctx)
 
 
 def tpmlp_get_status(ctx: int, stream=None):
@@ -278,6 +303,31 @@ class TPMLP:
                                (W2, (self.F, self.H), "W2"), (b2, (self.H,), "b2")):
             self._require(t, bf, shape, name)
         tpmlp_pack_shards_swiglu(self.ctx, Wg, bg, Wu, bu, W2, b2, stream)
+
+    def set_layernorm(self, gamma, beta, eps: float = 1e-5, stream=None):
+        import torch
+        self._require(gamma, torch.bfloat16, (self.H,), "gamma")
+        self._require(beta, torch.bfloat16, (self.H,), "beta")
+        tpmlp_set_layernorm(self.ctx, gamma, beta, eps, stream)
+
+    def layernorm(self, X2d, Xn=None, stream=None):
+        import torch
+        M = X2d.shape[0]
+        self._require(X2d, torch.bfloat16, (M, self.H), "X")
+        if Xn is None:
+            Xn = torch.empty_like(X2d)
+        tpmlp_layernorm(self.ctx, X2d, M, Xn, stream)
+        return Xn
+
+    def block(self, X, Z=None, stream=None):
+        """Z = X + MLP(LayerNorm(X)); pass Z=X to update the residual stream in place."""
+        import torch
+        B, S, H = X.shape
+        self._require(X, torch.bfloat16, (B, S, self.H), "X")
+        if Z is None:
+            Z = torch.empty((B, S, self.H), dtype=self.out_dtype(), device=X.device)
+        tpmlp_block_forward(self.ctx, X, B, S, Z, stream)
+        return Z
 
     def reserve(self, max_tokens: int):
         tpmlp_reserve(self.ctx, max_tokens)

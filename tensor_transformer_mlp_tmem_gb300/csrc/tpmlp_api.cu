@@ -16,6 +16,7 @@
 #include "tpmlp.h"
 #include "tpmlp_gemm.cuh"
 #include "tpmlp_gemm_2sm.cuh"
+#include "tpmlp_norm.cuh"
 #include "tpmlp_pack.cuh"
 
 struct tpmlp_ctx {
@@ -50,6 +51,14 @@ struct tpmlp_ctx {
     const void* y_map_ptr = nullptr;
     int64_t y_map_rows = -1;
     CUtensorMap tmY{};
+
+    // LayerNorm in front of the block (tpmlp_set_layernorm / tpmlp_block_forward)
+    float* ln_gamma = nullptr;  // [H] fp32
+    float* ln_beta = nullptr;   // [H] fp32
+    float ln_eps = 0.0f;
+    bool ln_set = false;
+    uint16_t* Xn = nullptr;  // [xn_rows][H] normalised block input
+    int64_t xn_rows = 0;
 
     int* status = nullptr;  // device status word
     int64_t launches = 0;
@@ -276,7 +285,8 @@ int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
     return dispatch_gemm<Mode::kGemm1, false>(c, c->bn1, tmX, c->tmW1, a, s);
 }
 
-int run_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, cudaStream_t s) {
+int run_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, cudaStream_t s,
+              const void* residual = nullptr) {
     int rc = activation_map(c, Y, M, c->F, c->y_map_ptr, c->y_map_rows, c->tmY);
     if (rc) return rc;
     const CUtensorMap& tmY = c->tmY;
@@ -287,6 +297,19 @@ int run_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, cudaStream_t s) {
     a.kb_tile = a.kb_shard * c->k;
     a.bias = c->b2;
     a.out = Z;
+    a.residual = residual;
+    if (residual) {
+        if (pair) {
+            if (c->flags & TPMLP_FLAG_Z_FP32)
+                return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2Residual, true>(
+                    c, tmY, c->tmW2_pair, a, s);
+            return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2Residual, false>(
+                c, tmY, c->tmW2_pair, a, s);
+        }
+        if (c->flags & TPMLP_FLAG_Z_FP32)
+            return dispatch_gemm<Mode::kGemm2Residual, true>(c, c->bn2, tmY, c->tmW2, a, s);
+        return dispatch_gemm<Mode::kGemm2Residual, false>(c, c->bn2, tmY, c->tmW2, a, s);
+    }
     if (pair) {
         if (c->flags & TPMLP_FLAG_Z_FP32)
             return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, true>(
@@ -363,6 +386,44 @@ int encode_weight_maps(tpmlp_ctx* c) {
         rc = encode_map(c, &c->tmW2_pair, c->W2p, 3, dims, strides, box_pair);
         if (rc) return rc;
     }
+    return TPMLP_OK;
+}
+
+int ensure_xn(tpmlp_ctx* c, int64_t rows) {
+    if (rows <= c->xn_rows) return TPMLP_OK;
+    const int64_t want = ((rows + tpmlp::kBM - 1) / tpmlp::kBM) * tpmlp::kBM;
+    TPMLP_CUDA(c, cudaDeviceSynchronize());  // the old buffer may still be in use
+    if (c->Xn) cudaFree(c->Xn);
+    c->Xn = nullptr;
+    c->xn_rows = 0;
+    TPMLP_CUDA(c, cudaMalloc(&c->Xn, static_cast<size_t>(want) * c->H * 2));
+    c->xn_rows = want;
+    return TPMLP_OK;
+}
+
+template <int NC>
+void launch_layernorm_nc(const tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t s) {
+    tpmlp::layernorm_kernel<NC><<<static_cast<unsigned>(M), tpmlp::kNormThreads, 0, s>>>(
+        static_cast<const uint16_t*>(X), c->ln_gamma, c->ln_beta, c->ln_eps,
+        static_cast<uint16_t*>(Xn), static_cast<int>(c->H));
+}
+
+int run_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t s) {
+    const int chunks_per_thread =
+        static_cast<int>((c->H / 8 + tpmlp::kNormThreads - 1) / tpmlp::kNormThreads);
+    switch (chunks_per_thread) {
+        case 1: launch_layernorm_nc<1>(c, X, M, Xn, s); break;
+        case 2: launch_layernorm_nc<2>(c, X, M, Xn, s); break;
+        case 3: launch_layernorm_nc<3>(c, X, M, Xn, s); break;
+        case 4: launch_layernorm_nc<4>(c, X, M, Xn, s); break;
+        case 5: launch_layernorm_nc<5>(c, X, M, Xn, s); break;
+        case 6: launch_layernorm_nc<6>(c, X, M, Xn, s); break;
+        case 7: launch_layernorm_nc<7>(c, X, M, Xn, s); break;
+        case 8: launch_layernorm_nc<8>(c, X, M, Xn, s); break;
+        default: return TPMLP_ERR_UNSUPPORTED_SHAPE;  // H > 16384
+    }
+    TPMLP_CUDA(c, cudaGetLastError());
+    ++c->launches;
     return TPMLP_OK;
 }
 
@@ -550,6 +611,78 @@ int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, v
     return TPMLP_OK;
 }
 
+int tpmlp_set_layernorm(tpmlp_ctx* c, const void* gamma, const void* beta, float eps,
+                        void* stream) {
+    if (!c || !gamma || !beta) return TPMLP_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps > 1.0f) return TPMLP_ERR_INVALID_ARG;  // also rejects NaN
+    if (c->H > static_cast<int64_t>(tpmlp::kNormThreads) * 8 * tpmlp::kNormMaxChunks)
+        return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(gamma) | reinterpret_cast<uintptr_t>(beta)) & 1)
+        return TPMLP_ERR_MISALIGNED;
+    if (!c->ln_gamma) {
+        TPMLP_CUDA(c, cudaMalloc(&c->ln_gamma, static_cast<size_t>(c->H) * 4));
+        TPMLP_CUDA(c, cudaMalloc(&c->ln_beta, static_cast<size_t>(c->H) * 4));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const unsigned blocks = static_cast<unsigned>((c->H + 255) / 256);
+    tpmlp::bf16_to_f32_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(gamma),
+                                                     c->ln_gamma, c->H);
+    TPMLP_CUDA(c, cudaGetLastError());
+    tpmlp::bf16_to_f32_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(beta),
+                                                     c->ln_beta, c->H);
+    TPMLP_CUDA(c, cudaGetLastError());
+    c->launches += 2;
+    c->ln_eps = eps;
+    c->ln_set = true;
+    return TPMLP_OK;
+}
+
+int tpmlp_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, void* stream) {
+    if (!c || M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (!c->ln_set) {
+        c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
+        return TPMLP_ERR_NOT_PACKED;
+    }
+    if (M == 0) return TPMLP_OK;
+    if (!X || !Xn) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(X) || !aligned16(Xn)) return TPMLP_ERR_MISALIGNED;
+    return run_layernorm(c, X, M, Xn, static_cast<cudaStream_t>(stream));
+}
+
+int tpmlp_block_forward(tpmlp_ctx* c, const void* X, int64_t B, int64_t S, void* Z,
+                        void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (!c->ln_set) {
+        c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
+        return TPMLP_ERR_NOT_PACKED;
+    }
+    if ((rc = check_tokens(B, S))) return rc;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if (!X || !Z) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(X) || !aligned16(Z)) return TPMLP_ERR_MISALIGNED;
+    if ((rc = ensure_xn(c, M)) || (rc = ensure_y(c, M))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = run_layernorm(c, X, M, c->Xn, s))) return rc;
+    if ((rc = run_gemm1(c, c->Xn, M, c->Y, s))) return rc;
+    return run_gemm2(c, c->Y, M, Z, s, X);  // epilogue: Z = X + (Y W2 + b2)
+}
+
+int tpmlp_gemm2_residual(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, const void* R,
+                         void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (M == 0) return TPMLP_OK;
+    if (!Y || !Z || !R) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(Y) || !aligned16(Z) || !aligned16(R)) return TPMLP_ERR_MISALIGNED;
+    return run_gemm2(c, Y, M, Z, static_cast<cudaStream_t>(stream), R);
+}
+
 int tpmlp_get_status(tpmlp_ctx* c, void* stream, int32_t* detail) {
     if (!c) return TPMLP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -586,6 +719,9 @@ void tpmlp_destroy(tpmlp_ctx* c) {
     cudaFree(c->Y);
     cudaFree(c->Xs);
     cudaFree(c->Zs);
+    cudaFree(c->Xn);
+    cudaFree(c->ln_gamma);
+    cudaFree(c->ln_beta);
     cudaFree(c->status);
     if (cur >= 0 && cur != c->device) cudaSetDevice(cur);
     delete c;

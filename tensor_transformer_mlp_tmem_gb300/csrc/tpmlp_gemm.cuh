@@ -48,9 +48,12 @@ static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
 
 // kGemm1: Y = GeLU(acc + b1).  kGemm1Gated: the accumulator's column halves hold the gate and
 // the up projection of the same outputs, Y = SiLU(gate + bg) * (up + bu).  kGemm2: Z = acc + b2.
-enum class Mode : int { kGemm1 = 1, kGemm2 = 2, kGemm1Gated = 3 };
+// kGemm2Residual: Z = R + (acc + b2), R the layer's input (the residual add after the block).
+enum class Mode : int { kGemm1 = 1, kGemm2 = 2, kGemm1Gated = 3, kGemm2Residual = 4 };
 
-__host__ __device__ constexpr bool is_gemm1(Mode m) { return m != Mode::kGemm2; }
+__host__ __device__ constexpr bool is_gemm1(Mode m) {
+    return m == Mode::kGemm1 || m == Mode::kGemm1Gated;
+}
 
 // Wait sites recorded in the status word when a bounded wait gives up: (mode << 8) | site.
 enum : int { kSiteProducer = 1, kSiteMmaAccum = 2, kSiteMmaFull = 3, kSiteEpilogue = 4 };
@@ -68,6 +71,7 @@ struct GemmArgs {
     int group_m;    // tile rasterisation: this many row blocks share a column sweep
     const float* bias;  // [ldo] fp32
     void* out;          // [M][ldo] bf16 or fp32
+    const void* residual;  // kGemm2Residual: [M][ldo] bf16 added to the output (may equal out)
     int* status;        // device status word
 };
 
@@ -116,11 +120,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&p);
 }
 
-// One 32-column slice of one output row: + bias, (GeLU), convert, store.
+// One 32-column slice of one output row: + bias, (GeLU), (+ residual), convert, store.
 template <Mode MODE, bool OUT_F32>
 __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const float* __restrict__ bias,
-                                               void* __restrict__ out, int row, int M, int ldo,
-                                               int col) {
+                                               void* out, int row, int M, int ldo, int col,
+                                               const void* residual = nullptr) {
     float x[32];
     const float4* b4 = reinterpret_cast<const float4*>(bias + col);
 #pragma unroll
@@ -136,6 +140,21 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const fl
         for (int j = 0; j < 32; ++j) x[j] = gelu_erf(x[j]);
     }
     if (row >= M) return;
+    if constexpr (MODE == Mode::kGemm2Residual) {
+        // read before the store below: the output may be the residual buffer itself
+        const uint4* r4 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(residual) +
+                                                         static_cast<size_t>(row) * ldo + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 u = r4[j];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[8 * j + 2 * i] += __uint_as_float(w[i] << 16);
+                x[8 * j + 2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        }
+    }
     if constexpr (OUT_F32) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) +
                                                 static_cast<size_t>(row) * ldo + col);
@@ -217,7 +236,8 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs
             ptx::tmem_ld_32x32b_x32(taddr + c, v);
             ptx::tmem_wait_ld(v);
             if (c + 32 == c0 + kCols) release();
-            epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo, n0 + c);
+            epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo, n0 + c,
+                                          args.residual);
         }
     }
 }
