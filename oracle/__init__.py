@@ -16,6 +16,9 @@ What it computes (the pages' definition of the Megatron MLP block):
 with GeLU(a) = a/2 (1 + erf(a/sqrt 2)) (reading: the exact form) and b2 added once.
 The layer around the block: Z = X + MLP(LayerNorm(X)) (residual of AI大模型分布式训练 §3.4,
 LayerNorm on the full hidden vector before the block, 大模型分布式并行策略详解 §4.2).
+The parallel linear layers on their own (the tensor-parallel attention's Q/K/V projection and
+output projection, AI大模型分布式训练 §2.3): column-parallel X W + b, and row-parallel
+sum_i X_i W_i + b.
 The gated variant (gate_up_proj column-parallel, down_proj row-parallel: 大模型分布式优化技术（一）
 §5.1, AI大模型分布式训练 §6.1) replaces GeLU(X W1 + b1) by SiLU(X Wg + bg) * (X Wu + bu).
 
@@ -69,6 +72,8 @@ class Oracle:
         lib.oracle_block_f64.argtypes = [vp, i64, vp, i64, vp, vp, ctypes.c_double, vp, vp, vp, vp,
                                          i64, i64, i32, vp, vp]
         lib.oracle_block_f64.restype = ctypes.c_int
+        lib.oracle_linear_f64.argtypes = [i32, vp, i64, vp, i64, vp, vp, i64, i64, i32, vp]
+        lib.oracle_linear_f64.restype = ctypes.c_int
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ctypes.c_int
         self.lib = lib
@@ -172,6 +177,25 @@ class Oracle:
         return out
 
 
+    def linear(self, kind: str, X, W, b, k: int, rows=None):
+        """Parallel linear layer in fp64: kind "column" (W split by columns, outputs
+        concatenated) or "row" (W split by rows, partials summed). X [x_rows, K], W [K, N]."""
+        X, W, b = (_u16(a) for a in (X, W, b))
+        x_rows, K = X.shape
+        if W.shape[0] != K or b.shape != (W.shape[1],):
+            raise ValueError("shape mismatch")
+        N = W.shape[1]
+        rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        R = x_rows if rows_arr is None else len(rows_arr)
+        out = np.empty((R, N), dtype=np.float64)
+        rc = self.lib.oracle_linear_f64({"column": 0, "row": 1}[kind], X.ctypes.data, x_rows,
+                                        None if rows_arr is None else rows_arr.ctypes.data, R,
+                                        W.ctypes.data, b.ctypes.data, K, N, k, out.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return out
+
+
 def _u16(a) -> np.ndarray:
     a = np.ascontiguousarray(a)
     if a.dtype != np.uint16:
@@ -229,3 +253,7 @@ def tpmlp_swiglu(X, Wg, bg, Wu, bu, W2, b2, k: int, rows=None, want_y: bool = Fa
 
 def block(X, gamma, beta, eps, W1, b1, W2, b2, k: int, rows=None, want_xn: bool = False):
     return default().block(X, gamma, beta, eps, W1, b1, W2, b2, k, rows=rows, want_xn=want_xn)
+
+
+def linear(kind: str, X, W, b, k: int, rows=None):
+    return default().linear(kind, X, W, b, k, rows=rows)

@@ -313,6 +313,78 @@ int oracle_block_f64(const uint16_t *X, int64_t x_rows, const int64_t *rows, int
     return failed ? -1 : 0;
 }
 
+/*
+ * The two parallel linear layers on their own, as the pages' tensor-parallel attention uses
+ * them (AI大模型分布式训练 §2.3: the Q/K/V projection is a ColumnParallelLinear, the output
+ * projection a RowParallelLinear followed by the All-Reduce; the heads are split into k
+ * groups, one per shard). W is [K][N] (Y = X W), b is [N].
+ *   kind 0, column-parallel: shard i owns columns [i f, (i+1) f), f = N / k;
+ *           out[m, i f + j] = b[i f + j] + sum_h X[m, h] W[h, i f + j]
+ *   kind 1, row-parallel:    shard i owns rows [i f, (i+1) f), f = K / k, and the input
+ *           columns with them; out[m, n] = b[n] + sum_i ( sum_{j<f} X[m, i f + j] W[i f + j, n] )
+ *           (each shard's partial first, then the sum over shards in shard order, then b once)
+ */
+int oracle_linear_f64(int32_t kind, const uint16_t *X, int64_t x_rows, const int64_t *rows,
+                      int64_t R, const uint16_t *W, const uint16_t *b, int64_t K, int64_t N,
+                      int32_t k, double *out) {
+    if (!X || !W || !b || !out || K <= 0 || N <= 0 || k <= 0 || R < 0) return -1;
+    if (kind != 0 && kind != 1) return -1;
+    if ((kind == 0 && N % k != 0) || (kind == 1 && K % k != 0)) return -1;
+    int failed = 0;
+
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc(sizeof(double) * (size_t)N);
+        double *part = (double *)malloc(sizeof(double) * (size_t)N);
+        if (!acc || !part) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < R; ++r) {
+                const int64_t m = rows ? rows[r] : r;
+                if (m < 0 || m >= x_rows) {
+#pragma omp atomic write
+                    failed = 1;
+                    continue;
+                }
+                const uint16_t *x = X + m * K;
+                if (kind == 0) {
+                    const int64_t f = N / k;
+                    for (int32_t i = 0; i < k; ++i) {
+                        const int64_t j0 = (int64_t)i * f;
+                        for (int64_t jj = 0; jj < f; ++jj) acc[jj] = 0.0;
+                        for (int64_t h = 0; h < K; ++h) {
+                            const double xh = widen_bf16(x[h]);
+                            const uint16_t *w = W + h * N + j0;
+                            for (int64_t jj = 0; jj < f; ++jj) acc[jj] += xh * widen_bf16(w[jj]);
+                        }
+                        for (int64_t jj = 0; jj < f; ++jj)
+                            out[r * N + j0 + jj] = acc[jj] + widen_bf16(b[j0 + jj]);
+                    }
+                } else {
+                    const int64_t f = K / k;
+                    for (int64_t n = 0; n < N; ++n) acc[n] = 0.0;
+                    for (int32_t i = 0; i < k; ++i) {
+                        const int64_t j0 = (int64_t)i * f;
+                        for (int64_t n = 0; n < N; ++n) part[n] = 0.0;
+                        for (int64_t jj = 0; jj < f; ++jj) {
+                            const double xj = widen_bf16(x[j0 + jj]);
+                            const uint16_t *w = W + (j0 + jj) * N;
+                            for (int64_t n = 0; n < N; ++n) part[n] += xj * widen_bf16(w[n]);
+                        }
+                        for (int64_t n = 0; n < N; ++n) acc[n] += part[n];
+                    }
+                    for (int64_t n = 0; n < N; ++n) out[r * N + n] = acc[n] + widen_bf16(b[n]);
+                }
+            }
+        }
+        free(acc);
+        free(part);
+    }
+    return failed ? -1 : 0;
+}
+
 int oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

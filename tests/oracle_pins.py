@@ -336,6 +336,39 @@ def pin_block_zero_mlp_is_identity(orc):
 BLOCK_PINS = [pin_layernorm_golden, pin_layernorm_matches_torch, pin_layernorm_scale_invariance,
               pin_block_is_residual_plus_mlp, pin_block_zero_mlp_is_identity]
 
+# ---------------------------------------------------------------------------------
+# the parallel linear layers on their own
+def _linear_inputs(K=192, N=256, M=23, seed=61):
+    X = synth.normal_bf16(seed, 50, (M, K), 1.0)
+    W = synth.normal_bf16(seed, 51, (K, N), 1.0 / np.sqrt(K))
+    b = synth.normal_bf16(seed, 52, (N,), 0.02)
+    return X, W, b
+
+
+def pin_linear_matches_numpy(orc):
+    """Both parallel linear layers equal X W + b (numpy float64 matmul) for every k."""
+    X, W, b = _linear_inputs()
+    ref = synth.bf16_to_f64(X) @ synth.bf16_to_f64(W) + synth.bf16_to_f64(b)
+    for kind, ks in (("column", (1, 2, 4, 8)), ("row", (1, 2, 3, 4, 6))):
+        for k in ks:
+            got = orc.linear(kind, X, W, b, k)
+            assert _rel_fro(got, ref) <= 1e-12, (kind, k, _rel_fro(got, ref))
+
+
+def pin_linear_row_parallel_is_a_sum_of_partials(orc):
+    """Row-parallel: zeroing the input columns of one shard removes exactly that shard's
+    partial, X_i W_i (numpy), from the output."""
+    X, W, b = _linear_inputs()
+    k, f = 3, 64
+    full = orc.linear("row", X, W, b, k)
+    Xz = X.copy()
+    Xz[:, f:2 * f] = 0
+    part = synth.bf16_to_f64(X[:, f:2 * f]) @ synth.bf16_to_f64(W[f:2 * f, :])
+    assert _rel_fro(full - orc.linear("row", Xz, W, b, k), part) <= 1e-12
+
+
+LINEAR_PINS = [pin_linear_matches_numpy, pin_linear_row_parallel_is_a_sum_of_partials]
+
 SWIGLU_PINS = [pin_silu_table_and_expit, pin_silu_odd_part, pin_swiglu_bruteforce_golden,
                pin_swiglu_matches_numpy, pin_swiglu_gate_only, pin_swiglu_k_invariance]
 
@@ -343,4 +376,4 @@ ALL_PINS = [
     pin_gelu_table, pin_gelu_ndtr, pin_gelu_odd_part, pin_bruteforce_golden,
     pin_identity_matches_numpy, pin_concat_identity, pin_row_split_sum, pin_k_invariance,
     pin_w2_zero, pin_w1_zero, pin_rows_independent, pin_x_linear_without_activation,
-] + SWIGLU_PINS + BLOCK_PINS
+] + SWIGLU_PINS + BLOCK_PINS + LINEAR_PINS

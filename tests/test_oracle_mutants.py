@@ -50,6 +50,12 @@ MUTANTS = {
                          "Z[r * H + n] = (zsum[n] + widen_bf16(b2[n]));"),
     "residual_of_normalised_input": ("Z[r * H + n] = widen_bf16(x[n]) + (zsum[n]",
                                      "Z[r * H + n] = xn[n] + (zsum[n]"),
+    "linear_column_without_shard_offset": ("const uint16_t *w = W + h * N + j0;",
+                                           "const uint16_t *w = W + h * N;"),
+    "linear_row_input_without_shard_offset": ("const double xj = widen_bf16(x[j0 + jj]);",
+                                              "const double xj = widen_bf16(x[jj]);"),
+    "linear_row_bias_per_shard": ("for (int64_t n = 0; n < N; ++n) acc[n] += part[n];",
+                                  "for (int64_t n = 0; n < N; ++n) acc[n] += part[n] + widen_bf16(b[n]);"),
     "activation_dropped": ("acc[jj] = (act == ORACLE_ACT_GELU) ? oracle_gelu(a) : a;",
                               "acc[jj] = a;"),
 }
