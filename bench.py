@@ -439,6 +439,94 @@ def alg_bytes(w: synth.Workload, kernel: str, variant: str = "gelu") -> int:
     return 2 * w.M * w.F + 2 * w.F * w.H + 4 * w.H + 2 * w.M * w.H + residual
 
 
+def run_gpu_linear(args, w: synth.Workload):
+    """The tensor-parallel attention projections on the workload's shape: "outproj" is the
+    row-parallel output projection (K = N = H, heads split into k groups, the sum over
+    shards in the accumulator), "qkv" the column-parallel Q/K/V projection (K = H, N = 3H)."""
+    import torch
+    import tensor_transformer_mlp_tmem_gb300 as tp
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    kind = "row" if args.variant == "outproj" else "column"
+    K, N, M = w.H, (w.H if kind == "row" else 3 * w.H), w.M
+    X = synth.normal_bf16(w.seed, 50, (M, K), 1.0)
+    W = synth.normal_bf16(w.seed, 51, (K, N), 1.0 / np.sqrt(K))
+    b = synth.normal_bf16(w.seed, 52, (N,), 0.02)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    Xd, out = to_dev(X), torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    lin = tp.Linear(kind, K, N, w.k)
+    lin.pack(to_dev(W), to_dev(b))
+    for _ in range(args.warmup):
+        flush.zero_()
+        tp.tpmlp_linear_forward(lin.ctx, Xd, M, out, stream)
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    n0 = tp.tpmlp_launch_count(lin.ctx)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        tp.tpmlp_linear_forward(lin.ctx, Xd, M, out, stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if pg is not None:
+        pg.barrier()
+    launches = tp.tpmlp_launch_count(lin.ctx) - n0
+    clk = clocks.stop()
+    rc, detail = lin.status()
+    if rc != tp.TPMLP_OK:
+        raise RuntimeError(f"device status {detail:#x}")
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    if pg is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t[0])
+    flops = 2 * M * K * N
+    peaks, peak_src = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    value = world * flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) X, N(0,1/K) W)",
+        "tokens_per_s": world * M / (ms * 1e-3),
+        "config": {"workload": f"{w.name}-shaped attention {'output' if kind == 'row' else 'Q/K/V'} "
+                               f"projection: X [{M},{K}] bf16, W [{K},{N}], {kind}-parallel, "
+                               f"k={w.k} head groups, seeded synthetic",
+                   "variant": args.variant, "M": M, "K": K, "N": N, "k": w.k,
+                   "flops_per_step": flops,
+                   "l2": "flushed between timed steps (256 MiB write, outside the timed events)"},
+        "roofline": {"bound": "tensor", "kernel": f"{kind}-parallel linear", "achieved": value / world,
+                     "peak": peak, "unit": "TFLOP/s", "frac": value / world / peak,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None},
+        "gpu_launches": launches, "clocks": clk,
+    }
+    lin.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
 def measured_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary
     (profiles/ncu_traffic.json-like lines in profiles/*.md: `traffic <workload> <kernel> <bytes>`),
@@ -468,10 +556,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--k", type=int, default=None, help="override the shard count")
-    ap.add_argument("--variant", default="gelu", choices=["gelu", "swiglu", "block"],
+    ap.add_argument("--variant", default="gelu",
+                    choices=["gelu", "swiglu", "block", "outproj", "qkv"],
                     help="gelu: the block of the pages' Megatron figure; swiglu: the gated block; "
                          "block: Z = X + MLP(LayerNorm(X)) (LayerNorm kernel + the GeLU block "
-                         "with the residual add in the second GEMM's epilogue)")
+                         "with the residual add in the second GEMM's epilogue); outproj / qkv: "
+                         "the tensor-parallel attention's output (row-parallel) and Q/K/V "
+                         "(column-parallel) projections on the workload's shape")
     ap.add_argument("--impl", default="tpmlp", choices=["tpmlp", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--cpu-max-rows", type=int, default=4096)
@@ -484,7 +575,11 @@ def main():
     if args.k is not None:
         w = synth.Workload(w.name, w.B, w.S, w.H, w.F, args.k, w.seed)
     if args.impl == "reference":
+        if args.variant in ("outproj", "qkv"):
+            ap.error("the reference arm covers the MLP variants")
         return run_reference(args, w)
+    if args.variant in ("outproj", "qkv"):
+        return run_gpu_linear(args, w)
     return run_gpu(args, w)
 
 

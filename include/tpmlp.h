@@ -162,7 +162,9 @@ TPMLP_API int tpmlp_gemm1(tpmlp_ctx *ctx, const void *X, int64_t M, void *Y, voi
 TPMLP_API int tpmlp_gemm2(tpmlp_ctx *ctx, const void *Y, int64_t M, void *Z, void *stream);
 
 /*
- * LayerNorm parameters for the layer around the block (see tpmlp_block_forward).
+ * LayerNorm parameters for the layer around the block (see tpmlp_block_forward), or for the
+ * input of a column-parallel linear layer (LayerNorm before the Q/K/V projection); the
+ * normalised width is the block's H, or the layer's K. Not for row-parallel layers.
  *   gamma, beta  device bf16 [H] (copied; may be freed once the stream has passed this call)
  *   eps          0 <= eps <= 1, added to the variance inside the square root
  * H must be at most 16384 for the LayerNorm kernel.
@@ -248,6 +250,42 @@ TPMLP_API int tpmlp_packed_buffer(const tpmlp_ctx *ctx, int32_t which, const voi
 #define TPMLP_NOALLOC_SCRATCH_BYTES (32ll << 20) /* 32 MiB */
 TPMLP_API int tpmlp_forward_noalloc(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z,
                                     void *stream);
+
+/*
+ * The two parallel linear layers on their own, all k shards on this GPU: the projections of
+ * the pages' tensor-parallel attention (AI大模型分布式训练 §2.3: Q/K/V is a ColumnParallelLinear
+ * with the heads split into k groups, the output projection a RowParallelLinear followed by
+ * the All-Reduce). W is [K, N] in math orientation (out = X W + b), b is [N].
+ *   TPMLP_LINEAR_COLUMN  W split by columns: out[:, i f:(i+1) f] = X W_i + b_i, f = N / k
+ *                        (the outputs of the shards side by side; the first GEMM's kernel
+ *                        with a bias-only epilogue)
+ *   TPMLP_LINEAR_ROW     W split by rows, X by the matching columns (f = K / k):
+ *                        out = sum_i X_i W_i + b, the sum over shards taken in the second
+ *                        GEMM's fp32 accumulator (the All-Reduce on chip), b added once
+ * Shapes: K, N multiples of 64; the sharded dimension divisible by k into multiples of 64.
+ * flags: 0, TPMLP_FLAG_Z_FP32 (fp32 output), TPMLP_FLAG_SINGLE_SM.
+ * The context is used with tpmlp_linear_pack / tpmlp_linear_forward / tpmlp_destroy (and the
+ * diagnostic calls); the MLP-block entry points reject it with TPMLP_ERR_INVALID_ARG.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ARCH, OOM, CUDA.
+ */
+#define TPMLP_LINEAR_COLUMN 0
+#define TPMLP_LINEAR_ROW 1
+TPMLP_API int tpmlp_linear_create(tpmlp_ctx **out, int32_t kind, int64_t K, int64_t N, int32_t k,
+                                  uint32_t flags);
+
+/*
+ * Pack a linear layer's weight: W device bf16 [K, N], b device bf16 [N] (may be freed once the
+ * stream has passed this call). Errors: INVALID_ARG (not a linear context), MISALIGNED, CUDA.
+ */
+TPMLP_API int tpmlp_linear_pack(tpmlp_ctx *ctx, const void *W, const void *b, void *stream);
+
+/*
+ * out = the layer applied to X: X device bf16 [M, K]; out device [M, N] (bf16, or fp32 with
+ * TPMLP_FLAG_Z_FP32). One kernel launch; M == 0 is a no-op.
+ * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, UNSUPPORTED_SHAPE, CUDA.
+ */
+TPMLP_API int tpmlp_linear_forward(tpmlp_ctx *ctx, const void *X, int64_t M, void *out,
+                                   void *stream);
 
 /* Release everything the context owns (synchronises its device first). NULL is a no-op. */
 TPMLP_API void tpmlp_destroy(tpmlp_ctx *ctx);

@@ -24,6 +24,8 @@ __all__ = [
     "TPMLP_ERR_CUDA", "TPMLP_ERR_OOM", "TPMLP_ERR_DEVICE_TIMEOUT", "TPMLP_ERR_ARCH",
     "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM", "TPMLP_FLAG_SWIGLU", "tpmlp_pack_shards_swiglu",
     "tpmlp_set_layernorm", "tpmlp_layernorm", "tpmlp_block_forward", "tpmlp_gemm2_residual",
+    "tpmlp_linear_create", "tpmlp_linear_pack", "tpmlp_linear_forward", "Linear",
+    "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW",
 ]
 
 TPMLP_OK = 0
@@ -38,6 +40,8 @@ TPMLP_ERR_MISALIGNED = -8
 TPMLP_FLAG_Z_FP32 = 0x1
 TPMLP_FLAG_SINGLE_SM = 0x2
 TPMLP_FLAG_SWIGLU = 0x4
+TPMLP_LINEAR_COLUMN = 0
+TPMLP_LINEAR_ROW = 1
 TPMLP_NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's fixed scratch for tpmlp_forward_noalloc
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -86,6 +90,9 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_gemm2_residual": ([vp, vp, i64, vp, vp, vp], ctypes.c_int),
         "tpmlp_get_status": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
         "tpmlp_packed_buffer": ([vp, i32, ctypes.POINTER(vp), ctypes.POINTER(i64)], ctypes.c_int),
+        "tpmlp_linear_create": ([ctypes.POINTER(vp), i32, i64, i64, i32, u32], ctypes.c_int),
+        "tpmlp_linear_pack": ([vp, vp, vp, vp], ctypes.c_int),
+        "tpmlp_linear_forward": ([vp, vp, i64, vp, vp], ctypes.c_int),
         "tpmlp_destroy": ([vp], None),
         "tpmlp_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "tpmlp_last_error": ([vp], ctypes.c_char_p),
@@ -223,6 +230,23 @@ def tpmlp_packed_buffer(ctx: int, which: int):
     _check(load_library().tpmlp_packed_buffer(ctx, which, ctypes.byref(p), ctypes.byref(n)),
            "tpmlp_packed_buffer", ctx)
     return p.value, n.value
+
+
+def tpmlp_linear_create(kind: int, K: int, N: int, k: int, flags: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(load_library().tpmlp_linear_create(ctypes.byref(out), kind, K, N, k, flags),
+           "tpmlp_linear_create")
+    return out.value
+
+
+def tpmlp_linear_pack(ctx: int, W, b, stream=None) -> None:
+    _check(load_library().tpmlp_linear_pack(ctx, _ptr(W), _ptr(b), _stream(stream)),
+           "tpmlp_linear_pack", ctx)
+
+
+def tpmlp_linear_forward(ctx: int, X, M: int, out, stream=None) -> None:
+    _check(load_library().tpmlp_linear_forward(ctx, _ptr(X), M, _ptr(out), _stream(stream)),
+           "tpmlp_linear_forward", ctx)
 
 
 def tpmlp_destroy(ctx) -> None:
@@ -375,3 +399,57 @@ class TPMLP:
     @property
     def launches(self) -> int:
         return tpmlp_launch_count(self.ctx)
+
+
+class Linear:
+    """A column- or row-parallel linear layer with all k shards on this GPU (the Q/K/V and
+    output projections of tensor-parallel attention): out = X W + b, W [K, N].
+
+        proj = Linear("row", K, N, k); proj.pack(W, b); out = proj(X2d)
+    """
+
+    def __init__(self, kind: str, K: int, N: int, k: int, out_fp32: bool = False,
+                 single_sm: bool = False):
+        self.kind, self.K, self.N, self.k = kind, K, N, k
+        self.out_fp32 = out_fp32
+        flags = (TPMLP_FLAG_Z_FP32 if out_fp32 else 0) | (TPMLP_FLAG_SINGLE_SM if single_sm else 0)
+        kid = {"column": TPMLP_LINEAR_COLUMN, "row": TPMLP_LINEAR_ROW}[kind]
+        self.ctx = tpmlp_linear_create(kid, K, N, k, flags)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            tpmlp_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def pack(self, W, b, stream=None):
+        import torch
+        TPMLP._require(W, torch.bfloat16, (self.K, self.N), "W")
+        TPMLP._require(b, torch.bfloat16, (self.N,), "b")
+        tpmlp_linear_pack(self.ctx, W, b, stream)
+
+    def forward(self, X, out=None, stream=None):
+        import torch
+        M = X.shape[0]
+        TPMLP._require(X, torch.bfloat16, (M, self.K), "X")
+        if out is None:
+            out = torch.empty((M, self.N), dtype=torch.float32 if self.out_fp32 else torch.bfloat16,
+                              device=X.device)
+        tpmlp_linear_forward(self.ctx, X, M, out, stream)
+        return out
+
+    __call__ = forward
+
+    def status(self, stream=None):
+        return tpmlp_get_status(self.ctx, stream)

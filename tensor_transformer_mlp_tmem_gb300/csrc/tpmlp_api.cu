@@ -35,6 +35,7 @@ struct tpmlp_ctx {
     CUtensorMap tmW1{}, tmW2{};            // B boxes for the single-SM kernel (BN rows)
     CUtensorMap tmW1_pair{}, tmW2_pair{};  // B boxes for the CTA-pair kernel (128 rows)
     bool pair1 = false, pair2 = false;     // GEMM1 / GEMM2 run on CTA pairs
+    int kind = 0;        // 0: MLP block; 1: column-parallel linear; 2: row-parallel linear
     bool gated = false;  // SwiGLU block: W1p holds gate and up rows interleaved
     int gate_block = 0;  // G: gate/up interleave block (output columns per half-tile)
 
@@ -235,8 +236,11 @@ GemmArgs base_args(const tpmlp_ctx* c, int64_t M, int ldo, int bm, int bn, int g
     return a;
 }
 
+constexpr int kKindBlock = 0, kKindColumn = 1, kKindRow = 2;
+
+// An MLP-block context whose weights are packed.
 int check_ctx(const tpmlp_ctx* c) {
-    if (!c) return TPMLP_ERR_INVALID_ARG;
+    if (!c || c->kind != kKindBlock) return TPMLP_ERR_INVALID_ARG;
     if (!c->packed) return TPMLP_ERR_NOT_PACKED;
     return TPMLP_OK;
 }
@@ -257,7 +261,8 @@ int activation_map(tpmlp_ctx* c, const void* ptr, int64_t rows, int64_t cols,
     return TPMLP_OK;
 }
 
-int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
+int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s,
+              bool linear = false) {
     int rc = activation_map(c, X, M, c->H, c->x_map_ptr, c->x_map_rows, c->tmX);
     if (rc) return rc;
     const CUtensorMap& tmX = c->tmX;
@@ -278,6 +283,19 @@ int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s) {
             return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1Gated, false>(
                 c, tmX, c->tmW1_pair, a, s);
         return dispatch_gemm<Mode::kGemm1Gated, false>(c, c->bn1, tmX, c->tmW1, a, s);
+    }
+    if (linear) {
+        // column-parallel linear layer: bias only, output bf16 or fp32
+        if (c->flags & TPMLP_FLAG_Z_FP32) {
+            if (pair)
+                return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1Linear, true>(
+                    c, tmX, c->tmW1_pair, a, s);
+            return dispatch_gemm<Mode::kGemm1Linear, true>(c, c->bn1, tmX, c->tmW1, a, s);
+        }
+        if (pair)
+            return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1Linear, false>(
+                c, tmX, c->tmW1_pair, a, s);
+        return dispatch_gemm<Mode::kGemm1Linear, false>(c, c->bn1, tmX, c->tmW1, a, s);
     }
     if (pair)
         return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1, false>(c, tmX,
@@ -361,7 +379,7 @@ int pack_second_layer(tpmlp_ctx* c, const void* W2, const void* b2, cudaStream_t
 // Tensor maps of the packed shards: box 64 (reduction) x rows x 1 shard, for the single-SM
 // kernel (rows = its tile width) and for the CTA-pair kernel (rows = 128 per CTA).
 int encode_weight_maps(tpmlp_ctx* c) {
-    {
+    if (c->W1p) {
         const int64_t rows1 = c->gated ? 2 * c->f : c->f;  // packed rows per shard
         const uint64_t dims[3] = {static_cast<uint64_t>(c->H), static_cast<uint64_t>(rows1),
                                   static_cast<uint64_t>(c->k)};
@@ -374,7 +392,7 @@ int encode_weight_maps(tpmlp_ctx* c) {
         rc = encode_map(c, &c->tmW1_pair, c->W1p, 3, dims, strides, box_pair);
         if (rc) return rc;
     }
-    {
+    if (c->W2p) {
         const uint64_t dims[3] = {static_cast<uint64_t>(c->f), static_cast<uint64_t>(c->H),
                                   static_cast<uint64_t>(c->k)};
         const uint64_t strides[2] = {static_cast<uint64_t>(c->f) * 2,
@@ -427,6 +445,8 @@ int run_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t
     return TPMLP_OK;
 }
 
+int create_context(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flags, int kind);
+
 }  // namespace
 
 extern "C" {
@@ -439,7 +459,30 @@ int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flag
         return TPMLP_ERR_INVALID_ARG;
     if (H % 64 || F % 64 || F % k || (F / k) % 64) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if (H > (int64_t(1) << 20) || F > (int64_t(1) << 22)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    return create_context(out, H, F, k, flags, kKindBlock);
+}
 
+int tpmlp_linear_create(tpmlp_ctx** out, int32_t kind, int64_t K, int64_t N, int32_t k,
+                        uint32_t flags) {
+    if (!out) return TPMLP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (K <= 0 || N <= 0 || k <= 0) return TPMLP_ERR_INVALID_ARG;
+    if (kind != TPMLP_LINEAR_COLUMN && kind != TPMLP_LINEAR_ROW) return TPMLP_ERR_INVALID_ARG;
+    if (flags & ~(TPMLP_FLAG_Z_FP32 | TPMLP_FLAG_SINGLE_SM)) return TPMLP_ERR_INVALID_ARG;
+    const int64_t split = (kind == TPMLP_LINEAR_COLUMN) ? N : K;  // the sharded dimension
+    if (K % 64 || N % 64 || split % k || (split / k) % 64) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (K > (int64_t(1) << 22) || N > (int64_t(1) << 22)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    // column: the first GEMM's roles (reduction H := K, outputs F := N);
+    // row:    the second GEMM's roles (reduction F := K, outputs H := N)
+    if (kind == TPMLP_LINEAR_COLUMN) return create_context(out, K, N, k, flags, kKindColumn);
+    return create_context(out, N, K, k, flags, kKindRow);
+}
+
+}  // extern "C"
+
+namespace {
+
+int create_context(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flags, int kind) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TPMLP_ERR_CUDA;
     cudaDeviceProp prop;
@@ -455,6 +498,7 @@ int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flag
     c->k = k;
     c->f = F / k;
     c->flags = flags;
+    c->kind = kind;
     c->gated = (flags & TPMLP_FLAG_SWIGLU) != 0;
     // gated: each first-GEMM tile holds G gate + G up columns of the same G outputs
     c->gate_block = (c->f % 128 == 0) ? 128 : 64;
@@ -466,10 +510,11 @@ int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flag
     int rc = TPMLP_OK;
     cudaError_t e;
     const size_t parts1 = c->gated ? 2 : 1;  // gate and up packed together
-    if ((e = cudaMalloc(&c->W1p, parts1 * H * F * 2)) != cudaSuccess ||
-        (e = cudaMalloc(&c->W2p, static_cast<size_t>(H) * F * 2)) != cudaSuccess ||
-        (e = cudaMalloc(&c->b1, parts1 * F * 4)) != cudaSuccess ||
-        (e = cudaMalloc(&c->b2, static_cast<size_t>(H) * 4)) != cudaSuccess ||
+    const bool first = kind != kKindRow, second = kind != kKindColumn;
+    if ((first && (e = cudaMalloc(&c->W1p, parts1 * H * F * 2)) != cudaSuccess) ||
+        (second && (e = cudaMalloc(&c->W2p, static_cast<size_t>(H) * F * 2)) != cudaSuccess) ||
+        (first && (e = cudaMalloc(&c->b1, parts1 * F * 4)) != cudaSuccess) ||
+        (second && (e = cudaMalloc(&c->b2, static_cast<size_t>(H) * 4)) != cudaSuccess) ||
         (e = cudaMalloc(&c->status, sizeof(int))) != cudaSuccess ||
         (e = cudaMemset(c->status, 0, sizeof(int))) != cudaSuccess) {
         rc = (e == cudaErrorMemoryAllocation) ? TPMLP_ERR_OOM : TPMLP_ERR_CUDA;
@@ -480,9 +525,14 @@ int tpmlp_create(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flag
     return TPMLP_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
 int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* W2, const void* b2,
                       void* stream) {
-    if (!c || !W1 || !b1 || !W2 || !b2 || c->gated) return TPMLP_ERR_INVALID_ARG;
+    if (!c || !W1 || !b1 || !W2 || !b2 || c->gated || c->kind != kKindBlock)
+        return TPMLP_ERR_INVALID_ARG;
     if (!aligned16(W1) || !aligned16(W2) || (reinterpret_cast<uintptr_t>(b1) & 1) ||
         (reinterpret_cast<uintptr_t>(b2) & 1))
         return TPMLP_ERR_MISALIGNED;
@@ -511,7 +561,8 @@ int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* 
 
 int tpmlp_pack_shards_swiglu(tpmlp_ctx* c, const void* Wg, const void* bg, const void* Wu,
                              const void* bu, const void* W2, const void* b2, void* stream) {
-    if (!c || !Wg || !bg || !Wu || !bu || !W2 || !b2 || !c->gated) return TPMLP_ERR_INVALID_ARG;
+    if (!c || !Wg || !bg || !Wu || !bu || !W2 || !b2 || !c->gated || c->kind != kKindBlock)
+        return TPMLP_ERR_INVALID_ARG;
     if (!aligned16(Wg) || !aligned16(Wu) || !aligned16(W2) ||
         ((reinterpret_cast<uintptr_t>(bg) | reinterpret_cast<uintptr_t>(bu) |
           reinterpret_cast<uintptr_t>(b2)) & 1))
@@ -542,7 +593,7 @@ int tpmlp_pack_shards_swiglu(tpmlp_ctx* c, const void* Wg, const void* bg, const
 }
 
 int tpmlp_reserve(tpmlp_ctx* c, int64_t max_tokens) {
-    if (!c || max_tokens < 0) return TPMLP_ERR_INVALID_ARG;
+    if (!c || c->kind != kKindBlock || max_tokens < 0) return TPMLP_ERR_INVALID_ARG;
     if (max_tokens > (int64_t(1) << 31)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     return ensure_y(c, max_tokens);
 }
@@ -613,7 +664,8 @@ int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, v
 
 int tpmlp_set_layernorm(tpmlp_ctx* c, const void* gamma, const void* beta, float eps,
                         void* stream) {
-    if (!c || !gamma || !beta) return TPMLP_ERR_INVALID_ARG;
+    // the block's input, or a column-parallel layer's input (LayerNorm before Q/K/V)
+    if (!c || !gamma || !beta || c->kind == kKindRow) return TPMLP_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || eps > 1.0f) return TPMLP_ERR_INVALID_ARG;  // also rejects NaN
     if (c->H > static_cast<int64_t>(tpmlp::kNormThreads) * 8 * tpmlp::kNormMaxChunks)
         return TPMLP_ERR_UNSUPPORTED_SHAPE;
@@ -683,6 +735,45 @@ int tpmlp_gemm2_residual(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, const 
     return run_gemm2(c, Y, M, Z, static_cast<cudaStream_t>(stream), R);
 }
 
+int tpmlp_linear_pack(tpmlp_ctx* c, const void* W, const void* b, void* stream) {
+    if (!c || !W || !b || c->kind == kKindBlock) return TPMLP_ERR_INVALID_ARG;
+    if (!aligned16(W) || (reinterpret_cast<uintptr_t>(b) & 1)) return TPMLP_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    c->packed = false;
+    int rc = TPMLP_OK;
+    if (c->kind == kKindColumn) {
+        // W [K = H][N = F] -> W1p [F][H] (= [k][f][H]), the layout of the first GEMM
+        const int T = tpmlp::kTransposeTile;
+        dim3 grid(static_cast<unsigned>(c->F / T), static_cast<unsigned>(c->H / T), 1);
+        tpmlp::transpose_bf16_kernel<<<grid, dim3(64, 4), 0, s>>>(
+            static_cast<const uint16_t*>(W), c->W1p, static_cast<int>(c->H),
+            static_cast<int>(c->F), 0, 0);
+        TPMLP_CUDA(c, cudaGetLastError());
+        tpmlp::bf16_to_f32_kernel<<<static_cast<unsigned>((c->F + 255) / 256), 256, 0, s>>>(
+            static_cast<const uint16_t*>(b), c->b1, c->F);
+        TPMLP_CUDA(c, cudaGetLastError());
+        c->launches += 2;
+    } else {
+        // W [K = F][N = H] -> W2p [k][H][f], the layout of the second GEMM
+        if ((rc = pack_second_layer(c, W, b, s))) return rc;
+    }
+    if ((rc = encode_weight_maps(c))) return rc;
+    c->packed = true;
+    return TPMLP_OK;
+}
+
+int tpmlp_linear_forward(tpmlp_ctx* c, const void* X, int64_t M, void* out, void* stream) {
+    if (!c || c->kind == kKindBlock || M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (!c->packed) return TPMLP_ERR_NOT_PACKED;
+    if (M == 0) return TPMLP_OK;
+    if (!X || !out) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(X) || !aligned16(out)) return TPMLP_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (c->kind == kKindColumn) return run_gemm1(c, X, M, out, s, /*linear=*/true);
+    return run_gemm2(c, X, M, out, s);
+}
+
 int tpmlp_get_status(tpmlp_ctx* c, void* stream, int32_t* detail) {
     if (!c) return TPMLP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -698,10 +789,18 @@ int tpmlp_packed_buffer(const tpmlp_ctx* c, int32_t which, const void** ptr, int
     if (!c || !ptr || !bytes) return TPMLP_ERR_INVALID_ARG;
     if (!c->packed) return TPMLP_ERR_NOT_PACKED;
     switch (which) {
-        case 0: *ptr = c->W1p; *bytes = (c->gated ? 2 : 1) * c->H * c->F * 2; return TPMLP_OK;
-        case 1: *ptr = c->W2p; *bytes = c->H * c->F * 2; return TPMLP_OK;
-        case 2: *ptr = c->b1; *bytes = (c->gated ? 2 : 1) * c->F * 4; return TPMLP_OK;
-        case 3: *ptr = c->b2; *bytes = c->H * 4; return TPMLP_OK;
+        case 0:
+            if (!c->W1p) return TPMLP_ERR_INVALID_ARG;
+            *ptr = c->W1p; *bytes = (c->gated ? 2 : 1) * c->H * c->F * 2; return TPMLP_OK;
+        case 1:
+            if (!c->W2p) return TPMLP_ERR_INVALID_ARG;
+            *ptr = c->W2p; *bytes = c->H * c->F * 2; return TPMLP_OK;
+        case 2:
+            if (!c->b1) return TPMLP_ERR_INVALID_ARG;
+            *ptr = c->b1; *bytes = (c->gated ? 2 : 1) * c->F * 4; return TPMLP_OK;
+        case 3:
+            if (!c->b2) return TPMLP_ERR_INVALID_ARG;
+            *ptr = c->b2; *bytes = c->H * 4; return TPMLP_OK;
         default: return TPMLP_ERR_INVALID_ARG;
     }
 }

@@ -49,10 +49,14 @@ static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
 // kGemm1: Y = GeLU(acc + b1).  kGemm1Gated: the accumulator's column halves hold the gate and
 // the up projection of the same outputs, Y = SiLU(gate + bg) * (up + bu).  kGemm2: Z = acc + b2.
 // kGemm2Residual: Z = R + (acc + b2), R the layer's input (the residual add after the block).
-enum class Mode : int { kGemm1 = 1, kGemm2 = 2, kGemm1Gated = 3, kGemm2Residual = 4 };
+// kGemm1Linear: the column-parallel tiling of kGemm1 without the activation (out = acc + b).
+enum class Mode : int {
+    kGemm1 = 1, kGemm2 = 2, kGemm1Gated = 3, kGemm2Residual = 4, kGemm1Linear = 5
+};
 
+// Modes whose B operand is the column-sharded weight (tiles inside one shard, K = H).
 __host__ __device__ constexpr bool is_gemm1(Mode m) {
-    return m == Mode::kGemm1 || m == Mode::kGemm1Gated;
+    return m == Mode::kGemm1 || m == Mode::kGemm1Gated || m == Mode::kGemm1Linear;
 }
 
 // Wait sites recorded in the status word when a bounded wait gives up: (mode << 8) | site.
