@@ -19,6 +19,7 @@ LayerNorm on the full hidden vector before the block, å¤§æ¨¡å‹åˆ†å¸ƒå¼å¹¶è¡Œç­
 The parallel linear layers on their own (the tensor-parallel attention's Q/K/V projection and
 output projection, AIå¤§æ¨¡å‹åˆ†å¸ƒå¼è®­ç»ƒ Â§2.3): column-parallel X W + b, and row-parallel
 sum_i X_i W_i + b.
+The backward pass of the block (dX as a sum over shards; dW1, db1, dW2, db2).
 The gated variant (gate_up_proj column-parallel, down_proj row-parallel: å¤§æ¨¡å‹åˆ†å¸ƒå¼ä¼˜åŒ–æŠ€æœ¯ï¼ˆä¸€ï¼‰
 Â§5.1, AIå¤§æ¨¡å‹åˆ†å¸ƒå¼è®­ç»ƒ Â§6.1) replaces GeLU(X W1 + b1) by SiLU(X Wg + bg) * (X Wu + bu).
 
@@ -74,6 +75,11 @@ class Oracle:
         lib.oracle_block_f64.restype = ctypes.c_int
         lib.oracle_linear_f64.argtypes = [i32, vp, i64, vp, i64, vp, vp, i64, i64, i32, vp]
         lib.oracle_linear_f64.restype = ctypes.c_int
+        lib.oracle_gelu_grad.argtypes = [ctypes.c_double]
+        lib.oracle_gelu_grad.restype = ctypes.c_double
+        lib.oracle_backward_f64.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp,
+                                            vp, vp]
+        lib.oracle_backward_f64.restype = ctypes.c_int
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ctypes.c_int
         self.lib = lib
@@ -196,6 +202,28 @@ class Oracle:
         return out
 
 
+    def gelu_grad(self, a: float) -> float:
+        return float(self.lib.oracle_gelu_grad(float(a)))
+
+    def backward(self, X, W1, b1, W2, dZ, k: int):
+        """Gradients of the block for upstream dZ [M, H]: dict of dX [M,H], dW1 [H,F],
+        db1 [F], dW2 [F,H], db2 [H] (fp64)."""
+        X, W1, b1, W2, dZ = (_u16(a) for a in (X, W1, b1, W2, dZ))
+        M, H = X.shape
+        F = W1.shape[1]
+        if W1.shape != (H, F) or W2.shape != (F, H) or b1.shape != (F,) or dZ.shape != (M, H):
+            raise ValueError("shape mismatch")
+        out = {"dX": np.empty((M, H)), "dW1": np.empty((H, F)), "db1": np.empty(F),
+               "dW2": np.empty((F, H)), "db2": np.empty(H)}
+        rc = self.lib.oracle_backward_f64(
+            X.ctypes.data, W1.ctypes.data, b1.ctypes.data, W2.ctypes.data, dZ.ctypes.data, M, H,
+            F, k, out["dX"].ctypes.data, out["dW1"].ctypes.data, out["db1"].ctypes.data,
+            out["dW2"].ctypes.data, out["db2"].ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return out
+
+
 def _u16(a) -> np.ndarray:
     a = np.ascontiguousarray(a)
     if a.dtype != np.uint16:
@@ -257,3 +285,11 @@ def block(X, gamma, beta, eps, W1, b1, W2, b2, k: int, rows=None, want_xn: bool 
 
 def linear(kind: str, X, W, b, k: int, rows=None):
     return default().linear(kind, X, W, b, k, rows=rows)
+
+
+def gelu_grad(a: float) -> float:
+    return default().gelu_grad(a)
+
+
+def backward(X, W1, b1, W2, dZ, k: int):
+    return default().backward(X, W1, b1, W2, dZ, k)

@@ -385,6 +385,110 @@ int oracle_linear_f64(int32_t kind, const uint16_t *X, int64_t x_rows, const int
     return failed ? -1 : 0;
 }
 
+/*
+ * Backward pass of the block (the pages note that the backward pass repeats the same split
+ * and needs its own All-Reduce: 分布式训练系列第四篇 §4.2-4.3; AI大模型分布式训练 §2.4 counts an
+ * All-Reduce in the forward and one in the backward of each block). Given the upstream
+ * gradient dZ [M, H] of Z = sum_i GeLU(X W1_i + b1_i) W2_i + b2:
+ *   A   = X W1 + b1                      pre-activation   [M, F]
+ *   dY  = dZ W2^T                        per column shard [M, F]
+ *   dA  = dY * GeLU'(A),  GeLU'(a) = Phi(a) + a phi(a),  phi(a) = exp(-a^2 / 2) / sqrt(2 pi)
+ *   dX  = sum_i dA_i W1_i^T              (the backward All-Reduce: a sum over shards)
+ *   dW1 = X^T dA,   db1 = sum_m dA[m, :]
+ *   dW2 = Y^T dZ,   db2 = sum_m dZ[m, :],   Y = GeLU(A)
+ * Sums in index order (over shards last for dX). All outputs are double; dW1 [H][F],
+ * dW2 [F][H]; any output pointer may be NULL to skip it.
+ */
+double oracle_gelu_grad(double a) {
+    const double inv_sqrt_2pi = 0.39894228040143267794; /* 1 / sqrt(2 pi) */
+    return 0.5 * (1.0 + erf(a / sqrt(2.0))) + a * inv_sqrt_2pi * exp(-0.5 * a * a);
+}
+
+int oracle_backward_f64(const uint16_t *X, const uint16_t *W1, const uint16_t *b1,
+                        const uint16_t *W2, const uint16_t *dZ, int64_t M, int64_t H, int64_t F,
+                        int32_t k, double *dX, double *dW1, double *db1, double *dW2,
+                        double *db2) {
+    if (!X || !W1 || !b1 || !W2 || !dZ || M <= 0 || H <= 0 || F <= 0 || k <= 0) return -1;
+    if (F % k != 0) return -1;
+    const int64_t f = F / k;
+    double *A = (double *)malloc(sizeof(double) * (size_t)(M * F));
+    double *dA = (double *)malloc(sizeof(double) * (size_t)(M * F));
+    if (!A || !dA) {
+        free(A);
+        free(dA);
+        return -1;
+    }
+    /* forward pre-activation and dA, row by row */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        double *a = A + m * F;
+        for (int64_t j = 0; j < F; ++j) a[j] = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            const double xh = widen_bf16(X[m * H + h]);
+            for (int64_t j = 0; j < F; ++j) a[j] += xh * widen_bf16(W1[h * F + j]);
+        }
+        for (int64_t j = 0; j < F; ++j) a[j] += widen_bf16(b1[j]);
+        /* dY[m, j] = sum_n dZ[m, n] W2[j, n], then dA = dY * GeLU'(A) */
+        for (int64_t j = 0; j < F; ++j) {
+            double dy = 0.0;
+            for (int64_t n = 0; n < H; ++n) dy += widen_bf16(dZ[m * H + n]) * widen_bf16(W2[j * H + n]);
+            dA[m * F + j] = dy * oracle_gelu_grad(a[j]);
+        }
+    }
+    if (dX) {
+        /* dX[m, h] = sum_i sum_{j in shard i} dA[m, j] W1[h, j]: each shard's partial, then the sum */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t m = 0; m < M; ++m) {
+            for (int64_t h = 0; h < H; ++h) {
+                double total = 0.0;
+                for (int32_t i = 0; i < k; ++i) {
+                    double part = 0.0;
+                    for (int64_t jj = 0; jj < f; ++jj)
+                        part += dA[m * F + i * f + jj] * widen_bf16(W1[h * F + i * f + jj]);
+                    total += part;
+                }
+                dX[m * H + h] = total;
+            }
+        }
+    }
+    if (dW1) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t j = 0; j < F; ++j) {
+                double acc = 0.0;
+                for (int64_t m = 0; m < M; ++m) acc += widen_bf16(X[m * H + h]) * dA[m * F + j];
+                dW1[h * F + j] = acc;
+            }
+    }
+    if (db1) {
+        for (int64_t j = 0; j < F; ++j) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += dA[m * F + j];
+            db1[j] = acc;
+        }
+    }
+    if (dW2) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t j = 0; j < F; ++j)
+            for (int64_t n = 0; n < H; ++n) {
+                double acc = 0.0;
+                for (int64_t m = 0; m < M; ++m)
+                    acc += oracle_gelu(A[m * F + j]) * widen_bf16(dZ[m * H + n]);
+                dW2[j * H + n] = acc;
+            }
+    }
+    if (db2) {
+        for (int64_t n = 0; n < H; ++n) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += widen_bf16(dZ[m * H + n]);
+            db2[n] = acc;
+        }
+    }
+    free(A);
+    free(dA);
+    return 0;
+}
+
 int oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -369,6 +369,35 @@ def pin_linear_row_parallel_is_a_sum_of_partials(orc):
 
 LINEAR_PINS = [pin_linear_matches_numpy, pin_linear_row_parallel_is_a_sum_of_partials]
 
+# ---------------------------------------------------------------------------------
+# backward pass
+def pin_gelu_grad_finite_difference(orc):
+    """GeLU'(a) against central differences of the oracle's own fp64 GeLU."""
+    h = 1e-5
+    for a in np.linspace(-6.0, 6.0, 241):
+        fd = (orc.gelu(float(a) + h) - orc.gelu(float(a) - h)) / (2 * h)
+        assert abs(orc.gelu_grad(float(a)) - fd) <= 1e-9, a
+
+
+def pin_backward_matches_torch_autograd(orc):
+    """All five gradients against torch.autograd in float64 (exact-erf GELU)."""
+    import torch
+    M, H, F = 13, 64, 256
+    d = synth.make_inputs(H, F, M, 71)
+    dZ = synth.normal_bf16(71, 60, (M, H), 1.0)
+    t = {n: torch.from_numpy(synth.bf16_to_f64(v)).requires_grad_(True)
+         for n, v in d.items()}
+    Z = torch.nn.functional.gelu(t["X"] @ t["W1"] + t["b1"]) @ t["W2"] + t["b2"]
+    Z.backward(torch.from_numpy(synth.bf16_to_f64(dZ)))
+    for k in (1, 4):
+        g = orc.backward(d["X"], d["W1"], d["b1"], d["W2"], dZ, k)
+        for name, ref in (("dX", t["X"].grad), ("dW1", t["W1"].grad), ("db1", t["b1"].grad),
+                          ("dW2", t["W2"].grad), ("db2", t["b2"].grad)):
+            assert _rel_fro(g[name], ref.numpy()) <= 1e-12, (k, name, _rel_fro(g[name], ref.numpy()))
+
+
+BACKWARD_PINS = [pin_gelu_grad_finite_difference, pin_backward_matches_torch_autograd]
+
 SWIGLU_PINS = [pin_silu_table_and_expit, pin_silu_odd_part, pin_swiglu_bruteforce_golden,
                pin_swiglu_matches_numpy, pin_swiglu_gate_only, pin_swiglu_k_invariance]
 
@@ -376,4 +405,4 @@ ALL_PINS = [
     pin_gelu_table, pin_gelu_ndtr, pin_gelu_odd_part, pin_bruteforce_golden,
     pin_identity_matches_numpy, pin_concat_identity, pin_row_split_sum, pin_k_invariance,
     pin_w2_zero, pin_w1_zero, pin_rows_independent, pin_x_linear_without_activation,
-] + SWIGLU_PINS + BLOCK_PINS + LINEAR_PINS
+] + SWIGLU_PINS + BLOCK_PINS + LINEAR_PINS + BACKWARD_PINS

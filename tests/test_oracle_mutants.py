@@ -56,6 +56,12 @@ MUTANTS = {
                                               "const double xj = widen_bf16(x[jj]);"),
     "linear_row_bias_per_shard": ("for (int64_t n = 0; n < N; ++n) acc[n] += part[n];",
                                   "for (int64_t n = 0; n < N; ++n) acc[n] += part[n] + widen_bf16(b[n]);"),
+    "gelu_grad_missing_density_term": ("+ a * inv_sqrt_2pi * exp(-0.5 * a * a);", ";"),
+    "gelu_grad_wrong_density": ("exp(-0.5 * a * a)", "exp(-a * a)"),
+    "backward_dx_without_shard_offset": ("widen_bf16(W1[h * F + i * f + jj]);", "widen_bf16(W1[h * F + jj]);"),
+    "backward_dw2_uses_preactivation": ("acc += oracle_gelu(A[m * F + j]) * widen_bf16(dZ[m * H + n]);",
+                                        "acc += A[m * F + j] * widen_bf16(dZ[m * H + n]);"),
+    "backward_dy_transposed_w2": ("widen_bf16(W2[j * H + n]);", "widen_bf16(W2[n * H + j]);"),
     "activation_dropped": ("acc[jj] = (act == ORACLE_ACT_GELU) ? oracle_gelu(a) : a;",
                               "acc[jj] = a;"),
 }
