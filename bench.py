@@ -527,6 +527,116 @@ def run_gpu_linear(args, w: synth.Workload):
     return 0
 
 
+def run_gpu_train(args, w: synth.Workload):
+    """One training step of the block: tpmlp_forward_train (keeps Y and the pre-activation)
+    then tpmlp_backward (dA, dX summed over shards in the accumulator, dW1, dW2, db1, db2).
+    FLOPs: forward 4 M H F, backward 8 M H F (four GEMMs of 2 M H F each)."""
+    import torch
+    import tensor_transformer_mlp_tmem_gb300 as tp
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    d = synth.workload_inputs(w)
+    dZh = synth.normal_bf16(w.seed, 60, (w.M, w.H), 1.0)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    X = to_dev(d["X"]).view(w.B, w.S, w.H)
+    W1, W2 = to_dev(d["W1"]), to_dev(d["W2"])
+    dZ = to_dev(dZh).view(w.B, w.S, w.H)
+    M = w.M
+    Z = torch.empty_like(X)
+    Ys = torch.empty((M, w.F), dtype=torch.bfloat16, device=dev)
+    As = torch.empty_like(Ys)
+    dX = torch.empty_like(X)
+    f32 = torch.float32
+    dW1 = torch.empty((w.H, w.F), dtype=f32, device=dev)
+    db1 = torch.empty((w.F,), dtype=f32, device=dev)
+    dW2 = torch.empty((w.F, w.H), dtype=f32, device=dev)
+    db2 = torch.empty((w.H,), dtype=f32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    mlp = tp.TPMLP(w.H, w.F, w.k)
+    mlp.pack(W1, to_dev(d["b1"]), W2, to_dev(d["b2"]))
+    mlp.reserve(M)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tp.tpmlp_forward_train(mlp.ctx, X, w.B, w.S, Z, Ys, As, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        tp.tpmlp_backward(mlp.ctx, dZ, X, Ys, As, W1, W2, w.B, w.S, dX, dW1, db1, dW2, db2, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    n0 = mlp.launches
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    if pg is not None:
+        pg.barrier()
+    launches = mlp.launches - n0
+    clk = clocks.stop()
+    rc, detail = mlp.status()
+    if rc != tp.TPMLP_OK:
+        raise RuntimeError(f"device status {detail:#x}")
+    fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ms = fwd + bwd
+    if pg is not None:
+        t = torch.tensor([ms, fwd, bwd], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms, fwd, bwd = (float(v) for v in t)
+    flops = 12 * M * w.H * w.F
+    peaks, peak_src = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    value = world * flops / (ms * 1e-3) / 1e12
+    bwd_tf = 8 * M * w.H * w.F / (bwd * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; dZ ~ N(0,1))",
+        "tokens_per_s": world * M / (ms * 1e-3),
+        "kernel_ms": {"forward_train": fwd, "backward": bwd},
+        "config": workload_config(w, {"parallelism": "replicas" if world > 1 else "single GPU",
+                                      "flops_per_step": flops,
+                                      "step": "forward_train + backward (dX, dW1, db1, dW2, db2)"},
+                                  variant="gelu"),
+        "roofline": {"bound": "tensor", "kernel": "backward (dA, dX, dW1, dW2 GEMMs + bias sums)",
+                     "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None},
+        "gpu_launches": launches, "clocks": clk,
+    }
+    line["config"]["variant"] = "train"
+    mlp.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
 def measured_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary
     (profiles/ncu_traffic.json-like lines in profiles/*.md: `traffic <workload> <kernel> <bytes>`),
@@ -557,12 +667,13 @@ def main():
     ap.add_argument("--workload", default="7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--k", type=int, default=None, help="override the shard count")
     ap.add_argument("--variant", default="gelu",
-                    choices=["gelu", "swiglu", "block", "outproj", "qkv"],
+                    choices=["gelu", "swiglu", "block", "outproj", "qkv", "train"],
                     help="gelu: the block of the pages' Megatron figure; swiglu: the gated block; "
                          "block: Z = X + MLP(LayerNorm(X)) (LayerNorm kernel + the GeLU block "
                          "with the residual add in the second GEMM's epilogue); outproj / qkv: "
                          "the tensor-parallel attention's output (row-parallel) and Q/K/V "
-                         "(column-parallel) projections on the workload's shape")
+                         "(column-parallel) projections on the workload's shape; train: the "
+                         "training forward plus the backward pass")
     ap.add_argument("--impl", default="tpmlp", choices=["tpmlp", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--cpu-max-rows", type=int, default=4096)
@@ -575,11 +686,13 @@ def main():
     if args.k is not None:
         w = synth.Workload(w.name, w.B, w.S, w.H, w.F, args.k, w.seed)
     if args.impl == "reference":
-        if args.variant in ("outproj", "qkv"):
+        if args.variant in ("outproj", "qkv", "train"):
             ap.error("the reference arm covers the MLP variants")
         return run_reference(args, w)
     if args.variant in ("outproj", "qkv"):
         return run_gpu_linear(args, w)
+    if args.variant == "train":
+        return run_gpu_train(args, w)
     return run_gpu(args, w)
 
 

@@ -211,6 +211,36 @@ TPMLP_API int tpmlp_gemm2_residual(tpmlp_ctx *ctx, const void *Y, int64_t M, voi
                                    const void *R, void *stream);
 
 /*
+ * Training forward pass of the block: tpmlp_forward, and the activations the backward pass
+ * needs are kept in the caller's buffers.
+ *   Ysave  device bf16 [B*S, F]: Y = GeLU(X W1 + b1) (the first GEMM's output)
+ *   Asave  device bf16 [B*S, F]: the pre-activation A = X W1 + b1
+ * GeLU blocks only (not TPMLP_FLAG_SWIGLU). Errors: as tpmlp_forward.
+ */
+TPMLP_API int tpmlp_forward_train(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z,
+                                  void *Ysave, void *Asave, void *stream);
+
+/*
+ * Backward pass of the block. The pages repeat the split for the gradients, with one more
+ * All-Reduce per block (分布式训练系列第四篇 §4.2-4.3; AI大模型分布式训练 §2.4); here that sum
+ * over shards is again taken in the fp32 accumulator:
+ *   dA  = (dZ W2^T) * GeLU'(A)     per column shard, GeLU'(a) = Phi(a) + a phi(a)
+ *   dX  = sum_i dA_i W1_i^T        the backward All-Reduce, in the accumulator
+ *   dW1 = X^T dA,  db1 = sum over tokens of dA
+ *   dW2 = Y^T dZ,  db2 = sum over tokens of dZ
+ * Inputs (device): dZ bf16 [B*S, H]; X bf16 [B*S, H]; Ysave, Asave from tpmlp_forward_train;
+ * W1 bf16 [H, F] and W2 bf16 [F, H]: the same weights that were packed, in the caller's own
+ * [in, out] layout (read directly; training keeps its parameters). Outputs (device, written,
+ * not accumulated): dX [B*S, H] (bf16, or fp32 with TPMLP_FLAG_Z_FP32); dW1 fp32 [H, F];
+ * db1 fp32 [F]; dW2 fp32 [F, H]; db2 fp32 [H]. The context's Y buffer holds dA meanwhile.
+ * Eight launches; deterministic. GeLU blocks only. Errors: as tpmlp_forward.
+ */
+TPMLP_API int tpmlp_backward(tpmlp_ctx *ctx, const void *dZ, const void *X, const void *Ysave,
+                             const void *Asave, const void *W1, const void *W2, int64_t B,
+                             int64_t S, void *dX, void *dW1, void *db1, void *dW2, void *db2,
+                             void *stream);
+
+/*
  * Read and clear the device status word that the kernels set when a bounded wait gives up
  * (synchronises `stream`). Returns TPMLP_OK, TPMLP_ERR_DEVICE_TIMEOUT or TPMLP_ERR_CUDA.
  * *detail (optional) receives the raw word: which barrier wait gave up.

@@ -25,7 +25,7 @@ __all__ = [
     "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM", "TPMLP_FLAG_SWIGLU", "tpmlp_pack_shards_swiglu",
     "tpmlp_set_layernorm", "tpmlp_layernorm", "tpmlp_block_forward", "tpmlp_gemm2_residual",
     "tpmlp_linear_create", "tpmlp_linear_pack", "tpmlp_linear_forward", "Linear",
-    "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW",
+    "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW", "tpmlp_forward_train", "tpmlp_backward",
 ]
 
 TPMLP_OK = 0
@@ -93,6 +93,9 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_linear_create": ([ctypes.POINTER(vp), i32, i64, i64, i32, u32], ctypes.c_int),
         "tpmlp_linear_pack": ([vp, vp, vp, vp], ctypes.c_int),
         "tpmlp_linear_forward": ([vp, vp, i64, vp, vp], ctypes.c_int),
+        "tpmlp_forward_train": ([vp, vp, i64, i64, vp, vp, vp, vp], ctypes.c_int),
+        "tpmlp_backward": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, vp],
+                           ctypes.c_int),
         "tpmlp_destroy": ([vp], None),
         "tpmlp_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "tpmlp_last_error": ([vp], ctypes.c_char_p),
@@ -249,6 +252,19 @@ def tpmlp_linear_forward(ctx: int, X, M: int, out, stream=None) -> None:
            "tpmlp_linear_forward", ctx)
 
 
+def tpmlp_forward_train(ctx: int, X, B: int, S: int, Z, Ysave, Asave, stream=None) -> None:
+    _check(load_library().tpmlp_forward_train(ctx, _ptr(X), B, S, _ptr(Z), _ptr(Ysave),
+                                              _ptr(Asave), _stream(stream)),
+           "tpmlp_forward_train", ctx)
+
+
+def tpmlp_backward(ctx: int, dZ, X, Ysave, Asave, W1, W2, B: int, S: int, dX, dW1, db1, dW2,
+                   db2, stream=None) -> None:
+    _check(load_library().tpmlp_backward(
+        ctx, _ptr(dZ), _ptr(X), _ptr(Ysave), _ptr(Asave), _ptr(W1), _ptr(W2), B, S, _ptr(dX),
+        _ptr(dW1), _ptr(db1), _ptr(dW2), _ptr(db2), _stream(stream)), "tpmlp_backward", ctx)
+
+
 def tpmlp_destroy(ctx) -> None:
     load_library().tpmlp_destroy(ctx)
 
@@ -352,6 +368,33 @@ class TPMLP:
             Z = torch.empty((B, S, self.H), dtype=self.out_dtype(), device=X.device)
         tpmlp_block_forward(self.ctx, X, B, S, Z, stream)
         return Z
+
+    def forward_train(self, X, stream=None):
+        """Returns (Z, Ysave, Asave); Ysave/Asave feed backward()."""
+        import torch
+        B, S, H = X.shape
+        self._require(X, torch.bfloat16, (B, S, self.H), "X")
+        M = B * S
+        Z = torch.empty((B, S, self.H), dtype=self.out_dtype(), device=X.device)
+        Ys = torch.empty((M, self.F), dtype=torch.bfloat16, device=X.device)
+        As = torch.empty((M, self.F), dtype=torch.bfloat16, device=X.device)
+        tpmlp_forward_train(self.ctx, X, B, S, Z, Ys, As, stream)
+        return Z, Ys, As
+
+    def backward(self, dZ, X, Ysave, Asave, W1, W2, stream=None):
+        """Gradients (dX, dW1, db1, dW2, db2) for upstream dZ [B, S, H]."""
+        import torch
+        B, S, H = X.shape
+        M = B * S
+        dev = X.device
+        dX = torch.empty((B, S, self.H), dtype=self.out_dtype(), device=dev)
+        f32 = torch.float32
+        dW1 = torch.empty((self.H, self.F), dtype=f32, device=dev)
+        db1 = torch.empty((self.F,), dtype=f32, device=dev)
+        dW2 = torch.empty((self.F, self.H), dtype=f32, device=dev)
+        db2 = torch.empty((self.H,), dtype=f32, device=dev)
+        tpmlp_backward(self.ctx, dZ, X, Ysave, Asave, W1, W2, B, S, dX, dW1, db1, dW2, db2, stream)
+        return dX, dW1, db1, dW2, db2
 
     def reserve(self, max_tokens: int):
         tpmlp_reserve(self.ctx, max_tokens)

@@ -17,6 +17,7 @@
 #include "tpmlp_gemm.cuh"
 #include "tpmlp_gemm_2sm.cuh"
 #include "tpmlp_norm.cuh"
+#include "tpmlp_reduce.cuh"
 #include "tpmlp_pack.cuh"
 
 struct tpmlp_ctx {
@@ -60,6 +61,11 @@ struct tpmlp_ctx {
     bool ln_set = false;
     uint16_t* Xn = nullptr;  // [xn_rows][H] normalised block input
     int64_t xn_rows = 0;
+
+    // backward pass
+    float* zeros = nullptr;        // [max(H, F)] fp32 zeros: the "no bias" of dX
+    float* colsum = nullptr;       // partial column sums for the bias gradients
+    int64_t colsum_floats = 0;
 
     int* status = nullptr;  // device status word
     int64_t launches = 0;
@@ -162,10 +168,10 @@ int ensure_smem_attr(tpmlp_ctx* c, Kernel kern, uint32_t smem, std::atomic<uint6
     return TPMLP_OK;
 }
 
-template <int BN, int STAGES, Mode MODE, bool F32>
+template <int BN, int STAGES, Mode MODE, bool F32, bool MN = false>
 int launch_gemm(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                 cudaStream_t s) {
-    auto kern = tpmlp::tpmlp_gemm_kernel<BN, STAGES, MODE, F32>;
+    auto kern = tpmlp::tpmlp_gemm_kernel<BN, STAGES, MODE, F32, MN>;
     constexpr uint32_t smem = tpmlp::GemmSmem<BN, STAGES>::kTotal;
     static std::atomic<uint64_t> attr_done{0};
     if (int rc = ensure_smem_attr(c, kern, smem, attr_done)) return rc;
@@ -262,7 +268,7 @@ int activation_map(tpmlp_ctx* c, const void* ptr, int64_t rows, int64_t cols,
 }
 
 int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s,
-              bool linear = false) {
+              bool linear = false, void* A_save = nullptr) {
     int rc = activation_map(c, X, M, c->H, c->x_map_ptr, c->x_map_rows, c->tmX);
     if (rc) return rc;
     const CUtensorMap& tmX = c->tmX;
@@ -283,6 +289,14 @@ int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s,
             return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1Gated, false>(
                 c, tmX, c->tmW1_pair, a, s);
         return dispatch_gemm<Mode::kGemm1Gated, false>(c, c->bn1, tmX, c->tmW1, a, s);
+    }
+    if (A_save) {
+        // training forward: also keep the pre-activation for the backward pass
+        a.out2 = A_save;
+        if (pair)
+            return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1Train, false>(
+                c, tmX, c->tmW1_pair, a, s);
+        return dispatch_gemm<Mode::kGemm1Train, false>(c, c->bn1, tmX, c->tmW1, a, s);
     }
     if (linear) {
         // column-parallel linear layer: bias only, output bf16 or fp32
@@ -446,6 +460,67 @@ int run_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t
 }
 
 int create_context(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flags, int kind);
+
+// bf16 [rows][cols] map with a 64 x 64 box: an M-contiguous operand of a weight-gradient GEMM
+// (inner index = output row or column, outer index = token).
+int token_major_map(tpmlp_ctx* c, CUtensorMap* map, const void* ptr, int64_t tokens, int64_t cols) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(tokens)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(cols) * 2};
+    const uint32_t box[2] = {64, 64};
+    return encode_map(c, map, ptr, 2, dims, strides, box);
+}
+
+// fp32 out[R][C] = sum over tokens of Aop[t][r] * Bop[t][c]  (A = X or Y, B = dA or dZ)
+int run_weight_grad(tpmlp_ctx* c, const void* Aop, int64_t R, const void* Bop, int64_t C,
+                    int64_t tokens, float* out, cudaStream_t s) {
+    CUtensorMap ta, tb;
+    int rc = token_major_map(c, &ta, Aop, tokens, R);
+    if (rc || (rc = token_major_map(c, &tb, Bop, tokens, C))) return rc;
+    const int bn = pick_bn(C);
+    GemmArgs a{};
+    a.M = static_cast<int>(R);
+    a.ldo = static_cast<int>(C);
+    a.f = static_cast<int>(C);
+    a.k = 1;
+    a.kb_tile = static_cast<int>((tokens + tpmlp::kBK - 1) / tpmlp::kBK);
+    a.kb_shard = a.kb_tile;
+    a.m_blocks = static_cast<int>((R + tpmlp::kBM - 1) / tpmlp::kBM);
+    a.n_blocks = static_cast<int>(C / bn);
+    a.num_tiles = a.m_blocks * a.n_blocks;
+    a.group_m = 8;
+    a.out = out;
+    a.status = c->status;
+    switch (bn) {
+        case 256: return launch_gemm<256, TPMLP_STAGES_256, Mode::kWeightGrad, true, true>(c, ta, tb, a, s);
+        case 128: return launch_gemm<128, 6, Mode::kWeightGrad, true, true>(c, ta, tb, a, s);
+        default: return launch_gemm<64, 8, Mode::kWeightGrad, true, true>(c, ta, tb, a, s);
+    }
+}
+
+// out[c] = sum over the M rows of in[m][c] (bf16 in, fp32 out), deterministic.
+int run_colsum(tpmlp_ctx* c, const void* in, int64_t M, int64_t C, float* out, cudaStream_t s) {
+    const int splits = static_cast<int>(std::min<int64_t>((M + 255) / 256, 128));
+    const int rows_per_split = static_cast<int>((M + splits - 1) / splits);
+    const int64_t need = static_cast<int64_t>(splits) * C;
+    if (need > c->colsum_floats) {
+        TPMLP_CUDA(c, cudaDeviceSynchronize());
+        cudaFree(c->colsum);
+        c->colsum = nullptr;
+        c->colsum_floats = 0;
+        TPMLP_CUDA(c, cudaMalloc(&c->colsum, static_cast<size_t>(need) * 4));
+        c->colsum_floats = need;
+    }
+    dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(splits));
+    tpmlp::colsum_partial_kernel<<<grid, tpmlp::kColsumThreads, 0, s>>>(
+        static_cast<const uint16_t*>(in), static_cast<int>(M), static_cast<int>(C), rows_per_split,
+        c->colsum);
+    TPMLP_CUDA(c, cudaGetLastError());
+    tpmlp::colsum_final_kernel<<<static_cast<unsigned>((C + 255) / 256), 256, 0, s>>>(
+        c->colsum, splits, static_cast<int>(C), out);
+    TPMLP_CUDA(c, cudaGetLastError());
+    c->launches += 2;
+    return TPMLP_OK;
+}
 
 }  // namespace
 
@@ -774,6 +849,108 @@ int tpmlp_linear_forward(tpmlp_ctx* c, const void* X, int64_t M, void* out, void
     return run_gemm2(c, X, M, out, s);
 }
 
+int tpmlp_forward_train(tpmlp_ctx* c, const void* X, int64_t B, int64_t S, void* Z, void* Ysave,
+                        void* Asave, void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (c->gated) return TPMLP_ERR_INVALID_ARG;
+    if ((rc = check_tokens(B, S))) return rc;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if (!X || !Z || !Ysave || !Asave) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(X) || !aligned16(Z) || !aligned16(Ysave) || !aligned16(Asave))
+        return TPMLP_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = run_gemm1(c, X, M, Ysave, s, false, Asave))) return rc;
+    return run_gemm2(c, Ysave, M, Z, s);
+}
+
+int tpmlp_backward(tpmlp_ctx* c, const void* dZ, const void* X, const void* Ysave,
+                   const void* Asave, const void* W1, const void* W2, int64_t B, int64_t S,
+                   void* dX, void* dW1, void* db1, void* dW2, void* db2, void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (c->gated) return TPMLP_ERR_INVALID_ARG;
+    if ((rc = check_tokens(B, S))) return rc;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if (!dZ || !X || !Ysave || !Asave || !W1 || !W2 || !dX || !dW1 || !db1 || !dW2 || !db2)
+        return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    for (const void* p : {dZ, X, Ysave, Asave, W1, W2, static_cast<const void*>(dX),
+                          static_cast<const void*>(dW1), static_cast<const void*>(db1),
+                          static_cast<const void*>(dW2), static_cast<const void*>(db2)})
+        if (!aligned16(p)) return TPMLP_ERR_MISALIGNED;
+    if ((rc = ensure_y(c, M))) return rc;  // the context's Y buffer holds dA
+    if (!c->zeros) {
+        const size_t n = static_cast<size_t>(std::max(c->H, c->F));
+        TPMLP_CUDA(c, cudaMalloc(&c->zeros, n * 4));
+        TPMLP_CUDA(c, cudaMemset(c->zeros, 0, n * 4));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // (1) dA = (dZ W2^T) * GeLU'(A): the first GEMM's tiling over the caller's W2 [F][H],
+    //     whose row shards are K-major blocks [k][f][H]
+    {
+        CUtensorMap tdz, tw2, tw2p;
+        int r = activation_map(c, dZ, M, c->H, c->x_map_ptr, c->x_map_rows, c->tmX);
+        if (r) return r;
+        tdz = c->tmX;
+        const uint64_t dims[3] = {static_cast<uint64_t>(c->H), static_cast<uint64_t>(c->f),
+                                  static_cast<uint64_t>(c->k)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(c->H) * 2,
+                                     static_cast<uint64_t>(c->f) * c->H * 2};
+        const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(c->bn1), 1};
+        const uint32_t box_pair[3] = {tpmlp::kBK, 128, 1};
+        if ((r = encode_map(c, &tw2, W2, 3, dims, strides, box)) ||
+            (r = encode_map(c, &tw2p, W2, 3, dims, strides, box_pair)))
+            return r;
+        GemmArgs a = base_args(c, M, static_cast<int>(c->F), c->pair1 ? tpmlp::kPairBM : tpmlp::kBM,
+                               c->pair1 ? tpmlp::kPairBN : c->bn1, TPMLP_GROUP_M1);
+        a.kb_tile = static_cast<int>(c->H / tpmlp::kBK);
+        a.kb_shard = a.kb_tile;
+        a.out = c->Y;
+        a.residual = Asave;
+        r = c->pair1 ? launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kBwdDA, false>(c, tdz, tw2p, a, s)
+                     : dispatch_gemm<Mode::kBwdDA, false>(c, c->bn1, tdz, tw2, a, s);
+        if (r) return r;
+    }
+    // (2) dX = sum_i dA_i W1_i^T: the second GEMM's shard-major reduction over the caller's
+    //     W1 [H][F], read as [k][H][f] blocks (element (j, h, i) at W1 + h F + i f + j)
+    {
+        CUtensorMap tw1, tw1p;
+        const uint64_t dims[3] = {static_cast<uint64_t>(c->f), static_cast<uint64_t>(c->H),
+                                  static_cast<uint64_t>(c->k)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(c->F) * 2, static_cast<uint64_t>(c->f) * 2};
+        const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(c->bn2), 1};
+        const uint32_t box_pair[3] = {tpmlp::kBK, 128, 1};
+        int r = encode_map(c, &tw1, W1, 3, dims, strides, box);
+        if (r || (r = encode_map(c, &tw1p, W1, 3, dims, strides, box_pair))) return r;
+        if ((r = activation_map(c, c->Y, M, c->F, c->y_map_ptr, c->y_map_rows, c->tmY))) return r;
+        GemmArgs a = base_args(c, M, static_cast<int>(c->H), c->pair2 ? tpmlp::kPairBM : tpmlp::kBM,
+                               c->pair2 ? tpmlp::kPairBN : c->bn2, TPMLP_GROUP_M2);
+        a.kb_shard = static_cast<int>(c->f / tpmlp::kBK);
+        a.kb_tile = a.kb_shard * c->k;
+        a.bias = c->zeros;
+        a.out = dX;
+        const bool f32 = (c->flags & TPMLP_FLAG_Z_FP32) != 0;
+        if (c->pair2)
+            r = f32 ? launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, true>(c, c->tmY, tw1p, a, s)
+                    : launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, false>(c, c->tmY, tw1p, a, s);
+        else
+            r = f32 ? dispatch_gemm<Mode::kGemm2, true>(c, c->bn2, c->tmY, tw1, a, s)
+                    : dispatch_gemm<Mode::kGemm2, false>(c, c->bn2, c->tmY, tw1, a, s);
+        if (r) return r;
+    }
+    // (3) dW1 = X^T dA [H][F], (4) dW2 = Y^T dZ [F][H]: reductions over the tokens
+    if ((rc = run_weight_grad(c, X, c->H, c->Y, c->F, M, static_cast<float*>(dW1), s))) return rc;
+    if ((rc = run_weight_grad(c, Ysave, c->F, dZ, c->H, M, static_cast<float*>(dW2), s))) return rc;
+    // (5) db1 = sum over tokens of dA, db2 = sum over tokens of dZ
+    if ((rc = run_colsum(c, c->Y, M, c->F, static_cast<float*>(db1), s))) return rc;
+    return run_colsum(c, dZ, M, c->H, static_cast<float*>(db2), s);
+}
+
 int tpmlp_get_status(tpmlp_ctx* c, void* stream, int32_t* detail) {
     if (!c) return TPMLP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -819,6 +996,8 @@ void tpmlp_destroy(tpmlp_ctx* c) {
     cudaFree(c->Xs);
     cudaFree(c->Zs);
     cudaFree(c->Xn);
+    cudaFree(c->zeros);
+    cudaFree(c->colsum);
     cudaFree(c->ln_gamma);
     cudaFree(c->ln_beta);
     cudaFree(c->status);

@@ -50,13 +50,18 @@ static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
 // the up projection of the same outputs, Y = SiLU(gate + bg) * (up + bu).  kGemm2: Z = acc + b2.
 // kGemm2Residual: Z = R + (acc + b2), R the layer's input (the residual add after the block).
 // kGemm1Linear: the column-parallel tiling of kGemm1 without the activation (out = acc + b).
+// Backward: kGemm1Train writes Y = GeLU(acc + b1) and the pre-activation A = acc + b1;
+// kBwdDA: dA = acc * GeLU'(A) (aux = the saved A); kWeightGrad: plain fp32 acc (no bias), with
+// both operands M-contiguous (the reduction runs over tokens).
 enum class Mode : int {
-    kGemm1 = 1, kGemm2 = 2, kGemm1Gated = 3, kGemm2Residual = 4, kGemm1Linear = 5
+    kGemm1 = 1, kGemm2 = 2, kGemm1Gated = 3, kGemm2Residual = 4, kGemm1Linear = 5,
+    kGemm1Train = 6, kBwdDA = 7, kWeightGrad = 8
 };
 
 // Modes whose B operand is the column-sharded weight (tiles inside one shard, K = H).
 __host__ __device__ constexpr bool is_gemm1(Mode m) {
-    return m == Mode::kGemm1 || m == Mode::kGemm1Gated || m == Mode::kGemm1Linear;
+    return m == Mode::kGemm1 || m == Mode::kGemm1Gated || m == Mode::kGemm1Linear ||
+           m == Mode::kGemm1Train || m == Mode::kBwdDA;
 }
 
 // Wait sites recorded in the status word when a bounded wait gives up: (mode << 8) | site.
@@ -75,7 +80,9 @@ struct GemmArgs {
     int group_m;    // tile rasterisation: this many row blocks share a column sweep
     const float* bias;  // [ldo] fp32
     void* out;          // [M][ldo] bf16 or fp32
-    const void* residual;  // kGemm2Residual: [M][ldo] bf16 added to the output (may equal out)
+    const void* residual;  // kGemm2Residual: [M][ldo] bf16 added to the output (may equal out);
+                           // kBwdDA: the saved pre-activation A [M][ldo] bf16
+    void* out2;            // kGemm1Train: the pre-activation A [M][ldo] bf16
     int* status;        // device status word
 };
 
@@ -94,11 +101,23 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
+// Descriptor for an MN-major operand tile (M- or N-index contiguous): TMA boxes of 64 (MN)
+// x 64 (K) bf16, each 8 KB, placed one after another along MN. In a box a K row is 128 bytes
+// of 64 consecutive MN elements, 128-byte swizzled in groups of 8 rows.
+//   leading-dimension byte offset: 8192 B between consecutive 64-wide MN blocks
+//   stride-dimension byte offset:  1024 B between consecutive 8-row K groups
+__device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+           (static_cast<uint64_t>(8192 >> 4) << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+           (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9 and
-// 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
+// 10-12 = 1), A / B major-ness in bits 15 / 16 (0 = K-major, 1 = MN-major), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (mn_major ? (1u << 15) | (1u << 16) : 0u) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 template <int BN, int STAGES>
@@ -116,6 +135,12 @@ __device__ __forceinline__ float gelu_erf(float a) {
     return 0.5f * a * (1.0f + erff(a * 0.70710678118654752440f));
 }
 
+// GeLU'(a) = Phi(a) + a phi(a), phi the standard normal density (CUDA's erff and expf).
+__device__ __forceinline__ float gelu_grad(float a) {
+    return 0.5f * (1.0f + erff(a * 0.70710678118654752440f)) +
+           a * 0.39894228040143267794f * expf(-0.5f * a * a);
+}
+
 // SiLU(a) = a * sigma(a) = a / (1 + e^-a), with CUDA's expf.
 __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
@@ -128,22 +153,56 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <Mode MODE, bool OUT_F32>
 __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const float* __restrict__ bias,
                                                void* out, int row, int M, int ldo, int col,
-                                               const void* residual = nullptr) {
+                                               const void* residual = nullptr,
+                                               void* out2 = nullptr) {
     float x[32];
-    const float4* b4 = reinterpret_cast<const float4*>(bias + col);
+    if constexpr (MODE == Mode::kBwdDA || MODE == Mode::kWeightGrad) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float4 bb = __ldg(b4 + j);
-        x[4 * j + 0] = __uint_as_float(v[4 * j + 0]) + bb.x;
-        x[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + bb.y;
-        x[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + bb.z;
-        x[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + bb.w;
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);  // no bias
+    } else {
+        const float4* b4 = reinterpret_cast<const float4*>(bias + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 bb = __ldg(b4 + j);
+            x[4 * j + 0] = __uint_as_float(v[4 * j + 0]) + bb.x;
+            x[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + bb.y;
+            x[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + bb.z;
+            x[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + bb.w;
+        }
     }
-    if constexpr (MODE == Mode::kGemm1) {
+    if constexpr (MODE == Mode::kGemm1Train) {
+        // save the pre-activation for the backward pass, then apply GeLU
+        if (row < M) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out2) +
+                                                  static_cast<size_t>(row) * ldo + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]),
+                                    pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
+                                    pack_bf16x2(x[8 * j + 4], x[8 * j + 5]),
+                                    pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+        }
+    }
+    if constexpr (MODE == Mode::kGemm1 || MODE == Mode::kGemm1Train) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = gelu_erf(x[j]);
     }
     if (row >= M) return;
+    if constexpr (MODE == Mode::kBwdDA) {
+        // dA = dY * GeLU'(A), A the saved (bf16) pre-activation
+        const uint4* a4 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(residual) +
+                                                         static_cast<size_t>(row) * ldo + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 u = a4[j];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[8 * j + 2 * i] *= gelu_grad(__uint_as_float(w[i] << 16));
+                x[8 * j + 2 * i + 1] *= gelu_grad(__uint_as_float(w[i] & 0xFFFF0000u));
+            }
+        }
+    }
     if constexpr (MODE == Mode::kGemm2Residual) {
         // read before the store below: the output may be the residual buffer itself
         const uint4* r4 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(residual) +
@@ -241,7 +300,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs
             ptx::tmem_wait_ld(v);
             if (c + 32 == c0 + kCols) release();
             epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo, n0 + c,
-                                          args.residual);
+                                          args.residual, args.out2);
         }
     }
 }
@@ -258,12 +317,15 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, int t, int& m_blk
 
 // A: GEMM1 -> X [M][H] (2-D map, box 64 x 128); GEMM2 -> Y [M][F] (2-D map, box 64 x 128).
 // B: GEMM1 -> W1p [k][f][H] (3-D map, box 64 x BN x 1); GEMM2 -> W2p [k][H][f] (same box).
-template <int BN, int STAGES, Mode MODE, bool OUT_F32>
+// MN: both operands M-/N-contiguous (the weight-gradient GEMMs, reduction over tokens):
+// A = 2 TMA boxes of 64 (M) x 64 (K), B = BN/64 boxes of 64 (N) x 64 (K); the maps' inner
+// dimension is the output row / column index and the outer one the token.
+template <int BN, int STAGES, Mode MODE, bool OUT_F32, bool MN = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     tpmlp_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
     using L = GemmSmem<BN, STAGES>;
-    constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, MN);
     constexpr int kCode = static_cast<int>(MODE) << 8;
 
     extern __shared__ uint8_t smem_raw[];
@@ -332,7 +394,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t sa = base + stage * L::kStageBytes;
                     const uint32_t sb = sa + L::kABytes;
                     ptx::mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
-                    if constexpr (is_gemm1(MODE)) {
+                    if constexpr (MN) {
+#pragma unroll
+                        for (int b = 0; b < kBM / 64; ++b)
+                            ptx::tma_load_2d(sa + b * 8192, &tmA, full_bar(stage), m0 + 64 * b,
+                                             kb * kBK);
+#pragma unroll
+                        for (int b = 0; b < BN / 64; ++b)
+                            ptx::tma_load_2d(sb + b * 8192, &tmB, full_bar(stage), n0 + 64 * b,
+                                             kb * kBK);
+                    } else if constexpr (is_gemm1(MODE)) {
                         ptx::tma_load_2d(sa, &tmA, full_bar(stage), kb * kBK, m0);
                         ptx::tma_load_3d(sb, &tmB, full_bar(stage), kb * kBK, n_in_shard1, shard1);
                     } else {
@@ -378,12 +449,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t sa = base + stage * L::kStageBytes;
-                    const uint64_t da = sdesc_k128(sa);
-                    const uint64_t db = sdesc_k128(sa + L::kABytes);
+                    const uint64_t da = MN ? sdesc_mn128(sa) : sdesc_k128(sa);
+                    const uint64_t db = MN ? sdesc_mn128(sa + L::kABytes) : sdesc_k128(sa + L::kABytes);
+                    // one MMA covers 16 of the stage's 64 K: 32 bytes along a K-major row
+                    // (>> 4 = 2), or 16 rows of 128 bytes in an MN-major box (>> 4 = 128)
+                    constexpr uint32_t kStep = MN ? 128u : 2u;
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        // advance both descriptors by kk * 16 elements = 32 bytes (>> 4 = 2)
-                        ptx::mma_bf16_ss(d_tmem, da + 2u * kk, db + 2u * kk, kIdesc,
+                        ptx::mma_bf16_ss(d_tmem, da + kStep * kk, db + kStep * kk, kIdesc,
                                          (kb | kk) != 0 ? 1u : 0u);
                     }
                     ptx::mma_commit(empty_bar(stage));  // stage free once these MMAs finish
