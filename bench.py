@@ -87,6 +87,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(values, pg=None, device="cpu"):
+    """Element-wise maximum of a list of floats over all ranks (identity without a group)."""
+    if pg is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_tflops(world: int, flops_per_rank_step: int, ms_per_step: float) -> float:
+    """Throughput of all ranks together: every rank did flops_per_rank_step in the slowest
+    rank's step time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
             int(os.environ.get("WORLD_SIZE", "1")))
@@ -94,7 +110,9 @@ def dist_env():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms; stop() keeps the samples taken inside the timed window
+    (mark_start / mark_stop) when there are any, else all of them (and says so)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -102,6 +120,13 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
 
     def start(self):
         try:
@@ -111,7 +136,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except Exception as e:  # no nvidia-smi: record nothing
             log("clock sampling unavailable:", e)
@@ -126,6 +151,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
+        import datetime
         rows = []
         with open(self.path) as fh:
             for ln in fh:
@@ -133,19 +159,24 @@ class ClockSampler:
                 if len(parts) < 9:
                     continue
                 try:
-                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
                 except ValueError:
                     continue
         os.unlink(self.path)
         if not rows:
             return None
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None
+                  and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        mx = max(r[1] for r in rows)
-        loaded = [r for r in rows if r[0] >= 0.5 * mx] or rows
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[2])
+        mx = max(r[2] for r in use)
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3])
                           if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": mx,
-                "reasons": reasons, "samples": len(rows)}
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole run (no sample fell inside the "
+                                                         "timed region)"}
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
@@ -309,11 +340,13 @@ def run_gpu(args, w: synth.Workload):
     launches0 = mlp.launches
     barrier()
     torch.cuda.synchronize(dev)
+    clocks.mark_start()
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
         step(evs[i])
     torch.cuda.synchronize(dev)
+    clocks.mark_stop()
     barrier()
     t_wall = time.perf_counter() - t_wall0
     launches = mlp.launches - launches0
@@ -331,10 +364,7 @@ def run_gpu(args, w: synth.Workload):
     g2 = [e[1].elapsed_time(e[2]) for e in evs]
     st = [e[0].elapsed_time(e[2]) for e in evs]
     ms_step = statistics.mean(st)
-    if pg is not None:
-        t = torch.tensor([ms_step, t_wall], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step, t_wall = float(t[0]), float(t[1])
+    ms_step, t_wall = max_over_ranks([ms_step, t_wall], pg, dev)
 
     # ---- end to end through the host-buffer entry point (pinned host memory)
     Xh = torch.from_numpy(np.ascontiguousarray(d["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -359,16 +389,13 @@ def run_gpu(args, w: synth.Workload):
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if pg is not None:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t[0])
+    (e2e_s,) = max_over_ranks([e2e_s], pg, dev)
     rc, detail = mlp.status()
     if rc != tp.TPMLP_OK:
         raise RuntimeError(f"device status after e2e steps: {detail:#x}")
 
     flops_step = step_flops(w, variant)
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, ms_step)
     tokens = world * w.M / (ms_step * 1e-3)
     peaks, peak_src = load_peaks()
     peak_burst = peaks["bf16_tflops"]
@@ -480,12 +507,14 @@ def run_gpu_linear(args, w: synth.Workload):
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize(dev)
+    clocks.mark_start()
     for i in range(args.steps):
         flush.zero_()
         evs[i][0].record(stream)
         tp.tpmlp_linear_forward(lin.ctx, Xd, M, out, stream)
         evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark_stop()
     if pg is not None:
         pg.barrier()
     launches = tp.tpmlp_launch_count(lin.ctx) - n0
@@ -494,14 +523,11 @@ def run_gpu_linear(args, w: synth.Workload):
     if rc != tp.TPMLP_OK:
         raise RuntimeError(f"device status {detail:#x}")
     ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    if pg is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t[0])
+    (ms,) = max_over_ranks([ms], pg, dev)
     flops = 2 * M * K * N
     peaks, peak_src = load_peaks()
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -589,10 +615,12 @@ def run_gpu_train(args, w: synth.Workload):
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize(dev)
+    clocks.mark_start()
     for i in range(args.steps):
         flush.zero_()
         step(evs[i])
     torch.cuda.synchronize(dev)
+    clocks.mark_stop()
     if pg is not None:
         pg.barrier()
     launches = mlp.launches - n0
@@ -603,14 +631,11 @@ def run_gpu_train(args, w: synth.Workload):
     fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     ms = fwd + bwd
-    if pg is not None:
-        t = torch.tensor([ms, fwd, bwd], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms, fwd, bwd = (float(v) for v in t)
+    ms, fwd, bwd = max_over_ranks([ms, fwd, bwd], pg, dev)
     flops = 12 * M * w.H * w.F
     peaks, peak_src = load_peaks()
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms)
     bwd_tf = 8 * M * w.H * w.F / (bwd * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -662,7 +687,7 @@ def measured_traffic(workload: str, kernel: str):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--k", type=int, default=None, help="override the shard count")

@@ -38,12 +38,14 @@ def stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str = None) -> str:
     """Compile every .cu under csrc/ into one shared library (a few seconds per kernel
-    instantiation). Returns the library path."""
-    if not force and not stale():
+    instantiation). Returns the library path. `out` + `extra_flags` build a variant (for
+    instance a test build with a planted pipeline stall) at another path."""
+    lib = out or LIB
+    if out is None and not force and not stale():
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", INCLUDE,
            "-I", CSRC, "-DTPMLP_BUILD", *extra_flags, *sources(), "-o", tmp]
@@ -51,5 +53,5 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd))
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib

@@ -393,6 +393,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                     const uint32_t sa = base + stage * L::kStageBytes;
                     const uint32_t sb = sa + L::kABytes;
+#ifdef TPMLP_TEST_SKIP_STAGE
+                    // test builds only: never fill this stage, so the MMA's wait on it runs out
+                    if (issued == TPMLP_TEST_SKIP_STAGE) {
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+#endif
                     ptx::mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
                     if constexpr (MN) {
 #pragma unroll
