@@ -116,6 +116,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     }
                     const uint32_t sa = base + stage * L::kStageBytes;
                     const uint32_t sb = sa + L::kABytes;
+#ifdef TPMLP_TEST_SKIP_STAGE
+                    // test builds only: rank 0 never arms this stage, so the MMA's wait runs out
+                    if (leader && issued == TPMLP_TEST_SKIP_STAGE) {
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+#endif
                     const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // rank 0's barrier
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
                     if constexpr (is_gemm1(MODE)) {

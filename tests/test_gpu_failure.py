@@ -1,5 +1,6 @@
 """Failure detection without a GPU fault: a test build of the library whose TMA producer
-never fills one pipeline stage. The MMA warp's bounded wait on that stage runs out after
+never fills one pipeline stage (in the CTA-pair kernel: rank 0 never arms it, while its
+peer's copies still land). The MMA warp's bounded wait on that stage runs out after
 about a second; the kernel records where in the device status word, drains what it has in
 flight, frees its tensor memory and returns. The host reads TPMLP_ERR_DEVICE_TIMEOUT and the
 CUDA context stays usable (the regular library still computes the right answer afterwards)."""
@@ -19,12 +20,18 @@ from gpu_util import assert_close, inputs_on_device, to_f64
 pytestmark = pytest.mark.gpu
 
 GEMM1_MMA_FULL_WAIT = (1 << 8) | 3  # (mode << 8) | wait site, as the kernel records it
+PAIR = 0x80                         # set by the CTA-pair kernel
 
 
-def test_pipeline_wait_runs_out_and_is_reported(lib, tmp_path):
-    path = _build.build(out=str(tmp_path / "libtpmlp_stall.so"),
+@pytest.fixture(scope="module")
+def stall_lib(tmp_path_factory):
+    return _build.build(out=str(tmp_path_factory.mktemp("stall") / "libtpmlp_stall.so"),
                         extra_flags=["-DTPMLP_TEST_SKIP_STAGE=5"])
-    dbg = ctypes.CDLL(path)
+
+
+@pytest.mark.parametrize("single_sm", [True, False], ids=["single-SM", "CTA-pair"])
+def test_pipeline_wait_runs_out_and_is_reported(lib, stall_lib, single_sm):
+    dbg = ctypes.CDLL(stall_lib)
     vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
     dbg.tpmlp_create.argtypes = [ctypes.POINTER(vp), i64, i64, i32, u32]
     dbg.tpmlp_pack_shards.argtypes = [vp] * 6
@@ -37,7 +44,8 @@ def test_pipeline_wait_runs_out_and_is_reported(lib, tmp_path):
     dd = inputs_on_device(d)
     Y = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
     ctx = vp()
-    assert dbg.tpmlp_create(ctypes.byref(ctx), H, F, k, tp.TPMLP_FLAG_SINGLE_SM) == 0
+    flags = tp.TPMLP_FLAG_SINGLE_SM if single_sm else 0
+    assert dbg.tpmlp_create(ctypes.byref(ctx), H, F, k, flags) == 0
     try:
         assert dbg.tpmlp_pack_shards(ctx, dd["W1"].data_ptr(), dd["b1"].data_ptr(),
                                      dd["W2"].data_ptr(), dd["b2"].data_ptr(), None) == 0
@@ -47,7 +55,7 @@ def test_pipeline_wait_runs_out_and_is_reported(lib, tmp_path):
         rc = dbg.tpmlp_get_status(ctx, None, ctypes.byref(detail))
         elapsed = time.time() - t0
         assert rc == tp.TPMLP_ERR_DEVICE_TIMEOUT
-        assert detail.value == GEMM1_MMA_FULL_WAIT, hex(detail.value)
+        assert detail.value == GEMM1_MMA_FULL_WAIT | (0 if single_sm else PAIR), hex(detail.value)
         assert 0.5 < elapsed < 30.0
         # the status word was cleared by the read
         assert dbg.tpmlp_get_status(ctx, None, ctypes.byref(detail)) == tp.TPMLP_OK
@@ -55,7 +63,7 @@ def test_pipeline_wait_runs_out_and_is_reported(lib, tmp_path):
         dbg.tpmlp_destroy(ctx)
 
     torch.cuda.synchronize()  # no sticky CUDA error: the context is still usable
-    with tp.TPMLP(H, F, k, single_sm=True) as mlp:
+    with tp.TPMLP(H, F, k, single_sm=single_sm) as mlp:
         mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
         Z = mlp(dd["X"].view(1, M, H))
         torch.cuda.synchronize()
