@@ -134,9 +134,12 @@ TPMLP_API int tpmlp_forward(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S,
 
 /*
  * tpmlp_forward on host buffers: copies X (host, [B,S,H] bf16) to a device staging buffer,
- * runs the forward pass and copies Z back to host memory, all on `stream`, then waits for
- * the stream. Page-locked host memory gives asynchronous, full-speed copies; pageable
- * memory works but is slower. Staging buffers are owned by the context and grow on demand.
+ * runs the forward pass and copies Z back to host memory, then waits for `stream`. Token rows
+ * are independent, so the work is split into up to 4 row chunks of at least 2048 rows: the
+ * copies in and out run on two streams of the context and overlap the GEMMs of the other
+ * chunks (which run on `stream`, after the work already queued there). Page-locked host
+ * memory gives asynchronous, full-speed copies; pageable memory works but is slower.
+ * Staging buffers are owned by the context and grow on demand.
  * Errors: as tpmlp_forward.
  */
 TPMLP_API int tpmlp_forward_host(tpmlp_ctx *ctx, const void *X_host, int64_t B, int64_t S, void *Z_host,

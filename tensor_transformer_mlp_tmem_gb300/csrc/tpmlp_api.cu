@@ -45,6 +45,8 @@ struct tpmlp_ctx {
     void* Xs = nullptr;  // staging for tpmlp_forward_host
     void* Zs = nullptr;
     int64_t stage_rows = 0;
+    cudaStream_t s_in = nullptr, s_out = nullptr;  // its copy streams (created on first use)
+    cudaEvent_t host_ev[5] = {}, in_ev[4] = {}, out_ev[4] = {};
 
     // activation tensor maps of the last call (re-encoded only when pointer or rows change)
     const void* x_map_ptr = nullptr;
@@ -93,6 +95,8 @@ struct tpmlp_ctx {
 #endif
 
 namespace {
+
+constexpr int kHostChunksMax = 4;  // row chunks of tpmlp_forward_host's copy/compute pipeline
 
 using tpmlp::GemmArgs;
 using tpmlp::Mode;
@@ -717,6 +721,7 @@ int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, v
     const int64_t M = B * S;
     if (M == 0) return TPMLP_OK;
     if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if (M > c->stage_rows) {
         TPMLP_CUDA(c, cudaDeviceSynchronize());
         if (c->Xs) cudaFree(c->Xs);
@@ -727,12 +732,49 @@ int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, v
         TPMLP_CUDA(c, cudaMalloc(&c->Zs, static_cast<size_t>(M) * c->H * z_elem_bytes(c)));
         c->stage_rows = M;
     }
+    if ((rc = ensure_y(c, M))) return rc;
+    if (!c->s_in) {
+        TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking));
+        TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking));
+        for (int i = 0; i < kHostChunksMax + 1; ++i)
+            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->host_ev[i], cudaEventDisableTiming));
+        for (int i = 0; i < kHostChunksMax; ++i) {
+            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->in_ev[i], cudaEventDisableTiming));
+            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->out_ev[i], cudaEventDisableTiming));
+        }
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    TPMLP_CUDA(c, cudaMemcpyAsync(c->Xs, X_host, static_cast<size_t>(M) * c->H * 2,
-                                  cudaMemcpyHostToDevice, s));
-    if ((rc = tpmlp_forward(c, c->Xs, B, S, c->Zs, stream))) return rc;
-    TPMLP_CUDA(c, cudaMemcpyAsync(Z_host, c->Zs, static_cast<size_t>(M) * c->H * z_elem_bytes(c),
-                                  cudaMemcpyDeviceToHost, s));
+    // Row chunks: the copy of chunk c+1 in and of chunk c-1 out overlap chunk c's GEMMs.
+    // At least 2048 rows per chunk keeps the GEMMs' grids several waves deep.
+    const int chunks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kHostChunksMax, M / 2048)));
+    const int64_t rows = ((M + chunks - 1) / chunks + tpmlp::kBM - 1) / tpmlp::kBM * tpmlp::kBM;
+    const size_t xrow = static_cast<size_t>(c->H) * 2, zrow = static_cast<size_t>(c->H) * z_elem_bytes(c);
+    // nothing may touch the staging buffers before earlier work on `stream` is done
+    TPMLP_CUDA(c, cudaEventRecord(c->host_ev[0], s));
+    TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_in, c->host_ev[0], 0));
+    TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->host_ev[0], 0));
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r0 = i * rows, n = std::min(rows, M - r0);
+        if (n <= 0) break;
+        TPMLP_CUDA(c, cudaMemcpyAsync(static_cast<char*>(c->Xs) + r0 * xrow,
+                                      static_cast<const char*>(X_host) + r0 * xrow, n * xrow,
+                                      cudaMemcpyHostToDevice, c->s_in));
+        TPMLP_CUDA(c, cudaEventRecord(c->in_ev[i], c->s_in));
+    }
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r0 = i * rows, n = std::min(rows, M - r0);
+        if (n <= 0) break;
+        TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->in_ev[i], 0));
+        const void* xi = static_cast<const char*>(c->Xs) + r0 * xrow;
+        void* zi = static_cast<char*>(c->Zs) + r0 * zrow;
+        if ((rc = run_gemm1(c, xi, n, c->Y, s)) || (rc = run_gemm2(c, c->Y, n, zi, s))) return rc;
+        TPMLP_CUDA(c, cudaEventRecord(c->out_ev[i], s));
+        TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->out_ev[i], 0));
+        TPMLP_CUDA(c, cudaMemcpyAsync(static_cast<char*>(Z_host) + r0 * zrow, zi, n * zrow,
+                                      cudaMemcpyDeviceToHost, c->s_out));
+    }
+    TPMLP_CUDA(c, cudaEventRecord(c->host_ev[1], c->s_out));
+    TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->host_ev[1], 0));
     TPMLP_CUDA(c, cudaStreamSynchronize(s));
     return TPMLP_OK;
 }
@@ -995,6 +1037,11 @@ void tpmlp_destroy(tpmlp_ctx* c) {
     cudaFree(c->Y);
     cudaFree(c->Xs);
     cudaFree(c->Zs);
+    for (cudaEvent_t e : c->host_ev) if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : c->in_ev) if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : c->out_ev) if (e) cudaEventDestroy(e);
+    if (c->s_in) cudaStreamDestroy(c->s_in);
+    if (c->s_out) cudaStreamDestroy(c->s_out);
     cudaFree(c->Xn);
     cudaFree(c->zeros);
     cudaFree(c->colsum);
