@@ -215,10 +215,10 @@ int max_resident_pairs(tpmlp_ctx* c, Kernel kern, uint32_t smem) {
     return n;
 }
 
-template <int STAGES, int NUM_ACC, Mode MODE, bool F32>
+template <int STAGES, int NUM_ACC, Mode MODE, bool F32, bool MN = false>
 int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                 cudaStream_t s) {
-    auto kern = tpmlp::tpmlp_gemm_pair_kernel<STAGES, NUM_ACC, MODE, F32>;
+    auto kern = tpmlp::tpmlp_gemm_pair_kernel<STAGES, NUM_ACC, MODE, F32, MN>;
     constexpr uint32_t smem = tpmlp::PairSmem<STAGES, NUM_ACC>::kTotal;
     static_assert(smem <= 232448, "shared memory per CTA");
     static std::atomic<uint64_t> attr_done{0};
@@ -481,6 +481,7 @@ int run_weight_grad(tpmlp_ctx* c, const void* Aop, int64_t R, const void* Bop, i
     int rc = token_major_map(c, &ta, Aop, tokens, R);
     if (rc || (rc = token_major_map(c, &tb, Bop, tokens, C))) return rc;
     const int bn = pick_bn(C);
+    const bool pair = bn == 256 && !(c->flags & TPMLP_FLAG_SINGLE_SM);
     GemmArgs a{};
     a.M = static_cast<int>(R);
     a.ldo = static_cast<int>(C);
@@ -488,12 +489,16 @@ int run_weight_grad(tpmlp_ctx* c, const void* Aop, int64_t R, const void* Bop, i
     a.k = 1;
     a.kb_tile = static_cast<int>((tokens + tpmlp::kBK - 1) / tpmlp::kBK);
     a.kb_shard = a.kb_tile;
-    a.m_blocks = static_cast<int>((R + tpmlp::kBM - 1) / tpmlp::kBM);
+    const int bm = pair ? tpmlp::kPairBM : tpmlp::kBM;
+    a.m_blocks = static_cast<int>((R + bm - 1) / bm);
     a.n_blocks = static_cast<int>(C / bn);
     a.num_tiles = a.m_blocks * a.n_blocks;
     a.group_m = 8;
     a.out = out;
     a.status = c->status;
+    if (pair)
+        return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kWeightGrad, true, true>(c, ta, tb,
+                                                                                             a, s);
     switch (bn) {
         case 256: return launch_gemm<256, TPMLP_STAGES_256, Mode::kWeightGrad, true, true>(c, ta, tb, a, s);
         case 128: return launch_gemm<128, 6, Mode::kWeightGrad, true, true>(c, ta, tb, a, s);

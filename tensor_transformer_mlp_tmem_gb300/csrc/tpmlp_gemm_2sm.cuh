@@ -39,12 +39,14 @@ struct PairSmem {
     static constexpr uint32_t kTmemCols = NUM_ACC * kPairBN;  // 256 or 512
 };
 
-template <int STAGES, int NUM_ACC, Mode MODE, bool OUT_F32>
+// MN: both operands M-/N-contiguous (the weight-gradient GEMMs): each CTA loads its 128 rows
+// of A and of B as two 64 (MN) x 64 (K) boxes each (see tpmlp_gemm_kernel).
+template <int STAGES, int NUM_ACC, Mode MODE, bool OUT_F32, bool MN = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     tpmlp_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
     using L = PairSmem<STAGES, NUM_ACC>;
-    constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, kPairBN);
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, kPairBN, MN);
     constexpr int kCode = (static_cast<int>(MODE) << 8) | 0x80;  // 0x80: pair kernel
 
     extern __shared__ uint8_t smem_raw[];
@@ -129,7 +131,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
 #endif
                     const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // rank 0's barrier
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
-                    if constexpr (is_gemm1(MODE)) {
+                    if constexpr (MN) {
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            ptx::tma_load_2d_pair(sa + b * 8192, &tmA, fb, m0 + 64 * b, kb * kBK);
+                            ptx::tma_load_2d_pair(sb + b * 8192, &tmB, fb, nb + 64 * b, kb * kBK);
+                        }
+                    } else if constexpr (is_gemm1(MODE)) {
                         ptx::tma_load_2d_pair(sa, &tmA, fb, kb * kBK, m0);
                         ptx::tma_load_3d_pair(sb, &tmB, fb, kb * kBK, nb_in_shard1, shard1);
                     } else {
@@ -181,11 +189,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t sa = base + stage * L::kStageBytes;
-                    const uint64_t da = sdesc_k128(sa);
-                    const uint64_t db = sdesc_k128(sa + L::kABytes);
+                    const uint64_t da = MN ? sdesc_mn128(sa) : sdesc_k128(sa);
+                    const uint64_t db = MN ? sdesc_mn128(sa + L::kABytes) : sdesc_k128(sa + L::kABytes);
+                    constexpr uint32_t kStep = MN ? 128u : 2u;  // 16 K: 32 B (K-major), 2 KB (MN)
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-                        ptx::mma_bf16_ss_pair(d_tmem, da + 2u * kk, db + 2u * kk, kIdesc,
+                        ptx::mma_bf16_ss_pair(d_tmem, da + kStep * kk, db + kStep * kk, kIdesc,
                                               (kb | kk) != 0 ? 1u : 0u);
                     ptx::mma_commit_pair(empty_bar(stage), 0x3);  // stage s free in both CTAs
                     if (++stage == STAGES) {
