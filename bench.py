@@ -5,7 +5,8 @@
 A step is one forward pass of the whole block -- the column-parallel GEMM with its fused
 bias + GeLU, then the row-parallel GEMM whose accumulator sums all k shards and adds b2 --
 over one batch of seeded synthetic input already resident in HBM. L2 is flushed (a
-256 MiB write) between timed steps, outside the timed events. The printed JSON line
+256 MiB write, then a read of it, so no dirty line is left) between timed steps, outside
+the timed events. The printed JSON line
 carries throughput (TFLOP/s of the two contractions, tokens/s), the roofline of the
 dominant kernel, an end-to-end figure through the host-buffer entry point, SM clocks
 sampled during the timed region, and the fp64 CPU oracle timed on a bounded sample of
@@ -44,6 +45,14 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+def l2_flush(buf):
+    """Evict L2 between timed steps: write a buffer larger than L2, then read it back, so the
+    next step starts on a cold L2 that holds no dirty lines (their write-back would otherwise
+    land inside the next timed kernel). Both run outside the timed events."""
+    buf.zero_()
+    buf.view(-1).view(dtype=__import__("torch").int64).sum()
+
+
 def step_flops(w: synth.Workload, variant: str) -> int:
     """FLOPs of one forward pass: 2*M*H*F per contraction (the gated block's first GEMM
     computes the gate and the up projection: twice that). LayerNorm and the residual add
@@ -71,7 +80,7 @@ def workload_config(w: synth.Workload, extra=None, variant: str = "gelu") -> dic
         "workload": desc, "variant": variant,
         "B": w.B, "S": w.S, "M": w.M, "H": w.H, "F": w.F, "k": w.k, "seed": w.seed,
         "flops_per_step": step_flops(w, variant),
-        "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+        "l2": "flushed between timed steps (256 MiB write then read, outside the timed events)",
     }
     if extra:
         cfg.update(extra)
@@ -326,7 +335,7 @@ def run_gpu(args, w: synth.Workload):
             ev[2].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        l2_flush(flush)
         step()
     torch.cuda.synchronize(dev)
     rc, detail = mlp.status()
@@ -343,7 +352,7 @@ def run_gpu(args, w: synth.Workload):
     clocks.mark_start()
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        l2_flush(flush)
         step(evs[i])
     torch.cuda.synchronize(dev)
     clocks.mark_stop()
@@ -496,7 +505,7 @@ def run_gpu_linear(args, w: synth.Workload):
     lin = tp.Linear(kind, K, N, w.k)
     lin.pack(to_dev(W), to_dev(b))
     for _ in range(args.warmup):
-        flush.zero_()
+        l2_flush(flush)
         tp.tpmlp_linear_forward(lin.ctx, Xd, M, out, stream)
     torch.cuda.synchronize(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
@@ -509,7 +518,7 @@ def run_gpu_linear(args, w: synth.Workload):
     torch.cuda.synchronize(dev)
     clocks.mark_start()
     for i in range(args.steps):
-        flush.zero_()
+        l2_flush(flush)
         evs[i][0].record(stream)
         tp.tpmlp_linear_forward(lin.ctx, Xd, M, out, stream)
         evs[i][1].record(stream)
@@ -538,7 +547,7 @@ def run_gpu_linear(args, w: synth.Workload):
                                f"k={w.k} head groups, seeded synthetic",
                    "variant": args.variant, "M": M, "K": K, "N": N, "k": w.k,
                    "flops_per_step": flops,
-                   "l2": "flushed between timed steps (256 MiB write, outside the timed events)"},
+                   "l2": "flushed between timed steps (256 MiB write then read, outside the timed events)"},
         "roofline": {"bound": "tensor", "kernel": f"{kind}-parallel linear", "achieved": value / world,
                      "peak": peak, "unit": "TFLOP/s", "frac": value / world / peak,
                      "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None},
@@ -604,7 +613,7 @@ def run_gpu_train(args, w: synth.Workload):
             ev[2].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        l2_flush(flush)
         step()
     torch.cuda.synchronize(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -617,7 +626,7 @@ def run_gpu_train(args, w: synth.Workload):
     torch.cuda.synchronize(dev)
     clocks.mark_start()
     for i in range(args.steps):
-        flush.zero_()
+        l2_flush(flush)
         step(evs[i])
     torch.cuda.synchronize(dev)
     clocks.mark_stop()

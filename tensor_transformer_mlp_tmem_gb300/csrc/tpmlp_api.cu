@@ -437,26 +437,38 @@ int ensure_xn(tpmlp_ctx* c, int64_t rows) {
     return TPMLP_OK;
 }
 
-template <int NC>
-void launch_layernorm_nc(const tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t s) {
-    tpmlp::layernorm_kernel<NC><<<static_cast<unsigned>(M), tpmlp::kNormThreads, 0, s>>>(
+template <int THREADS, int NC>
+void launch_layernorm(const tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t s) {
+    tpmlp::layernorm_kernel<THREADS, NC><<<static_cast<unsigned>(M), THREADS, 0, s>>>(
         static_cast<const uint16_t*>(X), c->ln_gamma, c->ln_beta, c->ln_eps,
         static_cast<uint16_t*>(Xn), static_cast<int>(c->H));
 }
 
+// CTA size by row length (measured: 64 / 128 / 256 threads best for H <= 4096 / 8192 / more);
+// NC = 16-byte chunks per thread, rounded up to an instantiated count.
 int run_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t s) {
-    const int chunks_per_thread =
-        static_cast<int>((c->H / 8 + tpmlp::kNormThreads - 1) / tpmlp::kNormThreads);
-    switch (chunks_per_thread) {
-        case 1: launch_layernorm_nc<1>(c, X, M, Xn, s); break;
-        case 2: launch_layernorm_nc<2>(c, X, M, Xn, s); break;
-        case 3: launch_layernorm_nc<3>(c, X, M, Xn, s); break;
-        case 4: launch_layernorm_nc<4>(c, X, M, Xn, s); break;
-        case 5: launch_layernorm_nc<5>(c, X, M, Xn, s); break;
-        case 6: launch_layernorm_nc<6>(c, X, M, Xn, s); break;
-        case 7: launch_layernorm_nc<7>(c, X, M, Xn, s); break;
-        case 8: launch_layernorm_nc<8>(c, X, M, Xn, s); break;
-        default: return TPMLP_ERR_UNSUPPORTED_SHAPE;  // H > 16384
+    const int64_t chunks = c->H / 8;
+    if (c->H <= 4096) {
+        switch ((chunks + 63) / 64) {
+            case 1: launch_layernorm<64, 1>(c, X, M, Xn, s); break;
+            case 2: launch_layernorm<64, 2>(c, X, M, Xn, s); break;
+            case 3: launch_layernorm<64, 3>(c, X, M, Xn, s); break;
+            case 4: launch_layernorm<64, 4>(c, X, M, Xn, s); break;
+            case 5: case 6: launch_layernorm<64, 6>(c, X, M, Xn, s); break;
+            default: launch_layernorm<64, 8>(c, X, M, Xn, s); break;
+        }
+    } else if (c->H <= 8192) {
+        switch ((chunks + 127) / 128) {
+            case 5: case 6: launch_layernorm<128, 6>(c, X, M, Xn, s); break;
+            default: launch_layernorm<128, 8>(c, X, M, Xn, s); break;
+        }
+    } else if (c->H <= tpmlp::kNormMaxH) {
+        switch ((chunks + 255) / 256) {
+            case 5: case 6: launch_layernorm<256, 6>(c, X, M, Xn, s); break;
+            default: launch_layernorm<256, 8>(c, X, M, Xn, s); break;
+        }
+    } else {
+        return TPMLP_ERR_UNSUPPORTED_SHAPE;
     }
     TPMLP_CUDA(c, cudaGetLastError());
     ++c->launches;
@@ -789,8 +801,7 @@ int tpmlp_set_layernorm(tpmlp_ctx* c, const void* gamma, const void* beta, float
     // the block's input, or a column-parallel layer's input (LayerNorm before Q/K/V)
     if (!c || !gamma || !beta || c->kind == kKindRow) return TPMLP_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || eps > 1.0f) return TPMLP_ERR_INVALID_ARG;  // also rejects NaN
-    if (c->H > static_cast<int64_t>(tpmlp::kNormThreads) * 8 * tpmlp::kNormMaxChunks)
-        return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (c->H > tpmlp::kNormMaxH) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if ((reinterpret_cast<uintptr_t>(gamma) | reinterpret_cast<uintptr_t>(beta)) & 1)
         return TPMLP_ERR_MISALIGNED;
     if (!c->ln_gamma) {
