@@ -126,35 +126,116 @@ struct GemmSmem {
     static constexpr uint32_t kBBytes = BN * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kCtrlBytes = 8 * (2 * STAGES + 5) + 8;
-    static constexpr uint32_t kTotal = 1024 /*alignment slack*/ + STAGES * kStageBytes + kCtrlBytes;
+    static constexpr uint32_t kEpiOffset = STAGES * kStageBytes + (kCtrlBytes + 127) / 128 * 128;
+    static constexpr uint32_t kTotal = 1024 /*alignment slack*/ + kEpiOffset + kEpiWarps * 2048;  // + epilogue staging
+    static_assert(kTotal <= 232448, "dynamic shared memory per CTA");
     static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; power of two >= 32
 };
 
-// GeLU, exact form a * Phi(a) = a/2 * (1 + erf(a / sqrt 2)), with CUDA's erff.
+// 2^x and 1/x on the special-function unit (PTX ex2.approx.ftz.f32: relative error near
+// 2^-22; rcp.approx.ftz.f32: within one ulp).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Standard normal lower tail Phi(-|a|) = erfc(|a| / sqrt 2) / 2 without a branch, in the form
+// erfc(z) = t exp(-z^2 + P(t)), t = 1 / (1 + z/2) (Press et al., Numerical Recipes in C,
+// 2nd ed., section 6.2), with a degree-7 P refitted to minimax relative error and carried to
+// base 2 with the factor 1/2 folded in (fit_phi.py writes the coefficients):
+//   Phi(-|a|) = t * 2^(P2(t) - a^2 log2(e) / 2).
+// Relative error below 1e-5 over the fp32 range, more than two orders of magnitude under a
+// bf16 step.
+__device__ __forceinline__ float normal_lower_tail(float a) {
+    const float t = rcp_approx(fmaf(fabsf(a), 0.35355339059327376f, 1.0f));
+    float p = -2.294616550e-01f;
+    p = fmaf(p, t, 9.304409623e-01f);
+    p = fmaf(p, t, -1.215087414e+00f);
+    p = fmaf(p, t, 3.299344182e-01f);
+    p = fmaf(p, t, 1.498845778e-02f);
+    p = fmaf(p, t, 5.527308583e-01f);
+    p = fmaf(p, t, 1.442202449e+00f);
+    p = fmaf(p, t, -2.825744629e+00f);
+    return t * ex2_approx(fmaf(a * a, -0.72134752044448170f, p));
+}
+
+// GeLU in its erf form, a * Phi(a) = a/2 * (1 + erf(a / sqrt 2)), Phi from the lower tail by
+// symmetry: Phi(a) = 1 - Phi(-a) for a >= 0.
 __device__ __forceinline__ float gelu_erf(float a) {
-    return 0.5f * a * (1.0f + erff(a * 0.70710678118654752440f));
+    const float q = normal_lower_tail(a);
+    return a * (a < 0.0f ? q : 1.0f - q);
 }
 
-// GeLU'(a) = Phi(a) + a phi(a), phi the standard normal density (CUDA's erff and expf).
+// GeLU'(a) = Phi(a) + a phi(a), phi(a) = 2^(-a^2 log2(e) / 2) / sqrt(2 pi) the normal density.
 __device__ __forceinline__ float gelu_grad(float a) {
-    return 0.5f * (1.0f + erff(a * 0.70710678118654752440f)) +
-           a * 0.39894228040143267794f * expf(-0.5f * a * a);
+    const float q = normal_lower_tail(a);
+    return (a < 0.0f ? q : 1.0f - q) +
+           a * 0.39894228040143267794f * ex2_approx(a * a * -0.72134752044448170f);
 }
 
-// SiLU(a) = a * sigma(a) = a / (1 + e^-a), with CUDA's expf.
-__device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
+// SiLU(a) = a * sigma(a) = a / (1 + e^-a) = a * 1 / (1 + 2^(-a log2 e)).
+__device__ __forceinline__ float silu(float a) {
+    return a * rcp_approx(1.0f + ex2_approx(a * -1.44269504088896341f));
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // round to nearest even
     return *reinterpret_cast<uint32_t*>(&p);
 }
 
-// One 32-column slice of one output row: + bias, (GeLU), (+ residual), convert, store.
+// Per-warp shared-memory staging for bf16 output slices (32 rows x 32 columns = 2 KB).
+constexpr uint32_t kStageSliceBytes = 32 * 64;
+
+// Store a warp's 32 rows x 32 bf16 columns (lane i holds row row0 + i as 16 packed words)
+// through the warp's 2 KB staging buffer, so that each global store writes eight whole
+// 64-byte row segments (four lanes per row) instead of 32 scattered 16-byte pieces. In the
+// buffer, 16-byte chunk c of row r sits at position c ^ ((r >> 1) & 3): both the row-wise
+// writes and the segment-wise reads touch 32 distinct banks per quarter warp.
+__device__ __forceinline__ void store_rows_coalesced(const uint32_t (&p)[16], uint32_t stage,
+                                                     __nv_bfloat16* out, int row0, int M, int ldo,
+                                                     int col) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t a = stage + lane * 64 + 16 * (c ^ ((lane >> 1) & 3));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(p[4 * c]),
+                     "r"(p[4 * c + 1]), "r"(p[4 * c + 2]), "r"(p[4 * c + 3])
+                     : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int r = 8 * j + (lane >> 2), c = lane & 3;
+        const uint32_t a = stage + r * 64 + 16 * (c ^ ((r >> 1) & 3));
+        uint4 v;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(a)
+                     : "memory");
+        if (row0 + r < M)
+            *reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + r) * ldo + col + 8 * c) = v;
+    }
+    __syncwarp();  // the buffer is free again
+}
+
+__device__ __forceinline__ void pack_slice(const float (&x)[32], uint32_t (&p)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+}
+
+// One 32-column slice of the warp's 32 output rows (this lane: `row`): + bias, (GeLU),
+// (+ residual), convert, store. All lanes of the warp call it together.
 template <Mode MODE, bool OUT_F32>
 __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const float* __restrict__ bias,
                                                void* out, int row, int M, int ldo, int col,
-                                               const void* residual = nullptr,
-                                               void* out2 = nullptr) {
+                                               const void* residual, void* out2, uint32_t stage) {
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
     float x[32];
     if constexpr (MODE == Mode::kBwdDA || MODE == Mode::kWeightGrad) {
 #pragma unroll
@@ -172,77 +253,72 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const fl
     }
     if constexpr (MODE == Mode::kGemm1Train) {
         // save the pre-activation for the backward pass, then apply GeLU
-        if (row < M) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out2) +
-                                                  static_cast<size_t>(row) * ldo + col);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                dst[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]),
-                                    pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
-                                    pack_bf16x2(x[8 * j + 4], x[8 * j + 5]),
-                                    pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
-        }
+        uint32_t p[16];
+        pack_slice(x, p);
+        store_rows_coalesced(p, stage, static_cast<__nv_bfloat16*>(out2), row0, M, ldo, col);
     }
     if constexpr (MODE == Mode::kGemm1 || MODE == Mode::kGemm1Train) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = gelu_erf(x[j]);
     }
-    if (row >= M) return;
     if constexpr (MODE == Mode::kBwdDA) {
         // dA = dY * GeLU'(A), A the saved (bf16) pre-activation
-        const uint4* a4 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(residual) +
-                                                         static_cast<size_t>(row) * ldo + col);
+        if (row < M) {
+            const uint4* a4 = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(residual) + static_cast<size_t>(row) * ldo + col);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 u = a4[j];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            for (int j = 0; j < 4; ++j) {
+                const uint4 u = a4[j];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                x[8 * j + 2 * i] *= gelu_grad(__uint_as_float(w[i] << 16));
-                x[8 * j + 2 * i + 1] *= gelu_grad(__uint_as_float(w[i] & 0xFFFF0000u));
+                for (int i = 0; i < 4; ++i) {
+                    x[8 * j + 2 * i] *= gelu_grad(__uint_as_float(w[i] << 16));
+                    x[8 * j + 2 * i + 1] *= gelu_grad(__uint_as_float(w[i] & 0xFFFF0000u));
+                }
             }
         }
     }
     if constexpr (MODE == Mode::kGemm2Residual) {
         // read before the store below: the output may be the residual buffer itself
-        const uint4* r4 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(residual) +
-                                                         static_cast<size_t>(row) * ldo + col);
+        if (row < M) {
+            const uint4* r4 = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(residual) + static_cast<size_t>(row) * ldo + col);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 u = r4[j];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            for (int j = 0; j < 4; ++j) {
+                const uint4 u = r4[j];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                x[8 * j + 2 * i] += __uint_as_float(w[i] << 16);
-                x[8 * j + 2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+                for (int i = 0; i < 4; ++i) {
+                    x[8 * j + 2 * i] += __uint_as_float(w[i] << 16);
+                    x[8 * j + 2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+                }
             }
         }
+        // every lane of the warp has read its residual row before any lane stores below
+        __syncwarp();
     }
     if constexpr (OUT_F32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) +
-                                                static_cast<size_t>(row) * ldo + col);
+        if (row < M) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) +
+                                                    static_cast<size_t>(row) * ldo + col);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+        }
     } else {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) +
-                                              static_cast<size_t>(row) * ldo + col);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]),
-                                pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
-                                pack_bf16x2(x[8 * j + 4], x[8 * j + 5]),
-                                pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+        uint32_t p[16];
+        pack_slice(x, p);
+        store_rows_coalesced(p, stage, static_cast<__nv_bfloat16*>(out), row0, M, ldo, col);
     }
 }
 
-// One 32-column slice of one output row of the gated first layer: the gate values g and the up
-// values u of the same 32 outputs; Y = SiLU(g + bias_g) * (u + bias_u), rounded to bf16.
+// One 32-column slice of the warp's 32 output rows of the gated first layer: the gate values g
+// and the up values u of the same 32 outputs; Y = SiLU(g + bias_g) * (u + bias_u), bf16.
 __device__ __forceinline__ void epilogue_gated_slice(const uint32_t (&g)[32], const uint32_t (&u)[32],
                                                      const float* __restrict__ bias_g,
                                                      const float* __restrict__ bias_u,
-                                                     void* __restrict__ out, int row, int M, int ldo,
-                                                     int col) {
+                                                     void* out, int row, int M, int ldo, int col,
+                                                     uint32_t stage) {
     float x[32];
     const float4* bg4 = reinterpret_cast<const float4*>(bias_g);
     const float4* bu4 = reinterpret_cast<const float4*>(bias_u);
@@ -255,13 +331,10 @@ __device__ __forceinline__ void epilogue_gated_slice(const uint32_t (&g)[32], co
         x[4 * j + 2] = silu(__uint_as_float(g[4 * j + 2]) + bg.z) * (__uint_as_float(u[4 * j + 2]) + bu.z);
         x[4 * j + 3] = silu(__uint_as_float(g[4 * j + 3]) + bg.w) * (__uint_as_float(u[4 * j + 3]) + bu.w);
     }
-    if (row >= M) return;
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) +
-                                          static_cast<size_t>(row) * ldo + col);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        dst[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
-                            pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+    uint32_t p[16];
+    pack_slice(x, p);
+    store_rows_coalesced(p, stage, static_cast<__nv_bfloat16*>(out),
+                         row - static_cast<int>(threadIdx.x & 31), M, ldo, col);
 }
 
 // Drain the accumulator columns [base, base + width) of this warp's 32 rows through the
@@ -272,7 +345,8 @@ __device__ __forceinline__ void epilogue_gated_slice(const uint32_t (&g)[32], co
 // `part` (0 .. kEpiParts-1) selects which share of the columns this warp drains.
 template <Mode MODE, bool OUT_F32, int WIDTH, typename Release>
 __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs& args, int row,
-                                                  int n0, int part, Release release) {
+                                                  int n0, int part, uint32_t stage,
+                                                  Release release) {
     if constexpr (MODE == Mode::kGemm1Gated) {
         constexpr int G = WIDTH / 2;
         constexpr int kCols = G / kEpiParts;
@@ -287,7 +361,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs
             ptx::tmem_wait_ld(u);
             if (c + 32 == c0 + kCols) release();
             epilogue_gated_slice(g, u, args.bias + n0 + c, args.bias + n0 + G + c, args.out, row,
-                                 args.M, args.ldo, n0 / 2 + c);
+                                 args.M, args.ldo, n0 / 2 + c, stage);
         }
     } else {
         constexpr int kCols = WIDTH / kEpiParts;
@@ -300,7 +374,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs
             ptx::tmem_wait_ld(v);
             if (c + 32 == c0 + kCols) release();
             epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo, n0 + c,
-                                          args.residual, args.out2);
+                                          args.residual, args.out2, stage);
         }
     }
 }
@@ -503,7 +577,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int row = m0 + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             const uint32_t empty = tempty_bar(acc);
-            drain_accumulator<MODE, OUT_F32, BN>(taddr, args, row, n0, part, [&] {
+            const uint32_t stage_buf = base + L::kEpiOffset + (warp - 2) * kStageSliceBytes;
+            drain_accumulator<MODE, OUT_F32, BN>(taddr, args, row, n0, part, stage_buf, [&] {
                 // all of this warp's accumulator columns are in registers: hand it back
                 ptx::tc_fence_before();
                 __syncwarp();

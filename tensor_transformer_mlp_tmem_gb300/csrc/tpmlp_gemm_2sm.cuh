@@ -35,7 +35,9 @@ struct PairSmem {
     static constexpr uint32_t kBBytes = 128 * kBK * 2;  // this CTA's 128 rows of B
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kCtrlBytes = 8 * (2 * STAGES + 2 * NUM_ACC + 1) + 8;
-    static constexpr uint32_t kTotal = 1024 + STAGES * kStageBytes + kCtrlBytes;
+    static constexpr uint32_t kEpiOffset = STAGES * kStageBytes + (kCtrlBytes + 127) / 128 * 128;
+    static constexpr uint32_t kTotal = 1024 + kEpiOffset + kEpiWarps * kStageSliceBytes;
+    static_assert(kTotal <= 232448, "dynamic shared memory per CTA");
     static constexpr uint32_t kTmemCols = NUM_ACC * kPairBN;  // 256 or 512
 };
 
@@ -231,7 +233,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kPairBN;
             const uint32_t empty = ptx::mapa_shared(tempty_bar(acc), 0);  // rank 0's barrier
-            drain_accumulator<MODE, OUT_F32, kPairBN>(taddr, args, row, n0, part, [&] {
+            const uint32_t stage_buf = base + L::kEpiOffset + (warp - 2) * kStageSliceBytes;
+            drain_accumulator<MODE, OUT_F32, kPairBN>(taddr, args, row, n0, part, stage_buf, [&] {
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive_cluster(empty);
