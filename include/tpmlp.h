@@ -59,9 +59,17 @@ typedef enum {
 /* Flags for tpmlp_create. */
 #define TPMLP_FLAG_Z_FP32 0x1u    /* Z is written as fp32 instead of bf16 */
 #define TPMLP_FLAG_SINGLE_SM 0x2u /* use only the single-SM kernel (128-row tiles), never the
-                                     CTA-pair kernel (256 x 256 tiles on two SMs); same results */
+                                     CTA-pair kernel (256 x 256 tiles on two SMs) */
 #define TPMLP_FLAG_SWIGLU 0x4u    /* gated block: Y_i = SiLU(X Wg_i + bg_i) * (X Wu_i + bu_i);
                                      weights come from tpmlp_pack_shards_swiglu */
+#define TPMLP_FLAG_FIXED_ORDER 0x8u /* never split an output tile's reduction across CTA pairs.
+                                     By default, when the last wave of 256 x 256 tiles would
+                                     leave CTA pairs idle, the reductions of the last tiles are
+                                     divided among all pairs and their fp32 partial sums added
+                                     in a fixed order: results are deterministic, but their
+                                     last bits then depend on the token count M. With this flag
+                                     every tile is summed in one pass in reduction order, so the
+                                     pair and single-SM kernels, and any M, give identical bits */
 
 /*
  * Create a context for one block shape on the current CUDA device.
@@ -72,9 +80,13 @@ typedef enum {
  *            parallel degree; shards are contiguous, equal column blocks of W1 and the
  *            matching row blocks of W2 -- AI大模型分布式训练 §2.1 splits W into
  *            [hidden, ffn/k] pieces)
- *   flags    0, or any of TPMLP_FLAG_Z_FP32, TPMLP_FLAG_SINGLE_SM, TPMLP_FLAG_SWIGLU
- * Allocates the packed-weight buffers (2*H*F bf16 + (F+H) fp32) and a device status word;
- * the intermediate activation buffer is allocated by tpmlp_reserve or the first forward.
+ *   flags    0, or any of TPMLP_FLAG_Z_FP32, TPMLP_FLAG_SINGLE_SM, TPMLP_FLAG_SWIGLU,
+ *            TPMLP_FLAG_FIXED_ORDER
+ * Allocates the packed-weight buffers (2*H*F bf16 + (F+H) fp32), a device status word and,
+ * unless TPMLP_FLAG_SINGLE_SM or TPMLP_FLAG_FIXED_ORDER is given, the split-reduction
+ * workspace (256 KB of fp32 partial sums and 64 bytes of flags per CTA pair: about 19 MB on
+ * 152 SMs); the intermediate activation buffer is allocated by tpmlp_reserve or the first
+ * forward.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ARCH (device is not sm_103), OOM, CUDA.
  */
 TPMLP_API int tpmlp_create(tpmlp_ctx **out, int64_t H, int64_t F, int32_t k, uint32_t flags);
@@ -296,7 +308,7 @@ TPMLP_API int tpmlp_forward_noalloc(tpmlp_ctx *ctx, const void *X, int64_t B, in
  *                        out = sum_i X_i W_i + b, the sum over shards taken in the second
  *                        GEMM's fp32 accumulator (the All-Reduce on chip), b added once
  * Shapes: K, N multiples of 64; the sharded dimension divisible by k into multiples of 64.
- * flags: 0, TPMLP_FLAG_Z_FP32 (fp32 output), TPMLP_FLAG_SINGLE_SM.
+ * flags: 0, TPMLP_FLAG_Z_FP32 (fp32 output), TPMLP_FLAG_SINGLE_SM, TPMLP_FLAG_FIXED_ORDER.
  * The context is used with tpmlp_linear_pack / tpmlp_linear_forward / tpmlp_destroy (and the
  * diagnostic calls); the MLP-block entry points reject it with TPMLP_ERR_INVALID_ARG.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ARCH, OOM, CUDA.

@@ -22,7 +22,7 @@ __all__ = [
     "tpmlp_strerror", "tpmlp_last_error", "tpmlp_launch_count",
     "TPMLP_OK", "TPMLP_ERR_INVALID_ARG", "TPMLP_ERR_UNSUPPORTED_SHAPE", "TPMLP_ERR_NOT_PACKED",
     "TPMLP_ERR_CUDA", "TPMLP_ERR_OOM", "TPMLP_ERR_DEVICE_TIMEOUT", "TPMLP_ERR_ARCH",
-    "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM", "TPMLP_FLAG_SWIGLU", "tpmlp_pack_shards_swiglu",
+    "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM", "TPMLP_FLAG_SWIGLU", "TPMLP_FLAG_FIXED_ORDER", "tpmlp_pack_shards_swiglu",
     "tpmlp_set_layernorm", "tpmlp_layernorm", "tpmlp_block_forward", "tpmlp_gemm2_residual",
     "tpmlp_linear_create", "tpmlp_linear_pack", "tpmlp_linear_forward", "Linear",
     "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW", "tpmlp_forward_train", "tpmlp_backward",
@@ -40,6 +40,7 @@ TPMLP_ERR_MISALIGNED = -8
 TPMLP_FLAG_Z_FP32 = 0x1
 TPMLP_FLAG_SINGLE_SM = 0x2
 TPMLP_FLAG_SWIGLU = 0x4
+TPMLP_FLAG_FIXED_ORDER = 0x8
 TPMLP_LINEAR_COLUMN = 0
 TPMLP_LINEAR_ROW = 1
 TPMLP_NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's fixed scratch for tpmlp_forward_noalloc
@@ -291,12 +292,13 @@ class TPMLP:
     """
 
     def __init__(self, H: int, F: int, k: int, z_fp32: bool = False, single_sm: bool = False,
-                 swiglu: bool = False):
+                 swiglu: bool = False, fixed_order: bool = False):
         self.H, self.F, self.k = H, F, k
         self.z_fp32 = z_fp32
         self.swiglu = swiglu
         flags = ((TPMLP_FLAG_Z_FP32 if z_fp32 else 0) | (TPMLP_FLAG_SINGLE_SM if single_sm else 0)
-                 | (TPMLP_FLAG_SWIGLU if swiglu else 0))
+                 | (TPMLP_FLAG_SWIGLU if swiglu else 0)
+                 | (TPMLP_FLAG_FIXED_ORDER if fixed_order else 0))
         self.ctx = tpmlp_create(H, F, k, flags)
 
     def close(self):
@@ -452,10 +454,11 @@ class Linear:
     """
 
     def __init__(self, kind: str, K: int, N: int, k: int, out_fp32: bool = False,
-                 single_sm: bool = False):
+                 single_sm: bool = False, fixed_order: bool = False):
         self.kind, self.K, self.N, self.k = kind, K, N, k
         self.out_fp32 = out_fp32
-        flags = (TPMLP_FLAG_Z_FP32 if out_fp32 else 0) | (TPMLP_FLAG_SINGLE_SM if single_sm else 0)
+        flags = ((TPMLP_FLAG_Z_FP32 if out_fp32 else 0) | (TPMLP_FLAG_SINGLE_SM if single_sm else 0)
+                 | (TPMLP_FLAG_FIXED_ORDER if fixed_order else 0))
         kid = {"column": TPMLP_LINEAR_COLUMN, "row": TPMLP_LINEAR_ROW}[kind]
         self.ctx = tpmlp_linear_create(kid, K, N, k, flags)
 

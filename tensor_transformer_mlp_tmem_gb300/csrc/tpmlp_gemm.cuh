@@ -65,7 +65,9 @@ __host__ __device__ constexpr bool is_gemm1(Mode m) {
 }
 
 // Wait sites recorded in the status word when a bounded wait gives up: (mode << 8) | site.
-enum : int { kSiteProducer = 1, kSiteMmaAccum = 2, kSiteMmaFull = 3, kSiteEpilogue = 4 };
+enum : int {
+    kSiteProducer = 1, kSiteMmaAccum = 2, kSiteMmaFull = 3, kSiteEpilogue = 4, kSiteSplitK = 5
+};
 
 struct GemmArgs {
     int M;          // valid output rows (token rows)
@@ -84,7 +86,122 @@ struct GemmArgs {
                            // kBwdDA: the saved pre-activation A [M][ldo] bf16
     void* out2;            // kGemm1Train: the pre-activation A [M][ldo] bf16
     int* status;        // device status word
+    // Split reduction of the last tiles (CTA-pair kernel only). Tiles [0, sk_first) are
+    // whole units handed out round robin; the sk_iters = (num_tiles - sk_first) * kb_tile
+    // reduction blocks of the remaining tiles are divided evenly among the pairs, in tile
+    // order. A pair whose share starts inside a tile writes its fp32 partial accumulator to
+    // its slot of sk_partial and stamps its flags with sk_epoch; the pair holding the tile's
+    // first block adds the partials of the later pairs and runs the epilogue.
+    int sk_first;          // == num_tiles: no split
+    int sk_iters;
+    float* sk_partial;     // [pairs][2 CTAs][256 columns][128 rows] fp32
+    uint32_t* sk_flags;    // [pairs][2 CTAs][epilogue warps]
+    uint32_t sk_epoch;     // nonzero, new for every launch that splits
 };
+
+constexpr int kSkSlotFloats = 128 * 256;  // one CTA's half of a 256 x 256 accumulator
+
+// The sequence of work units (tile, reduction blocks [kb0, kb1)) of one CTA pair: its whole
+// tiles first, then its share of the split region. Every role of the pair walks the same
+// sequence.
+struct WorkCursor {
+    int t;
+    long long it, it_end;
+};
+
+__device__ __forceinline__ WorkCursor work_begin(const GemmArgs& a, int pair, int num_pairs) {
+    WorkCursor c;
+    c.t = pair;
+    c.it = static_cast<long long>(a.sk_iters) * pair / num_pairs;
+    c.it_end = static_cast<long long>(a.sk_iters) * (pair + 1) / num_pairs;
+    return c;
+}
+
+__device__ __forceinline__ bool work_next(const GemmArgs& a, int num_pairs, WorkCursor& c,
+                                          int& tile, int& kb0, int& kb1) {
+    if (c.t < a.sk_first) {
+        tile = c.t;
+        kb0 = 0;
+        kb1 = a.kb_tile;
+        c.t += num_pairs;
+        return true;
+    }
+    if (c.it < c.it_end) {
+        const long long rel = c.it / a.kb_tile;
+        kb0 = static_cast<int>(c.it - rel * a.kb_tile);
+        kb1 = static_cast<int>(min(static_cast<long long>(a.kb_tile), kb0 + (c.it_end - c.it)));
+        tile = a.sk_first + static_cast<int>(rel);
+        c.it += kb1 - kb0;
+        return true;
+    }
+    return false;
+}
+
+// The pair whose share of the split region holds reduction block i (shares are
+// [floor(S p / P), floor(S (p + 1) / P))).
+__device__ __forceinline__ int work_pair_of(const GemmArgs& a, int num_pairs, long long i) {
+    const long long S = a.sk_iters;
+    return static_cast<int>(((i + 1) * num_pairs + S - 1) / S - 1);
+}
+
+// The accumulator columns one epilogue warp drains, 32 at a time: [c0, c0 + kCols) with
+// c0 = part * kCols, and in the gated layer also the same columns of the up half (+ G).
+template <Mode MODE, int WIDTH, typename Fn>
+__device__ __forceinline__ void for_each_warp_slice(int part, Fn&& fn) {
+    if constexpr (MODE == Mode::kGemm1Gated) {
+        constexpr int G = WIDTH / 2, kCols = G / kEpiParts;
+#pragma unroll 1
+        for (int c = part * kCols; c < (part + 1) * kCols; c += 32) {
+            fn(c);
+            fn(G + c);
+        }
+    } else {
+        constexpr int kCols = WIDTH / kEpiParts;
+#pragma unroll 1
+        for (int c = part * kCols; c < (part + 1) * kCols; c += 32) fn(c);
+    }
+}
+
+// Split units. A slot holds one CTA's 128 accumulator rows x 256 columns, column-major
+// (element (r, c) at c * 128 + r), so that a warp's 32 lanes write and read 128 contiguous
+// bytes per column.
+//
+// This warp's share of a partial accumulator -> the pair's slot; the accumulator is released
+// once it has been read.
+template <Mode MODE, int WIDTH, typename Release>
+__device__ __forceinline__ void save_partial(uint32_t taddr, int part, float* slot, int lrow,
+                                             Release release) {
+    for_each_warp_slice<MODE, WIDTH>(part, [&](int c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c, v);
+        ptx::tmem_wait_ld(v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            __stcg(slot + static_cast<size_t>(c + j) * 128 + lrow, __uint_as_float(v[j]));
+    });
+    release();
+}
+
+// Add the partials of n_in later pairs (slots `first`, first + 2 slots, ...; summed in that
+// order) into this warp's share of the accumulator in tensor memory.
+template <Mode MODE, int WIDTH>
+__device__ __forceinline__ void fold_partials(uint32_t taddr, int part, const float* first,
+                                              int n_in, int lrow) {
+    for_each_warp_slice<MODE, WIDTH>(part, [&](int c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c, v);
+        ptx::tmem_wait_ld(v);
+#pragma unroll 1
+        for (int p = 0; p < n_in; ++p) {
+            const float* slot = first + static_cast<size_t>(p) * 2 * kSkSlotFloats;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                v[j] = __float_as_uint(__uint_as_float(v[j]) +
+                                       __ldcg(slot + static_cast<size_t>(c + j) * 128 + lrow));
+        }
+        ptx::tmem_st_32x32b_x32_wait(taddr + c, v);
+    });
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile stored as rows of 64 bf16
 // (128 bytes) with the 128-byte swizzle, 8-row swizzle atoms 1024 bytes apart (the layout

@@ -104,7 +104,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
-            for (int t = pair; ok && t < args.num_tiles; t += num_pairs) {
+            WorkCursor cur = work_begin(args, pair, num_pairs);
+            int t, kb0, kb1;
+            while (ok && work_next(args, num_pairs, cur, t, kb0, kb1)) {
                 int m_blk, n_blk;
                 decode_tile(args, t, m_blk, n_blk);
                 const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;  // this CTA's A rows
@@ -112,7 +114,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 const int nb = n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
                 const int shard1 = is_gemm1(MODE) ? n0 / args.f : 0;
                 const int nb_in_shard1 = nb - shard1 * args.f;
-                for (int kb = 0; kb < args.kb_tile; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status,
                                         kCode | kSiteProducer)) {
                         ok = false;
@@ -175,7 +177,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         if (leader && lane == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = pair; ok && t < args.num_tiles; t += num_pairs) {
+            WorkCursor cur = work_begin(args, pair, num_pairs);
+            int t, kb0, kb1;
+            while (ok && work_next(args, num_pairs, cur, t, kb0, kb1)) {
                 if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status,
                                     kCode | kSiteMmaAccum)) {
                     ok = false;
@@ -183,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kPairBN;
-                for (int kb = 0; kb < args.kb_tile; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, args.status,
                                         kCode | kSiteMmaFull)) {
                         ok = false;
@@ -197,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk)
                         ptx::mma_bf16_ss_pair(d_tmem, da + kStep * kk, db + kStep * kk, kIdesc,
-                                              (kb | kk) != 0 ? 1u : 0u);
+                                              (kb != kb0 || kk != 0) ? 1u : 0u);
                     ptx::mma_commit_pair(empty_bar(stage), 0x3);  // stage s free in both CTAs
                     if (++stage == STAGES) {
                         stage = 0;
@@ -220,25 +224,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         const int q = warp & 3;
         const int part = (warp - 2) >> 2;
         uint32_t acc = 0, acc_phase = 0;
-        for (int t = pair; t < args.num_tiles; t += num_pairs) {
+        const int ew = warp - 2;  // epilogue warp index: its flag in a split unit
+        WorkCursor cur = work_begin(args, pair, num_pairs);
+        int t, kb0, kb1;
+        while (work_next(args, num_pairs, cur, t, kb0, kb1)) {
             int m_blk, n_blk;
             decode_tile(args, t, m_blk, n_blk);
             const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;
             const int n0 = n_blk * kPairBN;
-            bool ok = ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status,
-                                     kCode | kSiteEpilogue);
+            // split units: kb0 > 0 -> this pair's partial; kb1 < kb_tile -> add later pairs'
+            const int lrow = q * 32 + lane;
+            uint32_t* const my_flag =
+                args.sk_flags + (static_cast<size_t>(pair) * 2 + rank) * kEpiWarps + ew;
+            int n_in = 0;
+            bool ok = true;
+            if (kb0 == 0 && kb1 < args.kb_tile) {
+                const long long last =
+                    static_cast<long long>(t - args.sk_first + 1) * args.kb_tile - 1;
+                n_in = work_pair_of(args, num_pairs, last) - pair;
+                for (int p = 1; ok && p <= n_in; ++p)
+                    ok = ptx::flag_wait(my_flag + static_cast<size_t>(p) * 2 * kEpiWarps,
+                                        args.sk_epoch, abort_flag, args.status,
+                                        kCode | kSiteSplitK);
+            }
+            if (ok)
+                ok = ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status,
+                                    kCode | kSiteEpilogue);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const int row = m0 + q * 32 + lane;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kPairBN;
             const uint32_t empty = ptx::mapa_shared(tempty_bar(acc), 0);  // rank 0's barrier
-            const uint32_t stage_buf = base + L::kEpiOffset + (warp - 2) * kStageSliceBytes;
-            drain_accumulator<MODE, OUT_F32, kPairBN>(taddr, args, row, n0, part, stage_buf, [&] {
+            auto release = [&] {
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive_cluster(empty);
-            });
+            };
+            float* const slot =
+                args.sk_partial + (static_cast<size_t>(pair) * 2 + rank) * kSkSlotFloats;
+            if (kb0 > 0) {
+                save_partial<MODE, kPairBN>(taddr, part, slot, lrow, release);
+                __threadfence();  // the partial is in memory before the flag says so
+                __syncwarp();
+#ifndef TPMLP_TEST_SKIP_FLAG
+                if (lane == 0) ptx::st_release_gpu(my_flag, args.sk_epoch);
+#else
+                (void)my_flag;  // test builds only: the partial is never announced
+#endif
+            } else {
+                if (n_in > 0)
+                    fold_partials<MODE, kPairBN>(taddr, part, slot + 2 * kSkSlotFloats, n_in, lrow);
+                const uint32_t stage_buf = base + L::kEpiOffset + (warp - 2) * kStageSliceBytes;
+                drain_accumulator<MODE, OUT_F32, kPairBN>(taddr, args, row, n0, part, stage_buf,
+                                                          release);
+            }
             if (++acc == NUM_ACC) {
                 acc = 0;
                 acc_phase ^= 1u;

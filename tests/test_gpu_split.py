@@ -1,0 +1,109 @@
+"""The split reduction on CTA pairs.
+
+A launch of between one and two waves of 256 x 256 tiles, with at most 64 MB of operands and
+at least 16 reduction blocks per tile, divides all its reduction blocks evenly among the CTA
+pairs; a pair whose share starts inside a tile hands its fp32 partial accumulator to the pair
+holding the tile's first block, which adds it and runs the epilogue. Here the second GEMM has
+100 tiles (10 x 10, 32 blocks, 21 MB of operands) and the first 80 (10 x 8, 40 blocks,
+24 MB): both split on a GB300's 74 to 76 resident pairs.
+
+Checked: the oracle on sampled rows; agreement with TPMLP_FLAG_FIXED_ORDER (every tile in
+one pass) up to fp32 summation order and the bf16 roundings it moves; bitwise determinism
+from call to call; and, for the second GEMM with fp32 output on one Y, that the two
+schedules agree to fp32 accuracy but really differ (the split path ran)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import tensor_transformer_mlp_tmem_gb300 as tp
+from gpu_util import assert_close, inputs_on_device, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+H, F, K_SHARDS, M = 2560, 2048, 2, 2560
+
+
+@pytest.fixture(scope="module")
+def block():
+    d = synth.make_inputs(H, F, M, 211)
+    return d, inputs_on_device(d)
+
+
+def run(dd, **kw):
+    with tp.TPMLP(H, F, K_SHARDS, **kw) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        X = dd["X"].view(1, M, H)
+        Y = mlp.gemm1(dd["X"])
+        Z1 = mlp(X)
+        Z2 = mlp(X)
+        torch.cuda.synchronize()
+        rc, detail = mlp.status()
+        assert rc == tp.TPMLP_OK, f"device status {detail:#x}"
+    return Y, Z1.view(M, H), Z2.view(M, H)
+
+
+def test_split_matches_oracle_and_is_deterministic(lib, block):
+    d, dd = block
+    Y, Z1, Z2 = run(dd)
+    assert torch.equal(Z1, Z2)
+    rows = synth.sample_rows(M, 48)
+    ref = oracle.tpmlp(synth.make_inputs(H, F, M, 211, x_rows=rows)["X"], d["W1"], d["b1"],
+                       d["W2"], d["b2"], K_SHARDS, want_y=True)
+    assert_close(to_f64(Z1)[rows], ref["Z"], what="split Z")
+    assert_close(to_f64(Y)[rows], ref["Y"], what="split Y")
+
+
+def test_split_agrees_with_fixed_order(lib, block):
+    _, dd = block
+    Ys, Zs, _ = run(dd)
+    Yf, Zf, _ = run(dd, fixed_order=True)
+    # only the fp32 summation order differs: a few bf16 roundings flip by one step
+    assert_close(to_f64(Ys), to_f64(Yf), rel=2e-3, mx=1e-2, what="Y split vs fixed order")
+    assert_close(to_f64(Zs), to_f64(Zf), rel=2e-3, mx=1e-2, what="Z split vs fixed order")
+
+
+def test_split_path_runs_fp32_output(lib, block):
+    """The second GEMM alone on one Y, fp32 output: the two schedules differ only in the fp32
+    summation order of the split tiles (Y itself is held fixed, since bf16 Y from a split
+    first GEMM may differ by a rounding step in a few elements)."""
+    _, dd = block
+    Y, _, _ = run(dd, fixed_order=True)
+    outs = []
+    for fixed in (False, True):
+        with tp.TPMLP(H, F, K_SHARDS, z_fp32=True, fixed_order=fixed) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            outs.append(mlp.gemm2(Y))
+            torch.cuda.synchronize()
+            assert mlp.status()[0] == tp.TPMLP_OK
+    a, b = outs[0].double(), outs[1].double()
+    rel = (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item()
+    assert rel < 1e-5, rel
+    assert not torch.equal(outs[0], outs[1]), "no tile was split: the schedule did not change"
+
+
+def test_split_weight_gradients(lib):
+    """dW1 [H, F] and dW2 [F, H] have 4 x 24 = 96 tiles each with 16 reduction blocks (the
+    tokens): their reductions are split across pairs."""
+    Hb, Fb, kb, Mb = 1024, 6144, 8, 1024
+    d = synth.make_inputs(Hb, Fb, Mb, 221)
+    dZ = synth.normal_bf16(221, 60, (Mb, Hb), 1.0)
+    dd = inputs_on_device(d)
+    outs = {}
+    for fixed in (False, True):
+        with tp.TPMLP(Hb, Fb, kb, fixed_order=fixed) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            X = dd["X"].view(1, Mb, Hb)
+            _, Ys, As = mlp.forward_train(X)
+            g = mlp.backward(to_dev(dZ).view(1, Mb, Hb), X, Ys, As, dd["W1"], dd["W2"])
+            torch.cuda.synchronize()
+            rc, detail = mlp.status()
+            assert rc == tp.TPMLP_OK, f"device status {detail:#x}"
+            outs[fixed] = [to_f64(t) for t in g]
+    ref = oracle.backward(d["X"], d["W1"], d["b1"], d["W2"], dZ, kb)
+    for i, name in enumerate(("dX", "dW1", "db1", "dW2", "db2")):
+        got = outs[False][i].reshape(ref[name].shape)
+        assert_close(got, ref[name], what=f"split {name}")
+        assert_close(got, outs[True][i].reshape(ref[name].shape), rel=2e-3, mx=1e-2,
+                     what=f"{name} split vs fixed order")

@@ -13,9 +13,9 @@ from gpu_util import assert_close, bits_of, device_tensor, f64, inputs_on_device
 pytestmark = pytest.mark.gpu
 
 
-def run_swiglu(d, H, F, k, M, single_sm=False, want_y=False):
+def run_swiglu(d, H, F, k, M, single_sm=False, want_y=False, fixed_order=False):
     dd = inputs_on_device(d)
-    with tp.TPMLP(H, F, k, swiglu=True, single_sm=single_sm) as mlp:
+    with tp.TPMLP(H, F, k, swiglu=True, single_sm=single_sm, fixed_order=fixed_order) as mlp:
         mlp.pack_swiglu(dd["Wg"], dd["bg"], dd["Wu"], dd["bu"], dd["W2"], dd["b2"])
         Y = mlp.gemm1(dd["X"])
         Z = mlp.gemm2(Y)
@@ -63,11 +63,16 @@ def test_swiglu_matches_oracle(lib, H, F, k, M):
 def test_swiglu_activations_and_kernels_agree(lib, H, F, k, M):
     d = synth.make_swiglu_inputs(H, F, M, 121)
     y1, z1 = run_swiglu(d, H, F, k, M, single_sm=True, want_y=True)
-    y2, z2 = run_swiglu(d, H, F, k, M, single_sm=False, want_y=True)
+    y2, z2 = run_swiglu(d, H, F, k, M, single_sm=False, want_y=True, fixed_order=True)
     assert np.array_equal(y1, y2) and np.array_equal(z1, z2)
     ref = oracle.tpmlp_swiglu(d["X"], d["Wg"], d["bg"], d["Wu"], d["bu"], d["W2"], d["b2"], k,
                               want_y=True)
     assert_close(f64(y2), ref["Y"], what="swiglu Y")
+    # default schedule: at (1024, 4096, 8, 1000) the gated first GEMM has 4 x 32 pair tiles,
+    # so the last tiles' reductions are split across pairs
+    y3, z3 = run_swiglu(d, H, F, k, M, single_sm=False, want_y=True)
+    assert_close(f64(y3), ref["Y"], what="swiglu Y, default schedule")
+    assert_close(f64(z3), ref["Z"], what="swiglu Z, default schedule")
 
 
 def test_swiglu_7b_shape_sampled_rows(lib):
