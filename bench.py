@@ -443,7 +443,8 @@ def run_gpu(args, w: synth.Workload):
                 "h2d_bytes_per_step": w.M * w.H * 2, "d2h_bytes_per_step": w.M * w.H * 2,
                 "ms_per_step": e2e_s * 1e3,
                 "api": ("pinned host X -> tpmlp_block_forward -> pinned host Z" if variant == "block"
-                        else "tpmlp_forward_host (pinned host X, Z)")},
+                        else "tpmlp_forward_host (pinned host X, Z; planned row chunks, "
+                             "copies overlapped with the GEMMs)")},
         "gpu_launches": launches,
         "clocks": clk,
     }

@@ -145,12 +145,14 @@ TPMLP_API int tpmlp_reserve(tpmlp_ctx *ctx, int64_t max_tokens);
 TPMLP_API int tpmlp_forward(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z, void *stream);
 
 /*
- * tpmlp_forward on host buffers: copies X (host, [B,S,H] bf16) to a device staging buffer,
- * runs the forward pass and copies Z back to host memory, then waits for `stream`. Token rows
- * are independent, so the work is split into up to 4 row chunks of at least 2048 rows: the
- * copies in and out run on two streams of the context and overlap the GEMMs of the other
- * chunks (which run on `stream`, after the work already queued there). Page-locked host
- * memory gives asynchronous, full-speed copies; pageable memory works but is slower.
+ * tpmlp_forward on host buffers: X (host, [B,S,H] bf16) in, Z (host, [B,S,H]) out; returns
+ * once Z is in host memory (it waits for `stream`). Token rows are independent, so the work
+ * streams in up to 4 row chunks: the copies of X chunks into a device staging buffer and of Z
+ * chunks out of one run on two copy streams of the context and overlap the GEMMs of the other
+ * chunks, which run on `stream` after the work already queued there. The chunk sizes are
+ * planned once per token count under a pipeline model of the copies and of the GEMMs' rounds
+ * of tiles (small end chunks, tile counts that fill whole rounds). Page-locked host memory
+ * gives asynchronous, full-speed copies; pageable memory works but is slower.
  * Staging buffers are owned by the context and grow on demand.
  * Errors: as tpmlp_forward.
  */

@@ -27,8 +27,8 @@ def sources():
 
 
 def _inputs():
-    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(INCLUDE, "tpmlp.h"),
-                                                               __file__]
+    return (sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
+            + [os.path.join(INCLUDE, "tpmlp.h"), __file__])
 
 
 def stale() -> bool:

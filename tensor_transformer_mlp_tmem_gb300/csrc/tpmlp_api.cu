@@ -19,6 +19,7 @@
 #include "tpmlp_norm.cuh"
 #include "tpmlp_reduce.cuh"
 #include "tpmlp_pack.cuh"
+#include "tpmlp_plan.h"
 
 struct tpmlp_ctx {
     int device = -1;
@@ -47,6 +48,10 @@ struct tpmlp_ctx {
     int64_t stage_rows = 0;
     cudaStream_t s_in = nullptr, s_out = nullptr;  // its copy streams (created on first use)
     cudaEvent_t host_ev[5] = {}, in_ev[4] = {}, out_ev[4] = {};
+    // row chunks of the last tpmlp_forward_host call (re-planned when M changes)
+    int64_t plan_M = -1;
+    int plan_n = 0;
+    int64_t plan_rows[4] = {};
 
     // activation tensor maps of the last call (re-encoded only when pointer or rows change)
     const void* x_map_ptr = nullptr;
@@ -420,6 +425,35 @@ int check_tokens(int64_t B, int64_t S) {
 }
 
 int z_elem_bytes(const tpmlp_ctx* c) { return (c->flags & TPMLP_FLAG_Z_FP32) ? 4 : 2; }
+
+// Copy-engine bandwidth of page-locked host memory on GB300 (NVLink-C2C), measured with
+// 16-128 MB copies: about 168 GB/s per direction with copies in and out at once (205 GB/s in
+// alone). The chunk planner only needs its ratio to the GEMMs' round times.
+constexpr double kCopyBothBps = 168e9;
+// Sustained dense bf16 rate of the GPU under the power cap (for the round times).
+constexpr double kGemmFlops = 1.7e15;
+
+// Row chunks of tpmlp_forward_host for M tokens (tpmlp_plan.h).
+int plan_host_chunks(const tpmlp_ctx* c, int64_t M, int64_t* rows) {
+    tpmlp::ChunkModel m{};
+    const int64_t pairs = c->num_sms / 2;
+    const int64_t F1 = c->gated ? 2 * c->F : c->F;  // first GEMM's output columns (packed)
+    const int64_t K[2] = {c->H, c->F}, N[2] = {F1, c->H};
+    const bool pair[2] = {c->pair1, c->pair2};
+    const int64_t bn[2] = {c->bn1, c->bn2};
+    for (int i = 0; i < 2; ++i) {
+        tpmlp::ChunkGemm& g = m.g[i];
+        g.tile_rows = pair[i] ? tpmlp::kPairBM : tpmlp::kBM;
+        const int64_t w = pair[i] ? tpmlp::kPairBN : bn[i];
+        g.col_tiles = N[i] / w;
+        g.slots = pair[i] ? pairs : c->num_sms;
+        g.tile_s = 2.0 * g.tile_rows * w * K[i] / (kGemmFlops / g.slots);
+    }
+    m.x_row_bytes = 2.0 * c->H;
+    m.z_row_bytes = static_cast<double>(c->H) * z_elem_bytes(c);
+    m.copy_Bps = kCopyBothBps;
+    return tpmlp::plan_chunks(m, M, kHostChunksMax, 64, rows);
+}
 
 // W2 [F][H] = k blocks [f][H] -> W2p [k][H][f]; b2 -> fp32.
 int pack_second_layer(tpmlp_ctx* c, const void* W2, const void* b2, cudaStream_t s) {
@@ -816,27 +850,28 @@ int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, v
             TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->out_ev[i], cudaEventDisableTiming));
         }
     }
+    if (M != c->plan_M) {
+        c->plan_n = plan_host_chunks(c, M, c->plan_rows);
+        c->plan_M = M;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // Row chunks: the copy of chunk c+1 in and of chunk c-1 out overlap chunk c's GEMMs.
-    // At least 2048 rows per chunk keeps the GEMMs' grids several waves deep.
-    const int chunks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kHostChunksMax, M / 2048)));
-    const int64_t rows = ((M + chunks - 1) / chunks + tpmlp::kBM - 1) / tpmlp::kBM * tpmlp::kBM;
     const size_t xrow = static_cast<size_t>(c->H) * 2, zrow = static_cast<size_t>(c->H) * z_elem_bytes(c);
     // nothing may touch the staging buffers before earlier work on `stream` is done
     TPMLP_CUDA(c, cudaEventRecord(c->host_ev[0], s));
     TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_in, c->host_ev[0], 0));
     TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->host_ev[0], 0));
-    for (int i = 0; i < chunks; ++i) {
-        const int64_t r0 = i * rows, n = std::min(rows, M - r0);
-        if (n <= 0) break;
+    int64_t r0 = 0;
+    for (int i = 0; i < c->plan_n; ++i) {
+        const int64_t n = c->plan_rows[i];
         TPMLP_CUDA(c, cudaMemcpyAsync(static_cast<char*>(c->Xs) + r0 * xrow,
                                       static_cast<const char*>(X_host) + r0 * xrow, n * xrow,
                                       cudaMemcpyHostToDevice, c->s_in));
         TPMLP_CUDA(c, cudaEventRecord(c->in_ev[i], c->s_in));
+        r0 += n;
     }
-    for (int i = 0; i < chunks; ++i) {
-        const int64_t r0 = i * rows, n = std::min(rows, M - r0);
-        if (n <= 0) break;
+    r0 = 0;
+    for (int i = 0; i < c->plan_n; ++i) {
+        const int64_t n = c->plan_rows[i];
         TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->in_ev[i], 0));
         const void* xi = static_cast<const char*>(c->Xs) + r0 * xrow;
         void* zi = static_cast<char*>(c->Zs) + r0 * zrow;
@@ -845,6 +880,7 @@ int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, v
         TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->out_ev[i], 0));
         TPMLP_CUDA(c, cudaMemcpyAsync(static_cast<char*>(Z_host) + r0 * zrow, zi, n * zrow,
                                       cudaMemcpyDeviceToHost, c->s_out));
+        r0 += n;
     }
     TPMLP_CUDA(c, cudaEventRecord(c->host_ev[1], c->s_out));
     TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->host_ev[1], 0));

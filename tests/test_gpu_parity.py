@@ -253,18 +253,22 @@ def test_single_sm_kernel_on_a_large_workload(lib):
     assert_close(to_f64(Z.view(w.M, w.H))[sel], ref, what="7b single-SM")
 
 
+@pytest.mark.parametrize("pinned_z", [True, False], ids=["Z-pinned", "Z-pageable"])
 @pytest.mark.parametrize("M", [4096, 8192 + 300])
-def test_forward_host_pipelined_chunks(lib, M):
-    """Large token counts go through the chunked copy/compute pipeline (up to 4 row
-    chunks on separate copy streams). With TPMLP_FLAG_FIXED_ORDER the result equals the
-    device-buffer forward bit for bit; by default the chunks' split plans differ from the
-    whole batch's, so the two agree up to fp32 summation order."""
+def test_forward_host_pipelined_chunks(lib, M, pinned_z):
+    """Large token counts go through the planned chunks of the copy/compute pipeline (copies
+    in and out on the context's copy streams, page-locked or pageable host memory). With
+    TPMLP_FLAG_FIXED_ORDER the result equals the device-buffer forward bit for bit; by default
+    the chunks' split plans may differ from the whole batch's, so the two agree up to fp32
+    summation order."""
     H, F, k = 512, 2048, 4
     d = synth.make_inputs(H, F, M, 201)
     dd = inputs_on_device(d)
     Xh = torch.from_numpy(d["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
     for fixed in (True, False):
-        Zh = torch.full((M, H), float("nan"), dtype=torch.bfloat16).pin_memory()
+        Zh = torch.full((M, H), float("nan"), dtype=torch.bfloat16)
+        if pinned_z:
+            Zh = Zh.pin_memory()
         with tp.TPMLP(H, F, k, fixed_order=fixed) as mlp:
             mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
             Zd = mlp(dd["X"].view(1, M, H))
