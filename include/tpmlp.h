@@ -218,6 +218,18 @@ TPMLP_API int tpmlp_block_forward(tpmlp_ctx *ctx, const void *X, int64_t B, int6
                                   void *stream);
 
 /*
+ * tpmlp_block_forward on host buffers: X (host, [B,S,H] bf16) in, Z = X + MLP(LayerNorm(X))
+ * (host, [B,S,H]) out; returns once Z is in host memory (it waits for `stream`). The same
+ * row-chunk pipeline as tpmlp_forward_host: per chunk the LayerNorm kernel, the first GEMM and
+ * the second GEMM with the residual add run on `stream` while the copies of the other chunks
+ * in and out run on the context's copy streams. Z_host may equal X_host (the residual stream
+ * updated in place). Requires tpmlp_set_layernorm.
+ * Errors: as tpmlp_block_forward.
+ */
+TPMLP_API int tpmlp_block_forward_host(tpmlp_ctx *ctx, const void *X_host, int64_t B, int64_t S,
+                                       void *Z_host, void *stream);
+
+/*
  * The second step with the residual add (the last launch of tpmlp_block_forward):
  *   Z[m, n] = R[m, n] + (b2[n] + sum_i sum_{j<f} Y[m, i f + j] W2[i f + j, n])
  *   Y device bf16 [M, F]; R device bf16 [M, H]; Z device [M, H] (bf16, or fp32 with

@@ -23,7 +23,8 @@ __all__ = [
     "TPMLP_OK", "TPMLP_ERR_INVALID_ARG", "TPMLP_ERR_UNSUPPORTED_SHAPE", "TPMLP_ERR_NOT_PACKED",
     "TPMLP_ERR_CUDA", "TPMLP_ERR_OOM", "TPMLP_ERR_DEVICE_TIMEOUT", "TPMLP_ERR_ARCH",
     "TPMLP_ERR_MISALIGNED", "TPMLP_FLAG_Z_FP32", "TPMLP_FLAG_SINGLE_SM", "TPMLP_FLAG_SWIGLU", "TPMLP_FLAG_FIXED_ORDER", "tpmlp_pack_shards_swiglu",
-    "tpmlp_set_layernorm", "tpmlp_layernorm", "tpmlp_block_forward", "tpmlp_gemm2_residual",
+    "tpmlp_set_layernorm", "tpmlp_layernorm", "tpmlp_block_forward", "tpmlp_block_forward_host",
+    "tpmlp_gemm2_residual",
     "tpmlp_linear_create", "tpmlp_linear_pack", "tpmlp_linear_forward", "Linear",
     "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW", "tpmlp_forward_train", "tpmlp_backward",
 ]
@@ -86,6 +87,7 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_set_layernorm": ([vp, vp, vp, ctypes.c_float, vp], ctypes.c_int),
         "tpmlp_layernorm": ([vp, vp, i64, vp, vp], ctypes.c_int),
         "tpmlp_block_forward": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_block_forward_host": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_gemm1": ([vp, vp, i64, vp, vp], ctypes.c_int),
         "tpmlp_gemm2": ([vp, vp, i64, vp, vp], ctypes.c_int),
         "tpmlp_gemm2_residual": ([vp, vp, i64, vp, vp, vp], ctypes.c_int),
@@ -201,6 +203,11 @@ def tpmlp_layernorm(ctx: int, X, M: int, Xn, stream=None) -> None:
 def tpmlp_block_forward(ctx: int, X, B: int, S: int, Z, stream=None) -> None:
     _check(load_library().tpmlp_block_forward(ctx, _ptr(X), B, S, _ptr(Z), _stream(stream)),
            "tpmlp_block_forward", ctx)
+
+
+def tpmlp_block_forward_host(ctx: int, X_host, B: int, S: int, Z_host, stream=None) -> None:
+    _check(load_library().tpmlp_block_forward_host(ctx, _ptr(X_host), B, S, _ptr(Z_host),
+                                                   _stream(stream)), "tpmlp_block_forward_host", ctx)
 
 
 def tpmlp_gemm1(ctx: int, X, M: int, Y, stream=None) -> None:

@@ -552,6 +552,89 @@ int run_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t
     return TPMLP_OK;
 }
 
+// The host-buffer pipeline of tpmlp_forward_host (layer = false) and
+// tpmlp_block_forward_host (layer = true: LayerNorm in front, the residual added by the second
+// GEMM's epilogue). The planned row chunks of X are copied into a device staging buffer on one
+// copy stream, each chunk's kernels run on `s` once its rows have arrived, and each chunk of Z
+// is copied out on a second copy stream as soon as its second GEMM is done.
+int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void* Z_host,
+                      cudaStream_t s, bool layer) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (layer && !c->ln_set) {
+        c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
+        return TPMLP_ERR_NOT_PACKED;
+    }
+    if ((rc = check_tokens(B, S))) return rc;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if (M > c->stage_rows) {
+        TPMLP_CUDA(c, cudaDeviceSynchronize());
+        if (c->Xs) cudaFree(c->Xs);
+        if (c->Zs) cudaFree(c->Zs);
+        c->Xs = c->Zs = nullptr;
+        c->stage_rows = 0;
+        TPMLP_CUDA(c, cudaMalloc(&c->Xs, static_cast<size_t>(M) * c->H * 2));
+        TPMLP_CUDA(c, cudaMalloc(&c->Zs, static_cast<size_t>(M) * c->H * z_elem_bytes(c)));
+        c->stage_rows = M;
+    }
+    if ((rc = ensure_y(c, M))) return rc;
+    if (layer && (rc = ensure_xn(c, M))) return rc;
+    if (!c->s_in) {
+        TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking));
+        TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking));
+        for (int i = 0; i < kHostChunksMax + 1; ++i)
+            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->host_ev[i], cudaEventDisableTiming));
+        for (int i = 0; i < kHostChunksMax; ++i) {
+            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->in_ev[i], cudaEventDisableTiming));
+            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->out_ev[i], cudaEventDisableTiming));
+        }
+    }
+    if (M != c->plan_M) {
+        c->plan_n = plan_host_chunks(c, M, c->plan_rows);
+        c->plan_M = M;
+    }
+    const size_t xrow = static_cast<size_t>(c->H) * 2, zrow = static_cast<size_t>(c->H) * z_elem_bytes(c);
+    // nothing may touch the staging buffers before earlier work on `s` is done
+    TPMLP_CUDA(c, cudaEventRecord(c->host_ev[0], s));
+    TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_in, c->host_ev[0], 0));
+    TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->host_ev[0], 0));
+    int64_t r0 = 0;
+    for (int i = 0; i < c->plan_n; ++i) {
+        const int64_t n = c->plan_rows[i];
+        TPMLP_CUDA(c, cudaMemcpyAsync(static_cast<char*>(c->Xs) + r0 * xrow,
+                                      static_cast<const char*>(X_host) + r0 * xrow, n * xrow,
+                                      cudaMemcpyHostToDevice, c->s_in));
+        TPMLP_CUDA(c, cudaEventRecord(c->in_ev[i], c->s_in));
+        r0 += n;
+    }
+    r0 = 0;
+    for (int i = 0; i < c->plan_n; ++i) {
+        const int64_t n = c->plan_rows[i];
+        TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->in_ev[i], 0));
+        const void* xi = static_cast<const char*>(c->Xs) + r0 * xrow;
+        void* zi = static_cast<char*>(c->Zs) + r0 * zrow;
+        if (layer) {
+            if ((rc = run_layernorm(c, xi, n, c->Xn, s)) || (rc = run_gemm1(c, c->Xn, n, c->Y, s)) ||
+                (rc = run_gemm2(c, c->Y, n, zi, s, xi)))
+                return rc;
+        } else if ((rc = run_gemm1(c, xi, n, c->Y, s)) || (rc = run_gemm2(c, c->Y, n, zi, s))) {
+            return rc;
+        }
+        TPMLP_CUDA(c, cudaEventRecord(c->out_ev[i], s));
+        TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->out_ev[i], 0));
+        TPMLP_CUDA(c, cudaMemcpyAsync(static_cast<char*>(Z_host) + r0 * zrow, zi, n * zrow,
+                                      cudaMemcpyDeviceToHost, c->s_out));
+        r0 += n;
+    }
+    TPMLP_CUDA(c, cudaEventRecord(c->host_ev[1], c->s_out));
+    TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->host_ev[1], 0));
+    TPMLP_CUDA(c, cudaStreamSynchronize(s));
+    return TPMLP_OK;
+}
+
 int create_context(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flags, int kind);
 
 // bf16 [rows][cols] map with a 64 x 64 box: an M-contiguous operand of a weight-gradient GEMM
@@ -822,70 +905,7 @@ int tpmlp_forward(tpmlp_ctx* c, const void* X, int64_t B, int64_t S, void* Z, vo
 
 int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void* Z_host,
                        void* stream) {
-    int rc = check_ctx(c);
-    if (rc) return rc;
-    if ((rc = check_tokens(B, S))) return rc;
-    const int64_t M = B * S;
-    if (M == 0) return TPMLP_OK;
-    if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
-    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
-    if (M > c->stage_rows) {
-        TPMLP_CUDA(c, cudaDeviceSynchronize());
-        if (c->Xs) cudaFree(c->Xs);
-        if (c->Zs) cudaFree(c->Zs);
-        c->Xs = c->Zs = nullptr;
-        c->stage_rows = 0;
-        TPMLP_CUDA(c, cudaMalloc(&c->Xs, static_cast<size_t>(M) * c->H * 2));
-        TPMLP_CUDA(c, cudaMalloc(&c->Zs, static_cast<size_t>(M) * c->H * z_elem_bytes(c)));
-        c->stage_rows = M;
-    }
-    if ((rc = ensure_y(c, M))) return rc;
-    if (!c->s_in) {
-        TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking));
-        TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking));
-        for (int i = 0; i < kHostChunksMax + 1; ++i)
-            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->host_ev[i], cudaEventDisableTiming));
-        for (int i = 0; i < kHostChunksMax; ++i) {
-            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->in_ev[i], cudaEventDisableTiming));
-            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->out_ev[i], cudaEventDisableTiming));
-        }
-    }
-    if (M != c->plan_M) {
-        c->plan_n = plan_host_chunks(c, M, c->plan_rows);
-        c->plan_M = M;
-    }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t xrow = static_cast<size_t>(c->H) * 2, zrow = static_cast<size_t>(c->H) * z_elem_bytes(c);
-    // nothing may touch the staging buffers before earlier work on `stream` is done
-    TPMLP_CUDA(c, cudaEventRecord(c->host_ev[0], s));
-    TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_in, c->host_ev[0], 0));
-    TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->host_ev[0], 0));
-    int64_t r0 = 0;
-    for (int i = 0; i < c->plan_n; ++i) {
-        const int64_t n = c->plan_rows[i];
-        TPMLP_CUDA(c, cudaMemcpyAsync(static_cast<char*>(c->Xs) + r0 * xrow,
-                                      static_cast<const char*>(X_host) + r0 * xrow, n * xrow,
-                                      cudaMemcpyHostToDevice, c->s_in));
-        TPMLP_CUDA(c, cudaEventRecord(c->in_ev[i], c->s_in));
-        r0 += n;
-    }
-    r0 = 0;
-    for (int i = 0; i < c->plan_n; ++i) {
-        const int64_t n = c->plan_rows[i];
-        TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->in_ev[i], 0));
-        const void* xi = static_cast<const char*>(c->Xs) + r0 * xrow;
-        void* zi = static_cast<char*>(c->Zs) + r0 * zrow;
-        if ((rc = run_gemm1(c, xi, n, c->Y, s)) || (rc = run_gemm2(c, c->Y, n, zi, s))) return rc;
-        TPMLP_CUDA(c, cudaEventRecord(c->out_ev[i], s));
-        TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->out_ev[i], 0));
-        TPMLP_CUDA(c, cudaMemcpyAsync(static_cast<char*>(Z_host) + r0 * zrow, zi, n * zrow,
-                                      cudaMemcpyDeviceToHost, c->s_out));
-        r0 += n;
-    }
-    TPMLP_CUDA(c, cudaEventRecord(c->host_ev[1], c->s_out));
-    TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->host_ev[1], 0));
-    TPMLP_CUDA(c, cudaStreamSynchronize(s));
-    return TPMLP_OK;
+    return run_host_pipeline(c, X_host, B, S, Z_host, static_cast<cudaStream_t>(stream), false);
 }
 
 int tpmlp_set_layernorm(tpmlp_ctx* c, const void* gamma, const void* beta, float eps,
@@ -946,6 +966,11 @@ int tpmlp_block_forward(tpmlp_ctx* c, const void* X, int64_t B, int64_t S, void*
     if ((rc = run_layernorm(c, X, M, c->Xn, s))) return rc;
     if ((rc = run_gemm1(c, c->Xn, M, c->Y, s))) return rc;
     return run_gemm2(c, c->Y, M, Z, s, X);  // epilogue: Z = X + (Y W2 + b2)
+}
+
+int tpmlp_block_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S,
+                             void* Z_host, void* stream) {
+    return run_host_pipeline(c, X_host, B, S, Z_host, static_cast<cudaStream_t>(stream), true);
 }
 
 int tpmlp_gemm2_residual(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, const void* R,

@@ -90,3 +90,37 @@ def test_block_requires_layernorm_parameters(lib):
         with pytest.raises(tp.TpmlpError) as e:
             tp.tpmlp_set_layernorm(mlp.ctx, to_dev(g), to_dev(b), -1.0)
         assert e.value.status == tp.TPMLP_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M", [300, 8192 + 40])
+def test_block_forward_host_equals_device_and_in_place(lib, M):
+    """The layer on host buffers runs the planned row chunks (LayerNorm, both GEMMs and the
+    residual per chunk). With TPMLP_FLAG_FIXED_ORDER it equals the device-buffer layer bit for
+    bit, also when Z_host is X_host (in place); by default it matches the oracle."""
+    H, F, k = 512, 2048, 4
+    d = synth.make_inputs(H, F, M, 231)
+    g, b = ln_params(H)
+    dd = inputs_on_device(d)
+    Xh = torch.from_numpy(d["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    for fixed in (True, False):
+        Zh = torch.full((M, H), float("nan"), dtype=torch.bfloat16).pin_memory()
+        with tp.TPMLP(H, F, k, fixed_order=fixed) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            mlp.set_layernorm(to_dev(g), to_dev(b), 1e-5)
+            with pytest.raises(tp.TpmlpError):  # B * S must be the rows of X
+                tp.tpmlp_block_forward_host(mlp.ctx, Xh, -1, M, Zh)
+            Zd = mlp.block(dd["X"].view(1, M, H))
+            torch.cuda.synchronize()
+            tp.tpmlp_block_forward_host(mlp.ctx, Xh, 1, M, Zh)
+            Xi = Xh.clone().pin_memory()
+            tp.tpmlp_block_forward_host(mlp.ctx, Xi, 1, M, Xi)  # residual stream in place
+            assert mlp.status()[0] == tp.TPMLP_OK
+        if fixed:
+            assert torch.equal(Zd.view(M, H).cpu(), Zh)
+            assert torch.equal(Xi, Zh)
+        else:
+            sel = synth.sample_rows(M, 24)
+            ref = oracle.block(d["X"], g, b, 1e-5, d["W1"], d["b1"], d["W2"], d["b2"], k,
+                               rows=sel)["Z"]
+            assert_close(to_f64(Zh)[sel], ref, what="host-buffer layer")
+            assert torch.equal(Xi, Zh)
