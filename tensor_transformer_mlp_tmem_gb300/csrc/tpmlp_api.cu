@@ -246,14 +246,13 @@ constexpr double kSplitMaxOperandBytes = 64.0 * (1 << 20);
 void plan_split(tpmlp_ctx* c, GemmArgs& a, int pairs) {
     a.sk_first = a.num_tiles;
     a.sk_iters = 0;
-    if (!c->sk_partial || pairs <= 0 || pairs > c->num_sms / 2) return;
-    const int waves = a.num_tiles / pairs, rem = a.num_tiles % pairs;
-    if (waves != 1 || rem == 0 || rem * 100 > pairs * TPMLP_SPLIT_TAIL_PCT) return;
-    const double operand_bytes = static_cast<double>(a.m_blocks + a.n_blocks) * tpmlp::kPairBM *
-                                 a.kb_tile * tpmlp::kBK * 2.0;
-    if (a.kb_tile < kSplitMinBlocks || operand_bytes > kSplitMaxOperandBytes) return;
-    a.sk_first = 0;
-    a.sk_iters = (a.num_tiles - a.sk_first) * a.kb_tile;
+    if (!c->sk_partial || pairs > c->num_sms / 2) return;
+    const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(
+        a.num_tiles, pairs, a.kb_tile, a.m_blocks, a.n_blocks, tpmlp::kPairBM,
+        TPMLP_SPLIT_TAIL_PCT, kSplitMinBlocks, kSplitMaxOperandBytes);
+    if (p.sk_first == a.num_tiles) return;
+    a.sk_first = p.sk_first;
+    a.sk_iters = p.sk_iters;
     a.sk_partial = c->sk_partial;
     a.sk_flags = c->sk_flags;
     if (++c->sk_epoch == 0) c->sk_epoch = 1;  // flags start at 0: never reuse it
@@ -268,8 +267,13 @@ int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
     static_assert(smem <= 232448, "shared memory per CTA");
     static std::atomic<uint64_t> attr_done{0};
     if (int rc = ensure_smem_attr(c, kern, smem, attr_done)) return rc;
-    static int resident = 0;  // same for every GB300; looked up on first use
-    if (resident <= 0) resident = max_resident_pairs(c, kern, smem);
+    static std::atomic<int> resident_on[64];  // per device, looked up on first use (0: not yet)
+    std::atomic<int>& slot = resident_on[c->device & 63];
+    int resident = slot.load(std::memory_order_relaxed);
+    if (resident <= 0) {
+        resident = max_resident_pairs(c, kern, smem);
+        slot.store(resident, std::memory_order_relaxed);
+    }
     const int pairs = std::min(args.num_tiles, resident);
     GemmArgs run = args;
     plan_split(c, run, pairs);

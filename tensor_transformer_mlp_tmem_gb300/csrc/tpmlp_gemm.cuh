@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 
 #include "sm103_ptx.cuh"
+#include "tpmlp_plan.h"
 
 namespace tpmlp {
 
@@ -100,49 +101,6 @@ struct GemmArgs {
 };
 
 constexpr int kSkSlotFloats = 128 * 256;  // one CTA's half of a 256 x 256 accumulator
-
-// The sequence of work units (tile, reduction blocks [kb0, kb1)) of one CTA pair: its whole
-// tiles first, then its share of the split region. Every role of the pair walks the same
-// sequence.
-struct WorkCursor {
-    int t;
-    long long it, it_end;
-};
-
-__device__ __forceinline__ WorkCursor work_begin(const GemmArgs& a, int pair, int num_pairs) {
-    WorkCursor c;
-    c.t = pair;
-    c.it = static_cast<long long>(a.sk_iters) * pair / num_pairs;
-    c.it_end = static_cast<long long>(a.sk_iters) * (pair + 1) / num_pairs;
-    return c;
-}
-
-__device__ __forceinline__ bool work_next(const GemmArgs& a, int num_pairs, WorkCursor& c,
-                                          int& tile, int& kb0, int& kb1) {
-    if (c.t < a.sk_first) {
-        tile = c.t;
-        kb0 = 0;
-        kb1 = a.kb_tile;
-        c.t += num_pairs;
-        return true;
-    }
-    if (c.it < c.it_end) {
-        const long long rel = c.it / a.kb_tile;
-        kb0 = static_cast<int>(c.it - rel * a.kb_tile);
-        kb1 = static_cast<int>(min(static_cast<long long>(a.kb_tile), kb0 + (c.it_end - c.it)));
-        tile = a.sk_first + static_cast<int>(rel);
-        c.it += kb1 - kb0;
-        return true;
-    }
-    return false;
-}
-
-// The pair whose share of the split region holds reduction block i (shares are
-// [floor(S p / P), floor(S (p + 1) / P))).
-__device__ __forceinline__ int work_pair_of(const GemmArgs& a, int num_pairs, long long i) {
-    const long long S = a.sk_iters;
-    return static_cast<int>(((i + 1) * num_pairs + S - 1) / S - 1);
-}
 
 // The accumulator columns one epilogue warp drains, 32 at a time: [c0, c0 + kCols) with
 // c0 = part * kCols, and in the gated layer also the same columns of the up half (+ G).

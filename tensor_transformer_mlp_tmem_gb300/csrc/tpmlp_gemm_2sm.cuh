@@ -104,9 +104,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
-            WorkCursor cur = work_begin(args, pair, num_pairs);
+            WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
             int t, kb0, kb1;
-            while (ok && work_next(args, num_pairs, cur, t, kb0, kb1)) {
+            while (ok && work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
                 int m_blk, n_blk;
                 decode_tile(args, t, m_blk, n_blk);
                 const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;  // this CTA's A rows
@@ -177,9 +177,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         if (leader && lane == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            WorkCursor cur = work_begin(args, pair, num_pairs);
+            WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
             int t, kb0, kb1;
-            while (ok && work_next(args, num_pairs, cur, t, kb0, kb1)) {
+            while (ok && work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
                 if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status,
                                     kCode | kSiteMmaAccum)) {
                     ok = false;
@@ -225,9 +225,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         const int part = (warp - 2) >> 2;
         uint32_t acc = 0, acc_phase = 0;
         const int ew = warp - 2;  // epilogue warp index: its flag in a split unit
-        WorkCursor cur = work_begin(args, pair, num_pairs);
+        WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
         int t, kb0, kb1;
-        while (work_next(args, num_pairs, cur, t, kb0, kb1)) {
+        while (work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
             int m_blk, n_blk;
             decode_tile(args, t, m_blk, n_blk);
             const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;
@@ -241,7 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             if (kb0 == 0 && kb1 < args.kb_tile) {
                 const long long last =
                     static_cast<long long>(t - args.sk_first + 1) * args.kb_tile - 1;
-                n_in = work_pair_of(args, num_pairs, last) - pair;
+                n_in = work_pair_of(args.sk_iters, num_pairs, last) - pair;
                 for (int p = 1; ok && p <= n_in; ++p)
                     ok = ptx::flag_wait(my_flag + static_cast<size_t>(p) * 2 * kEpiWarps,
                                         args.sk_epoch, abort_flag, args.status,

@@ -1,5 +1,18 @@
-// Row-chunk planner of the host-buffer forward pass (plain C++, no CUDA: the host tests build
-// it alone).
+// Work planning shared by the host code, the GEMM kernels and the host tests (plain C++; the
+// host tests build it with g++ alone):
+//   1. the split reduction's plan and the CTA-pair kernel's walk over its work units;
+//   2. the row-chunk planner of the host-buffer forward pass.
+//
+// ---------------------------------------------------------------- 1. split reduction
+//
+// A CTA-pair launch of T output tiles, each reduced over kb_tile blocks of 64, on P resident
+// pairs. Tiles [0, sk_first) are whole units, handed out round robin (pair p: p, p + P, ...).
+// The sk_iters = (T - sk_first) * kb_tile reduction blocks of the remaining tiles, in tile
+// order, are cut into P contiguous shares [floor(S p / P), floor(S (p + 1) / P)) that every
+// role of a pair walks in order. A pair whose share starts inside a tile writes its partial sum
+// for the owner of that tile: the pair that holds the tile's first block, last in its share.
+//
+// ---------------------------------------------------------------- 2. host-buffer chunks
 //
 // Token rows are independent, so a forward pass on host buffers can stream: the copy of chunk
 // c + 1 in (and of chunk c - 1 out) overlaps the GEMMs of chunk c. Two effects pull the chunk
@@ -19,7 +32,79 @@
 
 #include <cstdint>
 
+#if defined(__CUDACC__)
+#define TPMLP_HD __host__ __device__ __forceinline__
+#else
+#define TPMLP_HD inline
+#endif
+
 namespace tpmlp {
+
+struct WorkCursor {
+    int t;                // next whole tile of this pair
+    long long it, it_end; // this pair's share of the split blocks
+};
+
+TPMLP_HD WorkCursor work_begin(int sk_iters, int pair, int num_pairs) {
+    WorkCursor c;
+    c.t = pair;
+    c.it = static_cast<long long>(sk_iters) * pair / num_pairs;
+    c.it_end = static_cast<long long>(sk_iters) * (pair + 1) / num_pairs;
+    return c;
+}
+
+// The next work unit of a pair: tile `tile`, reduction blocks [kb0, kb1). False when done.
+TPMLP_HD bool work_next(int sk_first, int kb_tile, int num_pairs, WorkCursor& c, int& tile,
+                        int& kb0, int& kb1) {
+    if (c.t < sk_first) {
+        tile = c.t;
+        kb0 = 0;
+        kb1 = kb_tile;
+        c.t += num_pairs;
+        return true;
+    }
+    if (c.it < c.it_end) {
+        const long long rel = c.it / kb_tile;
+        kb0 = static_cast<int>(c.it - rel * kb_tile);
+        const long long left = c.it_end - c.it;
+        kb1 = static_cast<int>(kb0 + left < kb_tile ? kb0 + left : kb_tile);
+        tile = sk_first + static_cast<int>(rel);
+        c.it += kb1 - kb0;
+        return true;
+    }
+    return false;
+}
+
+// The pair whose share holds split block i.
+TPMLP_HD int work_pair_of(int sk_iters, int num_pairs, long long i) {
+    const long long S = sk_iters;
+    return static_cast<int>(((i + 1) * num_pairs + S - 1) / S - 1);
+}
+
+// Which tiles of a launch are split (sk_first; sk_first == num_tiles: none). A launch of between
+// one and two waves (pairs < T, and the second wave at most tail_pct % full) is split
+// entirely, provided each tile has at least min_blocks reduction blocks and the operands
+// (A rows and B rows of every tile row and column, kb_tile blocks of 64 bf16 deep) fit in
+// max_operand_bytes. Longer launches keep whole tiles.
+struct SplitPlan {
+    int sk_first;
+    int sk_iters;
+};
+
+inline SplitPlan plan_split_tiles(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks,
+                                  int tile_rows, int tail_pct, int min_blocks,
+                                  double max_operand_bytes) {
+    SplitPlan p{num_tiles, 0};
+    if (pairs <= 0 || kb_tile <= 0) return p;
+    const int waves = num_tiles / pairs, rem = num_tiles % pairs;
+    if (waves != 1 || rem == 0 || rem * 100 > pairs * tail_pct) return p;
+    const double operand_bytes =
+        static_cast<double>(m_blocks + n_blocks) * tile_rows * kb_tile * 64 * 2.0;
+    if (kb_tile < min_blocks || operand_bytes > max_operand_bytes) return p;
+    p.sk_first = 0;
+    p.sk_iters = num_tiles * kb_tile;
+    return p;
+}
 
 struct ChunkGemm {
     int64_t tile_rows;   // token rows per output tile (256 on CTA pairs, 128 on one SM)

@@ -1,0 +1,144 @@
+"""The split reduction's schedule (csrc/tpmlp_plan.h), on the CPU: the same functions the
+CTA-pair kernel calls to walk its work units, built with g++.
+
+Checked for many launch shapes: every (tile, reduction block) is computed exactly once; a pair
+writes at most one partial sum, for the first unit of its share; the owner of a split tile
+(the pair holding its first block) processes that block range last and adds exactly the
+partials of the pairs after it; and which launches the host plan splits."""
+import ctypes
+import os
+import random
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(os.path.dirname(HERE), "tensor_transformer_mlp_tmem_gb300", "csrc")
+
+SHIM = r"""
+#include "tpmlp_plan.h"
+extern "C" {
+int shim_walk(int sk_first, int sk_iters, int kb_tile, int pair, int num_pairs, int max_units,
+              int* out) {
+    tpmlp::WorkCursor c = tpmlp::work_begin(sk_iters, pair, num_pairs);
+    int n = 0, t, kb0, kb1;
+    while (n < max_units && tpmlp::work_next(sk_first, kb_tile, num_pairs, c, t, kb0, kb1)) {
+        out[3 * n] = t; out[3 * n + 1] = kb0; out[3 * n + 2] = kb1; ++n;
+    }
+    return n;
+}
+int shim_pair_of(int sk_iters, int num_pairs, long long i) {
+    return tpmlp::work_pair_of(sk_iters, num_pairs, i);
+}
+void shim_plan(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks, int* out) {
+    tpmlp::SplitPlan p = tpmlp::plan_split_tiles(num_tiles, pairs, kb_tile, m_blocks, n_blocks,
+                                                 256, 85, 16, 64.0 * (1 << 20));
+    out[0] = p.sk_first; out[1] = p.sk_iters;
+}
+}
+"""
+
+
+@pytest.fixture(scope="module")
+def sched(tmp_path_factory):
+    d = tmp_path_factory.mktemp("sched")
+    src, so = d / "shim.cpp", d / "libsched.so"
+    src.write_text(SHIM)
+    subprocess.check_call(["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-I", CSRC, str(src),
+                           "-o", str(so)])
+    lib = ctypes.CDLL(str(so))
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.shim_walk.argtypes = [ctypes.c_int] * 6 + [ip]
+    lib.shim_pair_of.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_longlong]
+    lib.shim_plan.argtypes = [ctypes.c_int] * 5 + [ip]
+    return lib
+
+
+def walk(lib, sk_first, sk_iters, kb, pair, P):
+    buf = (ctypes.c_int * (3 * 4096))()
+    n = lib.shim_walk(sk_first, sk_iters, kb, pair, P, 4096, buf)
+    return [tuple(buf[3 * i:3 * i + 3]) for i in range(n)]
+
+
+def check_schedule(lib, T, P, kb, sk_first):
+    S = (T - sk_first) * kb
+    units = {p: walk(lib, sk_first, S, kb, p, P) for p in range(P)}
+    covered = {}
+    partial_of = {}  # tile -> pairs that write a partial for it
+    for p, us in units.items():
+        n_whole = len([u for u in us if u[0] < sk_first])
+        assert [u[0] for u in us[:n_whole]] == list(range(p, sk_first, P))
+        heads_missing = [u for u in us if u[1] > 0]
+        assert len(heads_missing) <= 1
+        if heads_missing:
+            assert us.index(heads_missing[0]) == n_whole  # the first unit of the share
+            partial_of.setdefault(heads_missing[0][0], []).append(p)
+        for t, k0, k1 in us:
+            assert 0 <= t < T and 0 <= k0 < k1 <= kb
+            for k in range(k0, k1):
+                assert (t, k) not in covered
+                covered[(t, k)] = p
+    assert len(covered) == T * kb
+    for p, us in units.items():
+        for i, (t, k0, k1) in enumerate(us):
+            if k0 == 0 and k1 < kb:  # owner of a split tile
+                assert i == len(us) - 1
+                last = (t - sk_first + 1) * kb - 1
+                n_in = lib.shim_pair_of(S, P, last) - p
+                assert sorted(partial_of.get(t, [])) == list(range(p + 1, p + 1 + n_in))
+                assert n_in >= 1
+            elif k0 > 0:
+                assert t in partial_of
+    # every split tile has exactly one owner
+    for t, ps in partial_of.items():
+        owners = [p for p, us in units.items() for u in us if u[0] == t and u[1] == 0]
+        assert len(owners) == 1 and owners[0] < min(ps)
+
+
+@pytest.mark.parametrize("T,P,kb", [(96, 76, 48), (100, 74, 16), (128, 76, 16), (80, 75, 40),
+                                    (96, 76, 8), (150, 76, 1), (77, 76, 300)])
+def test_whole_launch_split(sched, T, P, kb):
+    check_schedule(sched, T, P, kb, 0)
+
+
+@pytest.mark.parametrize("T,P,kb", [(512, 76, 256), (768, 76, 768), (1000, 74, 7)])
+def test_tail_split_and_whole_tiles(sched, T, P, kb):
+    check_schedule(sched, T, P, kb, (T // P - 1) * P)
+
+
+def test_no_split_is_round_robin(sched):
+    T, P, kb = 2048, 76, 64
+    for p in (0, 1, 75):
+        assert walk(sched, T, 0, kb, p, P) == [(t, 0, kb) for t in range(p, T, P)]
+
+
+def test_random_schedules(sched):
+    rng = random.Random(7)
+    for _ in range(150):
+        P = rng.randint(2, 76)
+        T = rng.randint(P + 1, 3 * P)
+        kb = rng.randint(1, 64)
+        first = rng.choice([0, (T // P - 1) * P])
+        check_schedule(sched, T, P, kb, first)
+
+
+def plan(lib, T, P, kb, mb, nb):
+    out = (ctypes.c_int * 2)()
+    lib.shim_plan(T, P, kb, mb, nb, out)
+    return out[0], out[1]
+
+
+@pytest.mark.parametrize("P", [74, 75, 76])
+def test_which_launches_split(sched, P):
+    # GPT-2 second GEMM: 32 x 3 tiles, 48 blocks, 55 MB of operands -> split
+    assert plan(sched, 96, P, 48, 32, 3) == (0, 96 * 48)
+    # 7b: 2048 and 512 tiles (many waves) -> whole tiles
+    assert plan(sched, 2048, P, 64, 32, 64)[0] == 2048
+    assert plan(sched, 512, P, 256, 32, 16)[0] == 512
+    # 7b second GEMM on a 2048-row chunk: 128 tiles but 201 MB of operands -> whole tiles
+    assert plan(sched, 128, P, 256, 8, 16)[0] == 128
+    # GPT-2 first GEMM on a 2048-row chunk: 96 tiles of 12 blocks -> too shallow to split
+    assert plan(sched, 96, P, 12, 8, 12)[0] == 96
+    # fewer tiles than pairs, or a second wave almost full -> whole tiles
+    assert plan(sched, 40, P, 64, 4, 10)[0] == 40
+    assert plan(sched, 2 * P - 1, P, 64, 4, 10)[0] == 2 * P - 1
