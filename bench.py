@@ -709,10 +709,19 @@ def main():
     ap.add_argument("--cpu-max-rows", type=int, default=4096)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default=None, metavar="H,F,k,M",
+                    help="a custom block shape instead of --workload (seeded like the named "
+                         "workloads; for profiling a kernel at another shape)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]
+    if args.shape:
+        try:
+            H, F, k, M = (int(v) for v in args.shape.split(","))
+        except ValueError:
+            ap.error("--shape wants four integers H,F,k,M")
+        w = synth.Workload(f"custom-h{H}-f{F}-k{k}-m{M}", 1, M, H, F, k, 7)
     if args.k is not None:
         w = synth.Workload(w.name, w.B, w.S, w.H, w.F, args.k, w.seed)
     if args.impl == "reference":
