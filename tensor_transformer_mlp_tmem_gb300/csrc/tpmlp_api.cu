@@ -230,26 +230,28 @@ int max_resident_pairs(tpmlp_ctx* c, Kernel kern, uint32_t smem) {
     return n;
 }
 
-// The split plan of one pair-kernel launch (GemmArgs::sk_*). A launch of between one and two
-// waves of tiles (pairs < T <= 2 pairs, with the second wave at most TPMLP_SPLIT_TAIL_PCT full)
-// divides all its reduction blocks evenly among the pairs, so that every pair finishes within
-// one block of the others instead of a second wave running on part of the GPU -- provided the
-// operands fit in half of L2 and each tile has at least kSplitMinBlocks reduction blocks.
-// Otherwise tiles stay whole: the pairs of a wave then walk the reduction in step and share
-// operand tiles in L2, which staggered shares lose, and a short reduction cannot pay for the
-// partial sums' round trip. Measured against whole tiles: the GPT-2 second GEMM (96 tiles,
-// 55 MB of operands, 48 blocks) 10 % faster; the 7b second GEMM on 2048-row chunks (128 tiles,
-// 201 MB) and the GPT-2 first GEMM on 2048-row chunks (96 tiles, 12 blocks) slower.
-constexpr int kSplitMinBlocks = 16;
-constexpr double kSplitMaxOperandBytes = 64.0 * (1 << 20);
+// The split plan of one pair-kernel launch (GemmArgs::sk_*, tpmlp_plan.h). Measured against
+// whole tiles:
+//  - Launches of one to two waves, split entirely: the GPT-2 second GEMM (96 tiles, 55 MB of
+//    operands, 48 blocks) 10 % faster. The 7b second GEMM on 2048-row chunks (128 tiles,
+//    201 MB) and the GPT-2 first GEMM on 2048-row chunks (96 tiles, 12 blocks) were slower,
+//    hence the L2 and depth limits.
+//  - Longer launches: splitting a whole wave plus the tail (132 of the 7b second GEMM's 512
+//    tiles) cost 9 %, because the pairs' staggered shares lose the wave's shared operands in
+//    L2. Only the last R tiles are split, and only where the model (R / P of a round plus
+//    one DRAM read of the tail's operands, under half a round) favours it: the GPT-3 second
+//    GEMM (R = 8, 768 blocks) 4.7 % faster; the GPT-3 first GEMM (R = 32, 192 blocks, at 70 %
+//    of a round by the model) 1.3 % slower, hence the half.
+constexpr tpmlp::SplitRule kSplitRule{TPMLP_SPLIT_TAIL_PCT, 16, 64.0 * (1 << 20),
+                                      1.7e15 / 76, 6.0e12, 0.5};
 
 void plan_split(tpmlp_ctx* c, GemmArgs& a, int pairs) {
     a.sk_first = a.num_tiles;
     a.sk_iters = 0;
     if (!c->sk_partial || pairs > c->num_sms / 2) return;
-    const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(
-        a.num_tiles, pairs, a.kb_tile, a.m_blocks, a.n_blocks, tpmlp::kPairBM,
-        TPMLP_SPLIT_TAIL_PCT, kSplitMinBlocks, kSplitMaxOperandBytes);
+    const tpmlp::SplitLaunch L{a.num_tiles, pairs,    a.kb_tile,       a.m_blocks,
+                               a.n_blocks,  a.group_m, tpmlp::kPairBM, tpmlp::kPairBN};
+    const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, kSplitRule);
     if (p.sk_first == a.num_tiles) return;
     a.sk_first = p.sk_first;
     a.sk_iters = p.sk_iters;

@@ -455,13 +455,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs
 }
 
 __device__ __forceinline__ void decode_tile(const GemmArgs& a, int t, int& m_blk, int& n_blk) {
-    const int per_group = a.group_m * a.n_blocks;
-    const int g = t / per_group;
-    const int first_m = g * a.group_m;
-    const int gm = min(a.m_blocks - first_m, a.group_m);
-    const int local = t - g * per_group;
-    m_blk = first_m + local % gm;
-    n_blk = local / gm;
+    decode_tile_mn(a.group_m, a.m_blocks, a.n_blocks, t, m_blk, n_blk);
 }
 
 // A: GEMM1 -> X [M][H] (2-D map, box 64 x 128); GEMM2 -> Y [M][F] (2-D map, box 64 x 128).

@@ -6,7 +6,10 @@
 // ---------------------------------------------------------------- 1. split reduction
 //
 // A CTA-pair launch of T output tiles, each reduced over kb_tile blocks of 64, on P resident
-// pairs. Tiles [0, sk_first) are whole units, handed out round robin (pair p: p, p + P, ...).
+// pairs. Tile t covers row block m and column block n of the output (decode_tile_mn: groups of
+// group_m row blocks, each swept column by column, so that the tiles running at once share
+// operand rows and columns in L2). Tiles [0, sk_first) are whole units, handed out round robin
+// (pair p: p, p + P, ...).
 // The sk_iters = (T - sk_first) * kb_tile reduction blocks of the remaining tiles, in tile
 // order, are cut into P contiguous shares [floor(S p / P), floor(S (p + 1) / P)) that every
 // role of a pair walks in order. A pair whose share starts inside a tile writes its partial sum
@@ -39,6 +42,17 @@
 #endif
 
 namespace tpmlp {
+
+TPMLP_HD void decode_tile_mn(int group_m, int m_blocks, int n_blocks, int t, int& m_blk,
+                             int& n_blk) {
+    const int per_group = group_m * n_blocks;
+    const int g = t / per_group;
+    const int first_m = g * group_m;
+    const int gm = m_blocks - first_m < group_m ? m_blocks - first_m : group_m;
+    const int local = t - g * per_group;
+    m_blk = first_m + local % gm;
+    n_blk = local / gm;
+}
 
 struct WorkCursor {
     int t;                // next whole tile of this pair
@@ -81,28 +95,73 @@ TPMLP_HD int work_pair_of(int sk_iters, int num_pairs, long long i) {
     return static_cast<int>(((i + 1) * num_pairs + S - 1) / S - 1);
 }
 
-// Which tiles of a launch are split (sk_first; sk_first == num_tiles: none). A launch of between
-// one and two waves (pairs < T, and the second wave at most tail_pct % full) is split
-// entirely, provided each tile has at least min_blocks reduction blocks and the operands
-// (A rows and B rows of every tile row and column, kb_tile blocks of 64 bf16 deep) fit in
-// max_operand_bytes. Longer launches keep whole tiles.
+// Which tiles of a launch are split (sk_first; sk_first == num_tiles: none). Two cases:
+//  - A launch of between one and two waves (pairs < T, the second wave at most tail_pct %
+//    full) is split entirely, provided each tile has at least min_blocks reduction blocks and
+//    the operands (A rows of every tile row and B rows of every tile column, kb_tile blocks of
+//    64 bf16 deep) fit in max_operand_bytes: the pairs of a wave no longer walk the reduction
+//    in step, so the operands must stay in L2.
+//  - A longer launch keeps its whole waves and splits only the last R = T mod P tiles, when
+//    that is modelled to take under tail_gain of a round: the R tiles' work spread over all
+//    pairs (R / P of a round) plus one read of their operand rows and columns from DRAM,
+//    against a round of whole tiles. Their shares must be non-empty (R * kb_tile >= P).
+// A round is 2 * 256 * 256 * 64 * kb_tile FLOP at pair_flops.
 struct SplitPlan {
     int sk_first;
     int sk_iters;
 };
 
-inline SplitPlan plan_split_tiles(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks,
-                                  int tile_rows, int tail_pct, int min_blocks,
-                                  double max_operand_bytes) {
-    SplitPlan p{num_tiles, 0};
-    if (pairs <= 0 || kb_tile <= 0) return p;
-    const int waves = num_tiles / pairs, rem = num_tiles % pairs;
-    if (waves != 1 || rem == 0 || rem * 100 > pairs * tail_pct) return p;
-    const double operand_bytes =
-        static_cast<double>(m_blocks + n_blocks) * tile_rows * kb_tile * 64 * 2.0;
-    if (kb_tile < min_blocks || operand_bytes > max_operand_bytes) return p;
-    p.sk_first = 0;
-    p.sk_iters = num_tiles * kb_tile;
+struct SplitLaunch {
+    int num_tiles, pairs, kb_tile;
+    int m_blocks, n_blocks, group_m;
+    int tile_rows, tile_cols;   // A rows per row block, B rows per column block
+};
+
+struct SplitRule {
+    int tail_pct;               // whole split: the second wave at most this full
+    int min_blocks;             // ... each tile has at least this many reduction blocks
+    double max_operand_bytes;   // ... and the operands fit in this much L2
+    double pair_flops;          // tail split: FLOP/s of one CTA pair
+    double dram_Bps;            // ... DRAM bandwidth for the tail's operands
+    double tail_gain;           // ... split when the modelled tail is below this share of a round
+};
+
+inline SplitPlan plan_split_tiles(const SplitLaunch& L, const SplitRule& rule) {
+    SplitPlan p{L.num_tiles, 0};
+    if (L.pairs <= 0 || L.kb_tile < rule.min_blocks) return p;
+    const int waves = L.num_tiles / L.pairs, rem = L.num_tiles % L.pairs;
+    if (rem == 0 || waves < 1) return p;
+    const double block_bytes = static_cast<double>(L.kb_tile) * 64 * 2.0;  // one row, all K
+    if (waves == 1) {
+        if (rem * 100 > L.pairs * rule.tail_pct) return p;
+        const double operand_bytes =
+            (static_cast<double>(L.m_blocks) * L.tile_rows +
+             static_cast<double>(L.n_blocks) * L.tile_cols) * block_bytes;
+        if (operand_bytes > rule.max_operand_bytes) return p;
+        p.sk_first = 0;
+        p.sk_iters = L.num_tiles * L.kb_tile;
+        return p;
+    }
+    if (static_cast<long long>(rem) * L.kb_tile < L.pairs) return p;
+    // the distinct row and column blocks of the last rem tiles
+    const int first = L.num_tiles - rem;
+    int m_lo = 1 << 30, m_hi = -1, n_cnt = 0, n_prev = -1;
+    for (int t = first; t < L.num_tiles; ++t) {
+        int m, n;
+        decode_tile_mn(L.group_m, L.m_blocks, L.n_blocks, t, m, n);
+        m_lo = m < m_lo ? m : m_lo;
+        m_hi = m > m_hi ? m : m_hi;
+        if (n != n_prev) ++n_cnt;  // the tail walks whole columns of one row group
+        n_prev = n;
+    }
+    const double round_s = 2.0 * 256 * 256 * 64 * L.kb_tile / rule.pair_flops;
+    const double tail_bytes =
+        (static_cast<double>(m_hi - m_lo + 1) * L.tile_rows + static_cast<double>(n_cnt) * L.tile_cols) *
+        block_bytes;
+    const double tail_s = round_s * rem / L.pairs + tail_bytes / rule.dram_Bps;
+    if (tail_s >= rule.tail_gain * round_s) return p;
+    p.sk_first = first;
+    p.sk_iters = rem * L.kb_tile;
     return p;
 }
 

@@ -107,3 +107,34 @@ def test_split_weight_gradients(lib):
         assert_close(got, ref[name], what=f"split {name}")
         assert_close(got, outs[True][i].reshape(ref[name].shape), rel=2e-3, mx=1e-2,
                      what=f"{name} split vs fixed order")
+
+
+def test_split_of_the_last_tiles(lib):
+    """A launch of several waves keeps whole tiles except its last R = T mod P: at H = 5120,
+    F = 16384, M = 2048 the second GEMM has 160 tiles (2 waves + R on 74-76 pairs), each 256
+    blocks deep, and only those R are split (their partial sums meet across up to a dozen
+    pairs)."""
+    Hs, Fs, ks, Ms = 5120, 16384, 8, 2048
+    d = synth.make_inputs(Hs, Fs, Ms, 251)
+    dd = inputs_on_device(d)
+    outs = {}
+    for name, kw in (("split", {}), ("fixed", dict(fixed_order=True)),
+                     ("split32", dict(z_fp32=True)), ("fixed32", dict(z_fp32=True, fixed_order=True))):
+        with tp.TPMLP(Hs, Fs, ks, **kw) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            Y = mlp.gemm1(dd["X"])
+            Z = mlp.gemm2(Y)
+            Z2 = mlp.gemm2(Y)
+            torch.cuda.synchronize()
+            rc, detail = mlp.status()
+            assert rc == tp.TPMLP_OK, f"device status {detail:#x}"
+            assert torch.equal(Z, Z2)  # deterministic
+            outs[name] = (Y, Z)
+    assert torch.equal(outs["split"][0], outs["fixed"][0])  # the first GEMM is not split here
+    a, b = outs["split32"][1].double(), outs["fixed32"][1].double()
+    assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() < 1e-5
+    assert not torch.equal(outs["split32"][1], outs["fixed32"][1]), "the tail was not split"
+    rows = synth.sample_rows(Ms, 24)
+    ref = oracle.tpmlp(synth.make_inputs(Hs, Fs, Ms, 251, x_rows=rows)["X"], d["W1"], d["b1"],
+                       d["W2"], d["b2"], ks)
+    assert_close(to_f64(outs["split"][1])[rows], ref["Z"], what="tail-split Z")

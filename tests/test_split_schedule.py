@@ -30,9 +30,11 @@ int shim_walk(int sk_first, int sk_iters, int kb_tile, int pair, int num_pairs, 
 int shim_pair_of(int sk_iters, int num_pairs, long long i) {
     return tpmlp::work_pair_of(sk_iters, num_pairs, i);
 }
-void shim_plan(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks, int* out) {
-    tpmlp::SplitPlan p = tpmlp::plan_split_tiles(num_tiles, pairs, kb_tile, m_blocks, n_blocks,
-                                                 256, 85, 16, 64.0 * (1 << 20));
+void shim_plan(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks, int group_m,
+               int* out) {
+    const tpmlp::SplitRule rule{85, 16, 64.0 * (1 << 20), 1.7e15 / 76, 6.0e12, 0.5};
+    const tpmlp::SplitLaunch L{num_tiles, pairs, kb_tile, m_blocks, n_blocks, group_m, 256, 256};
+    tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, rule);
     out[0] = p.sk_first; out[1] = p.sk_iters;
 }
 }
@@ -50,7 +52,7 @@ def sched(tmp_path_factory):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.shim_walk.argtypes = [ctypes.c_int] * 6 + [ip]
     lib.shim_pair_of.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_longlong]
-    lib.shim_plan.argtypes = [ctypes.c_int] * 5 + [ip]
+    lib.shim_plan.argtypes = [ctypes.c_int] * 6 + [ip]
     return lib
 
 
@@ -106,6 +108,15 @@ def test_tail_split_and_whole_tiles(sched, T, P, kb):
     check_schedule(sched, T, P, kb, (T // P - 1) * P)
 
 
+@pytest.mark.parametrize("T,P,kb", [(768, 76, 768), (768, 74, 768), (3072, 76, 192), (160, 76, 256),
+                                    (10 * 76 + 1, 76, 76), (5 * 74 + 3, 74, 30)])
+def test_split_of_the_last_tiles_only(sched, T, P, kb):
+    """Only the last R = T mod P tiles split: a tile may span many pairs' shares."""
+    R = T % P
+    assert R * kb >= P
+    check_schedule(sched, T, P, kb, T - R)
+
+
 def test_no_split_is_round_robin(sched):
     T, P, kb = 2048, 76, 64
     for p in (0, 1, 75):
@@ -118,27 +129,52 @@ def test_random_schedules(sched):
         P = rng.randint(2, 76)
         T = rng.randint(P + 1, 3 * P)
         kb = rng.randint(1, 64)
-        first = rng.choice([0, (T // P - 1) * P])
-        check_schedule(sched, T, P, kb, first)
+        R = T % P
+        choices = [0, (T // P - 1) * P] + ([T - R] if R and R * kb >= P else [])
+        check_schedule(sched, T, P, kb, rng.choice(choices))
 
 
-def plan(lib, T, P, kb, mb, nb):
+def plan(lib, T, P, kb, mb, nb, group_m=8):
     out = (ctypes.c_int * 2)()
-    lib.shim_plan(T, P, kb, mb, nb, out)
+    lib.shim_plan(T, P, kb, mb, nb, group_m, out)
     return out[0], out[1]
 
 
 @pytest.mark.parametrize("P", [74, 75, 76])
 def test_which_launches_split(sched, P):
-    # GPT-2 second GEMM: 32 x 3 tiles, 48 blocks, 55 MB of operands -> split
+    # GPT-2 second GEMM: 32 x 3 tiles, 48 blocks, 55 MB of operands -> split entirely
     assert plan(sched, 96, P, 48, 32, 3) == (0, 96 * 48)
-    # 7b: 2048 and 512 tiles (many waves) -> whole tiles
-    assert plan(sched, 2048, P, 64, 32, 64)[0] == 2048
+    # 7b first GEMM: a 50-, 23- or 72-tile tail of 64-block tiles is not worth spreading
+    assert plan(sched, 2048, P, 64, 32, 64, 16)[0] == 2048
+    # GPT-3 first GEMM: 3072 tiles of 192 blocks, a tail of 32-40 -> whole tiles
+    assert plan(sched, 3072, P, 192, 16, 192, 16)[0] == 3072
+    # 7b second GEMM (6.7 waves: spreading the 56-tile tail would take about as long as the
+    # round it saves) -> whole tiles
     assert plan(sched, 512, P, 256, 32, 16)[0] == 512
+    # GPT-3 second GEMM on the 76 pairs of a GB300: 768 tiles, an 8-tile tail in one column of
+    # one row group, 768 blocks deep -> the tail alone is split (on 74 pairs the 28-tile tail
+    # would not be worth it)
+    if P == 76:
+        assert plan(sched, 768, P, 768, 16, 48) == (760, 8 * 768)
+    if P == 74:
+        assert plan(sched, 768, P, 768, 16, 48)[0] == 768
     # 7b second GEMM on a 2048-row chunk: 128 tiles but 201 MB of operands -> whole tiles
     assert plan(sched, 128, P, 256, 8, 16)[0] == 128
-    # GPT-2 first GEMM on a 2048-row chunk: 96 tiles of 12 blocks -> too shallow to split
+    # GPT-2 first GEMM: 12 blocks per tile -> too shallow to split, whole or tail
     assert plan(sched, 96, P, 12, 8, 12)[0] == 96
+    assert plan(sched, 384, P, 12, 32, 12, 16)[0] == 384
     # fewer tiles than pairs, or a second wave almost full -> whole tiles
     assert plan(sched, 40, P, 64, 4, 10)[0] == 40
     assert plan(sched, 2 * P - 1, P, 64, 4, 10)[0] == 2 * P - 1
+
+
+def test_tail_split_keeps_shares_nonempty(sched):
+    """A tail of R tiles is split only if R * kb_tile >= P: every pair then has a share, so
+    every contributor an owner waits for exists."""
+    P = 76
+    for R in range(1, 20):
+        for kb in (16, 32, 64, 768):
+            T = 10 * P + R
+            first, iters = plan(sched, T, P, kb, 16, T // 16 + 1)
+            if first != T:
+                assert first == T - R and iters == R * kb and iters >= P
