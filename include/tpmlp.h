@@ -141,6 +141,10 @@ TPMLP_API int tpmlp_reserve(tpmlp_ctx *ctx, int64_t max_tokens);
  * Z may then be NULL).
  * Errors: INVALID_ARG, NOT_PACKED, MISALIGNED, OOM (growing Y), CUDA. A pipeline timeout
  * inside a kernel is reported by tpmlp_get_status, not here.
+ * CUDA graphs: the call can be captured once tpmlp_reserve has sized Y for the captured token
+ * count (capture forbids the allocation). Launches enqueued under stream capture never split
+ * their reduction across CTA pairs, so a replay computes what an eager call with
+ * TPMLP_FLAG_FIXED_ORDER computes.
  */
 TPMLP_API int tpmlp_forward(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z, void *stream);
 

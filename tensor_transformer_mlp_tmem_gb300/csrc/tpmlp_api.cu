@@ -245,10 +245,22 @@ int max_resident_pairs(tpmlp_ctx* c, Kernel kern, uint32_t smem) {
 constexpr tpmlp::SplitRule kSplitRule{TPMLP_SPLIT_TAIL_PCT, 16, 64.0 * (1 << 20),
                                       1.7e15 / 76, 6.0e12, 0.5};
 
-void plan_split(tpmlp_ctx* c, GemmArgs& a, int pairs) {
+// The split's flags carry an epoch chosen here, per launch. A launch recorded into a CUDA graph
+// would replay with the same epoch and could read partial sums before they are written, so
+// launches enqueued under stream capture never split.
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return true;  // unknown: take the safe path
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
+void plan_split(tpmlp_ctx* c, GemmArgs& a, int pairs, cudaStream_t s) {
     a.sk_first = a.num_tiles;
     a.sk_iters = 0;
-    if (!c->sk_partial || pairs > c->num_sms / 2) return;
+    if (!c->sk_partial || pairs > c->num_sms / 2 || capturing(s)) return;
     const tpmlp::SplitLaunch L{a.num_tiles, pairs,    a.kb_tile,       a.m_blocks,
                                a.n_blocks,  a.group_m, tpmlp::kPairBM, tpmlp::kPairBN};
     const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, kSplitRule);
@@ -278,7 +290,7 @@ int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
     }
     const int pairs = std::min(args.num_tiles, resident);
     GemmArgs run = args;
-    plan_split(c, run, pairs);
+    plan_split(c, run, pairs, s);
     kern<<<2 * pairs, tpmlp::kNumThreads, smem, s>>>(a, b, run);
     TPMLP_CUDA(c, cudaGetLastError());
     ++c->launches;

@@ -138,3 +138,32 @@ def test_split_of_the_last_tiles(lib):
     ref = oracle.tpmlp(synth.make_inputs(Hs, Fs, Ms, 251, x_rows=rows)["X"], d["W1"], d["b1"],
                        d["W2"], d["b2"], ks)
     assert_close(to_f64(outs["split"][1])[rows], ref["Z"], what="tail-split Z")
+
+
+def test_forward_in_a_cuda_graph(lib, block):
+    """A forward captured into a CUDA graph and replayed on new inputs. Launches enqueued under
+    stream capture never split their reduction (a replay would reuse the captured flags'
+    epoch), so every replay must equal the eager forward with TPMLP_FLAG_FIXED_ORDER."""
+    d, dd = block
+    X0 = dd["X"].view(1, M, H)
+    X1 = torch.flip(X0, dims=[1]).contiguous()  # other inputs: the rows in reverse order
+    with tp.TPMLP(H, F, K_SHARDS, fixed_order=True) as ref:
+        ref.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        want0, want1 = ref(X0), ref(X1)
+        torch.cuda.synchronize()
+    with tp.TPMLP(H, F, K_SHARDS) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        mlp.reserve(M)
+        Xs = X0.clone()
+        Zs = mlp(Xs)  # eager first: one-time set-up stays out of the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            mlp(Xs, Zs)
+        for X, want in ((X1, want1), (X0, want0), (X1, want1)):
+            Xs.copy_(X)
+            Zs.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(Zs, want)
+        assert mlp.status()[0] == tp.TPMLP_OK
