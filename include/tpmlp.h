@@ -25,7 +25,10 @@
  *    ever crosses this interface. A failed call leaves the context usable unless it
  *    returned TPMLP_ERR_CUDA (a sticky CUDA error, after which the context should be
  *    destroyed).
- *  - A context is used from one host thread at a time.
+ *  - A context is used from one host thread at a time, and its GEMM calls on one stream at a
+ *    time: calls on different streams must not overlap on the GPU, because they share the
+ *    context's intermediate and split-reduction workspaces. Separate contexts are
+ *    independent.
  */
 #ifndef TPMLP_H
 #define TPMLP_H
