@@ -387,7 +387,7 @@ def run_gpu(args, w: synth.Workload):
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(3, min(args.steps, 50))
     barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
