@@ -91,35 +91,49 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
-// ------------------------------------------------------------------ flags between CTAs
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+// ------------------------------------------------------------------ arrivals between CTAs
+// The arrivals of this launch on such a counter (acquire: what the arrivers wrote before they
+// counted in is visible afterwards); 0 while it still holds an earlier launch's epoch.
+__device__ __forceinline__ uint32_t epoch_count(const uint32_t* counter, uint32_t epoch) {
     uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    return (v & 0xFFFFFF00u) == ((epoch & 0xFFFFFFu) << 8) ? (v & 0xFFu) : 0u;
 }
 
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Wait until another CTA has written `value` to *flag (acquire). Bounded like mbar_wait:
-// gives up when this CTA has aborted or after kWaitLimitNs, then raises *abort and records
-// `code`.
-__device__ __forceinline__ bool flag_wait(const uint32_t* flag, uint32_t value,
-                                          volatile uint32_t* abort, int* status, int code) {
-    if (ld_acquire_gpu(flag) == value) return true;
+// Wait up to limit_ns (or until this CTA aborts) for a counter to show `target` arrivals of
+// this launch; returns the last count seen. A short, optional wait: the caller has a way on.
+__device__ __forceinline__ uint32_t epoch_count_wait(const uint32_t* counter, uint32_t epoch,
+                                                     uint32_t target, uint64_t limit_ns,
+                                                     volatile uint32_t* abort) {
+    uint32_t n = epoch_count(counter, epoch);
+    if (n >= target) return n;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t spin = 1;; ++spin) {
-        if (ld_acquire_gpu(flag) == value) return true;
-        if ((spin & 15u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                *abort = 1u;
-                atomicCAS(status, 0, code);
-                return false;
-            }
-        }
+    for (;;) {
+        n = epoch_count(counter, epoch);
+        if (n >= target || *abort || globaltimer_ns() - t0 > limit_ns) return n;
     }
+}
+
+// Count one arrival on a counter shared by the CTAs of one launch. The counter's upper 24 bits
+// hold the launch's epoch, the low 8 bits the arrivals of that launch: a value left by an
+// earlier launch counts as zero. Returns the arrivals including this one in *arrivals. Bounded:
+// gives up (raising *abort and recording `code`) if the compare-and-swap keeps losing.
+__device__ __forceinline__ bool epoch_arrive(uint32_t* counter, uint32_t epoch, uint32_t* arrivals,
+                                             volatile uint32_t* abort, int* status, int code) {
+    const uint32_t tag = (epoch & 0xFFFFFFu) << 8;
+    uint32_t cur = *reinterpret_cast<volatile uint32_t*>(counter);
+    for (int i = 0; i < (1 << 16); ++i) {
+        const uint32_t base = (cur & 0xFFFFFF00u) == tag ? cur : tag;
+        const uint32_t prev = atomicCAS(counter, cur, base + 1u);
+        if (prev == cur) {
+            *arrivals = (base + 1u) & 0xFFu;
+            return true;
+        }
+        cur = prev;
+    }
+    *abort = 1u;
+    atomicCAS(status, 0, code);
+    return false;
 }
 
 // ------------------------------------------------------------------ TMA
@@ -201,6 +215,31 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes (the load and the store, each
+// waited for): for the split reduction's fold, which keeps fewer registers live than x32.
+__device__ __forceinline__ void tmem_ld_32x32b_x16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x16_wait(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+          "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
 }
 
 // Store 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (the inverse of the load

@@ -75,8 +75,8 @@ struct tpmlp_ctx {
     int64_t colsum_floats = 0;
 
     // split reduction of the last tiles on CTA pairs (absent with TPMLP_FLAG_FIXED_ORDER)
-    float* sk_partial = nullptr;  // [num_sms / 2 pairs][2][128 x 256] fp32 partial accumulators
-    uint32_t* sk_flags = nullptr; // [num_sms / 2 pairs][2][epilogue warps] epoch stamps
+    float* sk_partial = nullptr;  // [num_sms / 2 pairs][2 units][2 CTAs][128 x 256] fp32 partials
+    uint32_t* sk_count = nullptr; // [num_sms split tiles][2 CTAs][epilogue warps] arrivals
     uint32_t sk_epoch = 0;
 
     int* status = nullptr;  // device status word
@@ -264,12 +264,13 @@ void plan_split(tpmlp_ctx* c, GemmArgs& a, int pairs, cudaStream_t s) {
     const tpmlp::SplitLaunch L{a.num_tiles, pairs,    a.kb_tile,       a.m_blocks,
                                a.n_blocks,  a.group_m, tpmlp::kPairBM, tpmlp::kPairBN};
     const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, kSplitRule);
-    if (p.sk_first == a.num_tiles) return;
+    // the counters hold num_sms split tiles (the plan never splits more than 2 * pairs)
+    if (p.sk_first == a.num_tiles || a.num_tiles - p.sk_first > c->num_sms) return;
     a.sk_first = p.sk_first;
     a.sk_iters = p.sk_iters;
     a.sk_partial = c->sk_partial;
-    a.sk_flags = c->sk_flags;
-    if (++c->sk_epoch == 0) c->sk_epoch = 1;  // flags start at 0: never reuse it
+    a.sk_count = c->sk_count;
+    if (++c->sk_epoch == 0) c->sk_epoch = 1;  // counters start at 0 (epoch 0): never reuse it
     a.sk_epoch = c->sk_epoch;
 }
 
@@ -797,13 +798,13 @@ int create_context(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t fl
         tpmlp_destroy(c);
         return rc;
     }
-    // workspace of the split reduction: one 256 KB slot and 16 flags per CTA pair
+    // workspace of the split reduction: two 256 KB slots per CTA pair, 16 counters per tile
     const size_t pairs = static_cast<size_t>(c->num_sms / 2);
-    const size_t nflags = pairs * 2 * tpmlp::kEpiWarps;
+    const size_t ncount = static_cast<size_t>(c->num_sms) * 2 * tpmlp::kEpiWarps;
     if (!(flags & (TPMLP_FLAG_SINGLE_SM | TPMLP_FLAG_FIXED_ORDER)) &&
-        ((e = cudaMalloc(&c->sk_partial, pairs * 2 * tpmlp::kSkSlotFloats * sizeof(float))) != cudaSuccess ||
-         (e = cudaMalloc(&c->sk_flags, nflags * sizeof(uint32_t))) != cudaSuccess ||
-         (e = cudaMemset(c->sk_flags, 0, nflags * sizeof(uint32_t))) != cudaSuccess)) {
+        ((e = cudaMalloc(&c->sk_partial, pairs * 4 * tpmlp::kSkSlotFloats * sizeof(float))) != cudaSuccess ||
+         (e = cudaMalloc(&c->sk_count, ncount * sizeof(uint32_t))) != cudaSuccess ||
+         (e = cudaMemset(c->sk_count, 0, ncount * sizeof(uint32_t))) != cudaSuccess)) {
         rc = (e == cudaErrorMemoryAllocation) ? TPMLP_ERR_OOM : TPMLP_ERR_CUDA;
         tpmlp_destroy(c);
         return rc;
@@ -1199,7 +1200,7 @@ void tpmlp_destroy(tpmlp_ctx* c) {
     cudaFree(c->ln_gamma);
     cudaFree(c->ln_beta);
     cudaFree(c->sk_partial);
-    cudaFree(c->sk_flags);
+    cudaFree(c->sk_count);
     cudaFree(c->status);
     if (cur >= 0 && cur != c->device) cudaSetDevice(cur);
     delete c;

@@ -67,7 +67,7 @@ __host__ __device__ constexpr bool is_gemm1(Mode m) {
 
 // Wait sites recorded in the status word when a bounded wait gives up: (mode << 8) | site.
 enum : int {
-    kSiteProducer = 1, kSiteMmaAccum = 2, kSiteMmaFull = 3, kSiteEpilogue = 4, kSiteSplitK = 5
+    kSiteProducer = 1, kSiteMmaAccum = 2, kSiteMmaFull = 3, kSiteEpilogue = 4, kSiteSplitCount = 5
 };
 
 struct GemmArgs {
@@ -87,17 +87,17 @@ struct GemmArgs {
                            // kBwdDA: the saved pre-activation A [M][ldo] bf16
     void* out2;            // kGemm1Train: the pre-activation A [M][ldo] bf16
     int* status;        // device status word
-    // Split reduction of the last tiles (CTA-pair kernel only). Tiles [0, sk_first) are
-    // whole units handed out round robin; the sk_iters = (num_tiles - sk_first) * kb_tile
-    // reduction blocks of the remaining tiles are divided evenly among the pairs, in tile
-    // order. A pair whose share starts inside a tile writes its fp32 partial accumulator to
-    // its slot of sk_partial and stamps its flags with sk_epoch; the pair holding the tile's
-    // first block adds the partials of the later pairs and runs the epilogue.
+    // Split reduction (CTA-pair kernel only; tpmlp_plan.h). Tiles [0, sk_first) are whole
+    // units handed out round robin; the sk_iters = (num_tiles - sk_first) * kb_tile reduction
+    // blocks of the remaining tiles are divided evenly among the pairs, in tile order. Every
+    // pair holding part of a split tile writes its fp32 partial sum to one of its two slots
+    // and counts itself in; the last to arrive sums all of them, in pair order, and runs the
+    // epilogue. Nothing waits on another CTA.
     int sk_first;          // == num_tiles: no split
     int sk_iters;
-    float* sk_partial;     // [pairs][2 CTAs][256 columns][128 rows] fp32
-    uint32_t* sk_flags;    // [pairs][2 CTAs][epilogue warps]
-    uint32_t sk_epoch;     // nonzero, new for every launch that splits
+    float* sk_partial;     // [pairs][2: first / last unit][2 CTAs][256 columns][128 rows] fp32
+    uint32_t* sk_count;    // [split tiles][2 CTAs][epilogue warps] epoch-tagged arrivals
+    uint32_t sk_epoch;     // new for every launch that splits
 };
 
 constexpr int kSkSlotFloats = 128 * 256;  // one CTA's half of a 256 x 256 accumulator
@@ -120,44 +120,98 @@ __device__ __forceinline__ void for_each_warp_slice(int part, Fn&& fn) {
     }
 }
 
-// Split units. A slot holds one CTA's 128 accumulator rows x 256 columns, column-major
-// (element (r, c) at c * 128 + r), so that a warp's 32 lanes write and read 128 contiguous
-// bytes per column.
-//
-// This warp's share of a partial accumulator -> the pair's slot; the accumulator is released
-// once it has been read.
-template <Mode MODE, int WIDTH, typename Release>
-__device__ __forceinline__ void save_partial(uint32_t taddr, int part, float* slot, int lrow,
-                                             Release release) {
+// Split units. A slot holds one CTA's 128 accumulator rows x 256 columns in groups of four
+// columns: element (r, c) at (c / 4) * 512 + r * 4 + c % 4, so that each lane moves 16 bytes
+// per access and a warp's 32 lanes cover 512 contiguous bytes. Pair p's slots: p * 2 + 0 for
+// the unit that starts its share inside a tile, p * 2 + 1 for the unit that holds a tile's
+// first blocks (a pair has at most one of each).
+__device__ __forceinline__ float* split_slot(float* partial, int pair, int which, uint32_t rank) {
+    return partial + ((static_cast<size_t>(pair) * 2 + which) * 2 + rank) * kSkSlotFloats;
+}
+
+__device__ __forceinline__ size_t slot_index(int c, int lrow) {
+    return static_cast<size_t>(c >> 2) * 512 + static_cast<size_t>(lrow) * 4 + (c & 3);
+}
+
+// This warp's share of its accumulator -> its slot.
+template <Mode MODE, int WIDTH>
+__device__ __forceinline__ void save_partial(uint32_t taddr, int part, float* slot, int lrow) {
     for_each_warp_slice<MODE, WIDTH>(part, [&](int c) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(taddr + c, v);
         ptx::tmem_wait_ld(v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            __stcg(slot + static_cast<size_t>(c + j) * 128 + lrow, __uint_as_float(v[j]));
+        for (int g = 0; g < 8; ++g)
+            __stcg(reinterpret_cast<float4*>(slot + slot_index(c + 4 * g, lrow)),
+                   make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                               __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
     });
-    release();
 }
 
-// Add the partials of n_in later pairs (slots `first`, first + 2 slots, ...; summed in that
-// order) into this warp's share of the accumulator in tensor memory.
+// The first pair's finish: its own part (the first in pair order) plus the partials of pairs
+// p_first + 1 .. p_last (slot 0 each), added in that order into its accumulator.
 template <Mode MODE, int WIDTH>
-__device__ __forceinline__ void fold_partials(uint32_t taddr, int part, const float* first,
-                                              int n_in, int lrow) {
+__device__ __forceinline__ void fold_partials(uint32_t taddr, int part, float* partial,
+                                              uint32_t rank, int p_first, int p_last, int lrow) {
     for_each_warp_slice<MODE, WIDTH>(part, [&](int c) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(taddr + c, v);
         ptx::tmem_wait_ld(v);
 #pragma unroll 1
-        for (int p = 0; p < n_in; ++p) {
-            const float* slot = first + static_cast<size_t>(p) * 2 * kSkSlotFloats;
+        for (int p = p_first + 1; p <= p_last; ++p) {
+            const float* slot = split_slot(partial, p, 0, rank);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                v[j] = __float_as_uint(__uint_as_float(v[j]) +
-                                       __ldcg(slot + static_cast<size_t>(c + j) * 128 + lrow));
+            for (int g = 0; g < 8; ++g) {
+                const float4 q = __ldcg(reinterpret_cast<const float4*>(slot + slot_index(c + 4 * g, lrow)));
+                v[4 * g] = __float_as_uint(__uint_as_float(v[4 * g]) + q.x);
+                v[4 * g + 1] = __float_as_uint(__uint_as_float(v[4 * g + 1]) + q.y);
+                v[4 * g + 2] = __float_as_uint(__uint_as_float(v[4 * g + 2]) + q.z);
+                v[4 * g + 3] = __float_as_uint(__uint_as_float(v[4 * g + 3]) + q.w);
+            }
         }
         ptx::tmem_st_32x32b_x32_wait(taddr + c, v);
+    });
+}
+
+// Any other pair's finish (the first pair handed the tile over): the same sum in pair order
+// p_first .. p_last (the first pair's part from its slot 1, the others' from slot 0, this
+// pair's own from its accumulator), written back into this warp's share of the accumulator,
+// 16 columns at a time (three arrays of them are live).
+template <Mode MODE, int WIDTH>
+__device__ __forceinline__ void reduce_partials(uint32_t taddr, int part, float* partial,
+                                                uint32_t rank, int p_first, int p_last, int self,
+                                                int lrow) {
+    for_each_warp_slice<MODE, WIDTH>(part, [&](int c) {
+#pragma unroll 1
+        for (int h = c; h < c + 32; h += 16) {
+            uint32_t own[16];
+            float sum[16];
+            ptx::tmem_ld_32x32b_x16_wait(taddr + h, own);
+#pragma unroll 1
+            for (int p = p_first; p <= p_last; ++p) {
+                float x[16];
+                if (p == self) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(own[j]);
+                } else {
+                    const float* slot = split_slot(partial, p, p == p_first ? 1 : 0, rank);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const float4 q = __ldcg(reinterpret_cast<const float4*>(slot + slot_index(h + 4 * g, lrow)));
+                        x[4 * g] = q.x;
+                        x[4 * g + 1] = q.y;
+                        x[4 * g + 2] = q.z;
+                        x[4 * g + 3] = q.w;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sum[j] = p == p_first ? x[j] : sum[j] + x[j];
+            }
+            uint32_t out[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) out[j] = __float_as_uint(sum[j]);
+            ptx::tmem_st_32x32b_x16_wait(taddr + h, out);
+        }
     });
 }
 

@@ -26,6 +26,10 @@
 
 namespace tpmlp {
 
+// How long the first pair of a split tile waits for the others' partial sums before it hands
+// the tile over (see the epilogue).
+constexpr uint64_t kSplitWaitNs = 50000;
+
 constexpr int kPairBM = 256;  // output rows per pair tile (128 per CTA)
 constexpr int kPairBN = 256;  // output columns per pair tile (B: 128 rows per CTA)
 
@@ -224,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         const int q = warp & 3;
         const int part = (warp - 2) >> 2;
         uint32_t acc = 0, acc_phase = 0;
-        const int ew = warp - 2;  // epilogue warp index: its flag in a split unit
+        const int ew = warp - 2;  // epilogue warp index: its arrival counter in a split tile
         WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
         int t, kb0, kb1;
         while (work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
@@ -232,24 +236,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             decode_tile(args, t, m_blk, n_blk);
             const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;
             const int n0 = n_blk * kPairBN;
-            // split units: kb0 > 0 -> this pair's partial; kb1 < kb_tile -> add later pairs'
-            const int lrow = q * 32 + lane;
-            uint32_t* const my_flag =
-                args.sk_flags + (static_cast<size_t>(pair) * 2 + rank) * kEpiWarps + ew;
-            int n_in = 0;
-            bool ok = true;
-            if (kb0 == 0 && kb1 < args.kb_tile) {
-                const long long last =
-                    static_cast<long long>(t - args.sk_first + 1) * args.kb_tile - 1;
-                n_in = work_pair_of(args.sk_iters, num_pairs, last) - pair;
-                for (int p = 1; ok && p <= n_in; ++p)
-                    ok = ptx::flag_wait(my_flag + static_cast<size_t>(p) * 2 * kEpiWarps,
-                                        args.sk_epoch, abort_flag, args.status,
-                                        kCode | kSiteSplitK);
-            }
-            if (ok)
-                ok = ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status,
-                                    kCode | kSiteEpilogue);
+            bool ok = ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status,
+                                     kCode | kSiteEpilogue);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             const int row = m0 + q * 32 + lane;
@@ -261,24 +249,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive_cluster(empty);
             };
-            float* const slot =
-                args.sk_partial + (static_cast<size_t>(pair) * 2 + rank) * kSkSlotFloats;
-            if (kb0 > 0) {
-                save_partial<MODE, kPairBN>(taddr, part, slot, lrow, release);
-                __threadfence();  // the partial is in memory before the flag says so
-                __syncwarp();
-#ifndef TPMLP_TEST_SKIP_FLAG
-                if (lane == 0) ptx::st_release_gpu(my_flag, args.sk_epoch);
-#else
-                (void)my_flag;  // test builds only: the partial is never announced
-#endif
-            } else {
-                if (n_in > 0)
-                    fold_partials<MODE, kPairBN>(taddr, part, slot + 2 * kSkSlotFloats, n_in, lrow);
-                const uint32_t stage_buf = base + L::kEpiOffset + (warp - 2) * kStageSliceBytes;
+            const uint32_t stage_buf = base + L::kEpiOffset + (warp - 2) * kStageSliceBytes;
+            bool epilogue = true;
+            if (kb0 != 0 || kb1 != args.kb_tile) {
+                // Part of a split tile, held by pairs p_first .. p_last. The other pairs publish
+                // their partial sums and count in. The pair holding the tile's first blocks
+                // works on them last in its share, so the others are normally in by then: it
+                // waits for them (kSplitWaitNs at most), then sums all parts in pair order from
+                // its accumulator and the published partials and runs the epilogue. If they are
+                // not all in by then (a pair not yet resident while other work holds SMs), it
+                // publishes its own part and counts in too, and whichever pair counts in last
+                // finishes the tile. The count reaches its total only through the first pair,
+                // so exactly one warp finishes each tile, and no wait outlives kSplitWaitNs.
+                const int lrow = q * 32 + lane;
+                const long long i0 = static_cast<long long>(t - args.sk_first) * args.kb_tile;
+                const int p_first = work_pair_of(args.sk_iters, num_pairs, i0);
+                const int p_last = work_pair_of(args.sk_iters, num_pairs, i0 + args.kb_tile - 1);
+                const uint32_t n_parts = static_cast<uint32_t>(p_last - p_first + 1);
+                uint32_t* const counter =
+                    args.sk_count + (static_cast<size_t>(t - args.sk_first) * 2 + rank) * kEpiWarps + ew;
+                bool finish = false;
+                if (kb0 == 0) {
+                    uint32_t in = 0;
+                    if (lane == 0)
+                        in = ptx::epoch_count_wait(counter, args.sk_epoch, n_parts - 1, kSplitWaitNs,
+                                                   abort_flag);
+                    finish = __shfl_sync(0xffffffffu, in, 0) == n_parts - 1;
+                }
+                if (!finish) {
+                    save_partial<MODE, kPairBN>(
+                        taddr, part, split_slot(args.sk_partial, pair, kb0 > 0 ? 0 : 1, rank), lrow);
+                    __threadfence();  // the partial is visible before the arrival is
+                    __syncwarp();
+                    uint32_t arrivals = 0;
+                    bool counted = true;
+                    if (lane == 0)
+                        counted = ptx::epoch_arrive(counter, args.sk_epoch, &arrivals, abort_flag,
+                                                    args.status, kCode | kSiteSplitCount);
+                    arrivals = __shfl_sync(0xffffffffu, arrivals, 0);
+                    counted = __shfl_sync(0xffffffffu, counted, 0);
+                    finish = counted && arrivals == n_parts;
+                }
+                if (finish) {
+                    __threadfence();  // every other partial of the tile is visible
+                    if (pair == p_first)
+                        fold_partials<MODE, kPairBN>(taddr, part, args.sk_partial, rank, p_first,
+                                                     p_last, lrow);
+                    else
+                        reduce_partials<MODE, kPairBN>(taddr, part, args.sk_partial, rank,
+                                                       p_first, p_last, pair, lrow);
+                } else {
+                    release();
+                }
+                epilogue = finish;
+            }
+            if (epilogue)
                 drain_accumulator<MODE, OUT_F32, kPairBN>(taddr, args, row, n0, part, stage_buf,
                                                           release);
-            }
             if (++acc == NUM_ACC) {
                 acc = 0;
                 acc_phase ^= 1u;

@@ -2,9 +2,10 @@
 CTA-pair kernel calls to walk its work units, built with g++.
 
 Checked for many launch shapes: every (tile, reduction block) is computed exactly once; a pair
-writes at most one partial sum, for the first unit of its share; the owner of a split tile
-(the pair holding its first block) processes that block range last and adds exactly the
-partials of the pairs after it; and which launches the host plan splits."""
+writes at most one partial sum per slot (the unit that starts its share inside a tile, and
+the unit that holds a tile's first blocks); the pairs holding a split tile are exactly
+p_first .. p_last of the kernel's arrival count, with the slots the last arriver reads; and
+which launches the host plan splits."""
 import ctypes
 import os
 import random
@@ -66,35 +67,29 @@ def check_schedule(lib, T, P, kb, sk_first):
     S = (T - sk_first) * kb
     units = {p: walk(lib, sk_first, S, kb, p, P) for p in range(P)}
     covered = {}
-    partial_of = {}  # tile -> pairs that write a partial for it
+    segments = {}  # split tile -> [(pair, which slot)]
     for p, us in units.items():
         n_whole = len([u for u in us if u[0] < sk_first])
         assert [u[0] for u in us[:n_whole]] == list(range(p, sk_first, P))
-        heads_missing = [u for u in us if u[1] > 0]
-        assert len(heads_missing) <= 1
-        if heads_missing:
-            assert us.index(heads_missing[0]) == n_whole  # the first unit of the share
-            partial_of.setdefault(heads_missing[0][0], []).append(p)
+        slots = []
         for t, k0, k1 in us:
             assert 0 <= t < T and 0 <= k0 < k1 <= kb
             for k in range(k0, k1):
                 assert (t, k) not in covered
                 covered[(t, k)] = p
+            if k0 != 0 or k1 != kb:  # part of a split tile
+                which = 0 if k0 > 0 else 1
+                slots.append(which)
+                segments.setdefault(t, []).append((p, which))
+        assert len(slots) == len(set(slots)) <= 2  # one partial per slot and pair
     assert len(covered) == T * kb
-    for p, us in units.items():
-        for i, (t, k0, k1) in enumerate(us):
-            if k0 == 0 and k1 < kb:  # owner of a split tile
-                assert i == len(us) - 1
-                last = (t - sk_first + 1) * kb - 1
-                n_in = lib.shim_pair_of(S, P, last) - p
-                assert sorted(partial_of.get(t, [])) == list(range(p + 1, p + 1 + n_in))
-                assert n_in >= 1
-            elif k0 > 0:
-                assert t in partial_of
-    # every split tile has exactly one owner
-    for t, ps in partial_of.items():
-        owners = [p for p, us in units.items() for u in us if u[0] == t and u[1] == 0]
-        assert len(owners) == 1 and owners[0] < min(ps)
+    for t, segs in segments.items():
+        i0 = (t - sk_first) * kb
+        p_first = lib.shim_pair_of(S, P, i0)
+        p_last = lib.shim_pair_of(S, P, i0 + kb - 1)
+        # the kernel counts p_last - p_first + 1 arrivals and reads these slots in pair order
+        assert sorted(segs) == [(p, 1 if p == p_first else 0) for p in range(p_first, p_last + 1)]
+        assert len(segs) >= 2
 
 
 @pytest.mark.parametrize("T,P,kb", [(96, 76, 48), (100, 74, 16), (128, 76, 16), (80, 75, 40),
