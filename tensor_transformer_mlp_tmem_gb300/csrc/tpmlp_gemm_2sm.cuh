@@ -28,7 +28,10 @@ namespace tpmlp {
 
 // How long the first pair of a split tile waits for the others' partial sums before it hands
 // the tile over (see the epilogue).
-constexpr uint64_t kSplitWaitNs = 50000;
+#ifndef TPMLP_SPLIT_WAIT_NS
+#define TPMLP_SPLIT_WAIT_NS 50000
+#endif
+constexpr uint64_t kSplitWaitNs = TPMLP_SPLIT_WAIT_NS;
 
 constexpr int kPairBM = 256;  // output rows per pair tile (128 per CTA)
 constexpr int kPairBN = 256;  // output columns per pair tile (B: 128 rows per CTA)
@@ -281,6 +284,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                         taddr, part, split_slot(args.sk_partial, pair, kb0 > 0 ? 0 : 1, rank), lrow);
                     __threadfence();  // the partial is visible before the arrival is
                     __syncwarp();
+#ifdef TPMLP_TEST_LATE_PARTIALS
+                    // test builds only: the other pairs count in late, so that the first pair
+                    // hands its tiles over and they finish them
+                    if (kb0 > 0) {
+                        const uint64_t t_late = ptx::globaltimer_ns();
+                        while (ptx::globaltimer_ns() - t_late < 200000ull) {
+                        }
+                    }
+#endif
                     uint32_t arrivals = 0;
                     bool counted = true;
                     if (lane == 0)

@@ -167,3 +167,51 @@ def test_forward_in_a_cuda_graph(lib, block):
             torch.cuda.synchronize()
             assert torch.equal(Zs, want)
         assert mlp.status()[0] == tp.TPMLP_OK
+
+
+@pytest.fixture(scope="module")
+def handoff_lib(tmp_path_factory):
+    from tensor_transformer_mlp_tmem_gb300 import _build
+    return _build.build(out=str(tmp_path_factory.mktemp("handoff") / "libtpmlp_handoff.so"),
+                        extra_flags=["-DTPMLP_SPLIT_WAIT_NS=0", "-DTPMLP_TEST_LATE_PARTIALS"])
+
+
+@pytest.mark.parametrize("Hs,Fs,ks,Ms", [(2560, 2048, 2, 2560),     # whole launches split
+                                         (5120, 16384, 8, 2048)])   # the second GEMM's tail split
+def test_split_tiles_handed_over_give_identical_bits(lib, handoff_lib, Hs, Fs, ks, Ms):
+    """A test build whose first pairs never wait and whose other pairs count in 200 us late:
+    the first pair hands every split tile over and the last of the others finishes it through
+    the general reduction. The partials are added in the same order either way, so Y and Z
+    equal the regular library's bit for bit."""
+    import ctypes
+    d = synth.make_inputs(Hs, Fs, Ms, 261)
+    dd = inputs_on_device(d)
+    dbg = ctypes.CDLL(handoff_lib)
+    vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+    dbg.tpmlp_create.argtypes = [ctypes.POINTER(vp), i64, i64, i32, u32]
+    dbg.tpmlp_pack_shards.argtypes = [vp] * 6
+    dbg.tpmlp_gemm1.argtypes = [vp, vp, i64, vp, vp]
+    dbg.tpmlp_gemm2.argtypes = [vp, vp, i64, vp, vp]
+    dbg.tpmlp_get_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+    dbg.tpmlp_destroy.argtypes = [vp]
+    Yh = torch.empty((Ms, Fs), dtype=torch.bfloat16, device="cuda")
+    Zh = torch.empty((Ms, Hs), dtype=torch.bfloat16, device="cuda")
+    ctx = vp()
+    assert dbg.tpmlp_create(ctypes.byref(ctx), Hs, Fs, ks, 0) == 0
+    try:
+        assert dbg.tpmlp_pack_shards(ctx, dd["W1"].data_ptr(), dd["b1"].data_ptr(),
+                                     dd["W2"].data_ptr(), dd["b2"].data_ptr(), None) == 0
+        assert dbg.tpmlp_gemm1(ctx, dd["X"].data_ptr(), Ms, Yh.data_ptr(), None) == 0
+        assert dbg.tpmlp_gemm2(ctx, Yh.data_ptr(), Ms, Zh.data_ptr(), None) == 0
+        detail = ctypes.c_int32(0)
+        assert dbg.tpmlp_get_status(ctx, None, ctypes.byref(detail)) == tp.TPMLP_OK, hex(detail.value)
+    finally:
+        dbg.tpmlp_destroy(ctx)
+    with tp.TPMLP(Hs, Fs, ks) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        Y = mlp.gemm1(dd["X"])
+        Z = mlp.gemm2(Y)
+        torch.cuda.synchronize()
+        assert mlp.status()[0] == tp.TPMLP_OK
+    assert torch.equal(Y, Yh)
+    assert torch.equal(Z, Zh)
