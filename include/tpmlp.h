@@ -29,6 +29,13 @@
  *    time: calls on different streams must not overlap on the GPU, because they share the
  *    context's intermediate and split-reduction workspaces. Separate contexts are
  *    independent.
+ *  - The GEMM kernels are launched with programmatic stream serialisation: each may be
+ *    scheduled while the kernel before it in the stream finishes, and waits (griddepcontrol)
+ *    for that kernel's results before touching global memory. Each also lets the next
+ *    kernel in the stream be scheduled early. A kernel launched normally after a library call
+ *    is unaffected. A caller's own kernel that is launched with programmatic stream
+ *    serialisation after a library call must execute griddepcontrol.wait before it reads
+ *    that call's outputs, as the programmatic dependent launch rules require anyway.
  */
 #ifndef TPMLP_H
 #define TPMLP_H

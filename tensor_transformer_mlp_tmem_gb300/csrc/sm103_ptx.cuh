@@ -273,6 +273,19 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
 }
 
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while the kernel before it
+// in the stream is still running. griddep_wait blocks until that kernel has completed and its
+// memory operations are visible; nothing may touch global memory before it.
+// griddep_launch_dependents lets the next such kernel in the stream be scheduled onto SMs as
+// this grid's CTAs leave them (it still waits in its own griddep_wait).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ CTA pairs (cta_group::2)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

@@ -187,6 +187,25 @@ int ensure_smem_attr(tpmlp_ctx* c, Kernel kern, uint32_t smem, std::atomic<uint6
     return TPMLP_OK;
 }
 
+// Launch a GEMM kernel with programmatic stream serialisation: its CTAs may be scheduled while
+// the kernel before it in the stream finishes, run their set-up (barriers, tensor memory,
+// descriptor prefetch), and wait in griddep_wait until that kernel's results are visible.
+template <typename Kernel>
+cudaError_t launch_overlapped(Kernel kern, int grid, uint32_t smem, cudaStream_t s,
+                              const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(tpmlp::kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, b, args);
+}
+
 template <int BN, int STAGES, Mode MODE, bool F32, bool MN = false>
 int launch_gemm(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                 cudaStream_t s) {
@@ -195,8 +214,7 @@ int launch_gemm(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
     static std::atomic<uint64_t> attr_done{0};
     if (int rc = ensure_smem_attr(c, kern, smem, attr_done)) return rc;
     const int grid = std::min(args.num_tiles, c->num_sms);
-    kern<<<grid, tpmlp::kNumThreads, smem, s>>>(a, b, args);
-    TPMLP_CUDA(c, cudaGetLastError());
+    TPMLP_CUDA(c, launch_overlapped(kern, grid, smem, s, a, b, args));
     ++c->launches;
     return TPMLP_OK;
 }
@@ -292,8 +310,7 @@ int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
     const int pairs = std::min(args.num_tiles, resident);
     GemmArgs run = args;
     plan_split(c, run, pairs, s);
-    kern<<<2 * pairs, tpmlp::kNumThreads, smem, s>>>(a, b, run);
-    TPMLP_CUDA(c, cudaGetLastError());
+    TPMLP_CUDA(c, launch_overlapped(kern, 2 * pairs, smem, s, a, b, run));
     ++c->launches;
     return TPMLP_OK;
 }

@@ -512,6 +512,26 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, int t, int& m_blk
     decode_tile_mn(a.group_m, a.m_blocks, a.n_blocks, t, m_blk, n_blk);
 }
 
+// Bring the bias of this warp's columns in tile t (the CTA's first) into L2 while the tile's
+// operands stream in. In a short launch after a cold L2, the epilogue's bias loads would
+// otherwise wait on DRAM once per 32-column slice; later tiles find the bias in L2.
+template <Mode MODE, int WIDTH>
+__device__ __forceinline__ void prefetch_tile_bias(const GemmArgs& a, int t, int part) {
+    if constexpr (MODE != Mode::kBwdDA && MODE != Mode::kWeightGrad) {
+        if (t >= a.num_tiles) return;
+        int m_blk, n_blk;
+        decode_tile(a, t, m_blk, n_blk);
+        constexpr bool kGated = MODE == Mode::kGemm1Gated;
+        constexpr int kCols = (kGated ? WIDTH / 2 : WIDTH) / kEpiParts;  // <= 128: 4 lines
+        const int lane = threadIdx.x & 31;
+        const int line = lane & 3, half = lane >> 2;  // half 1: the gated layer's up columns
+        if (32 * line < kCols && half < (kGated ? 2 : 1)) {
+            const float* p = a.bias + n_blk * WIDTH + half * (WIDTH / 2) + part * kCols + 32 * line;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        }
+    }
+}
+
 // A: GEMM1 -> X [M][H] (2-D map, box 64 x 128); GEMM2 -> Y [M][F] (2-D map, box 64 x 128).
 // B: GEMM1 -> W1p [k][f][H] (3-D map, box 64 x BN x 1); GEMM2 -> W2p [k][H][f] (same box).
 // MN: both operands M-/N-contiguous (the weight-gradient GEMMs, reduction over tokens):
@@ -569,6 +589,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // The set-up above overlaps the previous kernel's tail; global memory only from here on.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------- TMA producer
@@ -688,6 +711,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int q = warp & 3;  // TMEM lanes [32q, 32q+32) = tile rows this warp may read
         const int part = (warp - 2) >> 2;  // which share of the columns
         uint32_t acc = 0, acc_phase = 0;
+        prefetch_tile_bias<MODE, BN>(args, blockIdx.x, part);
         for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
             int m_blk, n_blk;
             decode_tile(args, t, m_blk, n_blk);

@@ -105,6 +105,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     ptx::cluster_sync();  // barriers of both CTAs initialised, tensor memory allocated
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // The set-up above overlaps the previous kernel's tail; global memory only from here on.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------- TMA producer (both CTAs)
@@ -234,6 +237,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         const int ew = warp - 2;  // epilogue warp index: its arrival counter in a split tile
         WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
         int t, kb0, kb1;
+        {
+            WorkCursor first = cur;
+            if (work_next(args.sk_first, args.kb_tile, num_pairs, first, t, kb0, kb1))
+                prefetch_tile_bias<MODE, kPairBN>(args, t, part);
+        }
         while (work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
             int m_blk, n_blk;
             decode_tile(args, t, m_blk, n_blk);
