@@ -21,7 +21,8 @@ output projection, AI大模型分布式训练 §2.3): column-parallel X W + b, a
 sum_i X_i W_i + b.
 The backward pass of the block (dX as a sum over shards; dW1, db1, dW2, db2).
 The gated variant (gate_up_proj column-parallel, down_proj row-parallel: 大模型分布式优化技术（一）
-§5.1, AI大模型分布式训练 §6.1) replaces GeLU(X W1 + b1) by SiLU(X Wg + bg) * (X Wu + bu).
+§5.1, AI大模型分布式训练 §6.1) replaces GeLU(X W1 + b1) by SiLU(X Wg + bg) * (X Wu + bu); its
+backward pass gives dX (a sum over shards of the gate and up parts), dWg, dbg, dWu, dbu, dW2, db2.
 
 Pins (tests/test_oracle.py): identity-activation case against numpy float64 matmul,
 GeLU values from the normal-CDF table and scipy's ndtr, the odd-part identity
@@ -80,6 +81,11 @@ class Oracle:
         lib.oracle_backward_f64.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp,
                                             vp, vp]
         lib.oracle_backward_f64.restype = ctypes.c_int
+        lib.oracle_silu_grad.argtypes = [ctypes.c_double]
+        lib.oracle_silu_grad.restype = ctypes.c_double
+        lib.oracle_swiglu_backward_f64.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                                   vp, vp, vp, vp, vp, vp, vp]
+        lib.oracle_swiglu_backward_f64.restype = ctypes.c_int
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ctypes.c_int
         self.lib = lib
@@ -223,6 +229,29 @@ class Oracle:
             raise ValueError("oracle rejected its arguments")
         return out
 
+    def silu_grad(self, g: float) -> float:
+        return float(self.lib.oracle_silu_grad(float(g)))
+
+    def swiglu_backward(self, X, Wg, bg, Wu, bu, W2, dZ, k: int):
+        """Gradients of the gated block for upstream dZ [M, H]: dict of dX [M,H], dWg [H,F],
+        dbg [F], dWu [H,F], dbu [F], dW2 [F,H], db2 [H] (fp64)."""
+        X, Wg, bg, Wu, bu, W2, dZ = (_u16(a) for a in (X, Wg, bg, Wu, bu, W2, dZ))
+        M, H = X.shape
+        F = Wg.shape[1]
+        if (Wg.shape != (H, F) or Wu.shape != (H, F) or W2.shape != (F, H) or bg.shape != (F,)
+                or bu.shape != (F,) or dZ.shape != (M, H)):
+            raise ValueError("shape mismatch")
+        out = {"dX": np.empty((M, H)), "dWg": np.empty((H, F)), "dbg": np.empty(F),
+               "dWu": np.empty((H, F)), "dbu": np.empty(F), "dW2": np.empty((F, H)),
+               "db2": np.empty(H)}
+        rc = self.lib.oracle_swiglu_backward_f64(
+            X.ctypes.data, Wg.ctypes.data, bg.ctypes.data, Wu.ctypes.data, bu.ctypes.data,
+            W2.ctypes.data, dZ.ctypes.data, M, H, F, k,
+            *(out[n].ctypes.data for n in ("dX", "dWg", "dbg", "dWu", "dbu", "dW2", "db2")))
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return out
+
 
 def _u16(a) -> np.ndarray:
     a = np.ascontiguousarray(a)
@@ -293,3 +322,11 @@ def gelu_grad(a: float) -> float:
 
 def backward(X, W1, b1, W2, dZ, k: int):
     return default().backward(X, W1, b1, W2, dZ, k)
+
+
+def silu_grad(g: float) -> float:
+    return default().silu_grad(g)
+
+
+def swiglu_backward(X, Wg, bg, Wu, bu, W2, dZ, k: int):
+    return default().swiglu_backward(X, Wg, bg, Wu, bu, W2, dZ, k)

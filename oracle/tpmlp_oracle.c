@@ -489,6 +489,133 @@ int oracle_backward_f64(const uint16_t *X, const uint16_t *W1, const uint16_t *b
     return 0;
 }
 
+/*
+ * Backward pass of the gated block. The pages split gate_up_proj by columns and down_proj by
+ * rows (大模型分布式优化技术（一） §5.1; AI大模型分布式训练 §6.1), and the backward pass repeats
+ * the forward's split with one more sum over shards (分布式训练系列第四篇 §4.2-4.3; AI大模型分布式训练
+ * §2.4). Given dZ [M, H] of Z = sum_i (SiLU(G_i) * U_i) W2_i + b2, by the chain rule:
+ *   G   = X Wg + bg,   U = X Wu + bu                     pre-activations [M, F]
+ *   dY  = dZ W2^T                                        per column shard [M, F]
+ *   dU  = dY * SiLU(G)
+ *   dG  = dY * U * SiLU'(G),  SiLU'(g) = s (1 + g (1 - s)),  s = 1 / (1 + exp(-g))
+ *   dX  = sum_i (dG_i Wg_i^T + dU_i Wu_i^T)             (the backward All-Reduce)
+ *   dWg = X^T dG, dbg = sum_m dG[m, :];  dWu = X^T dU, dbu = sum_m dU[m, :]
+ *   dW2 = Y^T dZ, db2 = sum_m dZ[m, :],  Y = SiLU(G) * U
+ * Sums in index order; for dX, shard i's gate part then its up part, then the sum over
+ * shards. All outputs are double; dWg, dWu [H][F], dW2 [F][H]; any output may be NULL.
+ */
+double oracle_silu_grad(double g) {
+    const double s = 1.0 / (1.0 + exp(-g));
+    return s * (1.0 + g * (1.0 - s));
+}
+
+int oracle_swiglu_backward_f64(const uint16_t *X, const uint16_t *Wg, const uint16_t *bg,
+                               const uint16_t *Wu, const uint16_t *bu, const uint16_t *W2,
+                               const uint16_t *dZ, int64_t M, int64_t H, int64_t F, int32_t k,
+                               double *dX, double *dWg, double *dbg, double *dWu, double *dbu,
+                               double *dW2, double *db2) {
+    if (!X || !Wg || !bg || !Wu || !bu || !W2 || !dZ || M <= 0 || H <= 0 || F <= 0 || k <= 0)
+        return -1;
+    if (F % k != 0) return -1;
+    const int64_t f = F / k;
+    const size_t n = (size_t)(M * F);
+    double *G = (double *)malloc(sizeof(double) * n);
+    double *U = (double *)malloc(sizeof(double) * n);
+    double *dG = (double *)malloc(sizeof(double) * n);
+    double *dU = (double *)malloc(sizeof(double) * n);
+    if (!G || !U || !dG || !dU) {
+        free(G);
+        free(U);
+        free(dG);
+        free(dU);
+        return -1;
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        double *g = G + m * F, *u = U + m * F;
+        for (int64_t j = 0; j < F; ++j) g[j] = u[j] = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            const double xh = widen_bf16(X[m * H + h]);
+            for (int64_t j = 0; j < F; ++j) {
+                g[j] += xh * widen_bf16(Wg[h * F + j]);
+                u[j] += xh * widen_bf16(Wu[h * F + j]);
+            }
+        }
+        for (int64_t j = 0; j < F; ++j) {
+            g[j] += widen_bf16(bg[j]);
+            u[j] += widen_bf16(bu[j]);
+        }
+        for (int64_t j = 0; j < F; ++j) {
+            double dy = 0.0;
+            for (int64_t c = 0; c < H; ++c) dy += widen_bf16(dZ[m * H + c]) * widen_bf16(W2[j * H + c]);
+            dU[m * F + j] = dy * oracle_silu(g[j]);
+            dG[m * F + j] = dy * u[j] * oracle_silu_grad(g[j]);
+        }
+    }
+    if (dX) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t m = 0; m < M; ++m) {
+            for (int64_t h = 0; h < H; ++h) {
+                double total = 0.0;
+                for (int32_t i = 0; i < k; ++i) {
+                    double part = 0.0;
+                    for (int64_t jj = 0; jj < f; ++jj)
+                        part += dG[m * F + i * f + jj] * widen_bf16(Wg[h * F + i * f + jj]);
+                    for (int64_t jj = 0; jj < f; ++jj)
+                        part += dU[m * F + i * f + jj] * widen_bf16(Wu[h * F + i * f + jj]);
+                    total += part;
+                }
+                dX[m * H + h] = total;
+            }
+        }
+    }
+    if (dWg || dWu) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t j = 0; j < F; ++j) {
+                double ag = 0.0, au = 0.0;
+                for (int64_t m = 0; m < M; ++m) {
+                    const double xh = widen_bf16(X[m * H + h]);
+                    ag += xh * dG[m * F + j];
+                    au += xh * dU[m * F + j];
+                }
+                if (dWg) dWg[h * F + j] = ag;
+                if (dWu) dWu[h * F + j] = au;
+            }
+    }
+    for (int64_t j = 0; j < F && (dbg || dbu); ++j) {
+        double ag = 0.0, au = 0.0;
+        for (int64_t m = 0; m < M; ++m) {
+            ag += dG[m * F + j];
+            au += dU[m * F + j];
+        }
+        if (dbg) dbg[j] = ag;
+        if (dbu) dbu[j] = au;
+    }
+    if (dW2) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t j = 0; j < F; ++j)
+            for (int64_t c = 0; c < H; ++c) {
+                double acc = 0.0;
+                for (int64_t m = 0; m < M; ++m)
+                    acc += oracle_silu(G[m * F + j]) * U[m * F + j] * widen_bf16(dZ[m * H + c]);
+                dW2[j * H + c] = acc;
+            }
+    }
+    if (db2) {
+        for (int64_t c = 0; c < H; ++c) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += widen_bf16(dZ[m * H + c]);
+            db2[c] = acc;
+        }
+    }
+    free(G);
+    free(U);
+    free(dG);
+    free(dU);
+    return 0;
+}
+
 int oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -396,7 +396,35 @@ def pin_backward_matches_torch_autograd(orc):
             assert _rel_fro(g[name], ref.numpy()) <= 1e-12, (k, name, _rel_fro(g[name], ref.numpy()))
 
 
-BACKWARD_PINS = [pin_gelu_grad_finite_difference, pin_backward_matches_torch_autograd]
+def pin_silu_grad_finite_difference(orc):
+    """SiLU'(g) against central differences of the oracle's own fp64 SiLU."""
+    h = 1e-5
+    for g in np.linspace(-12.0, 12.0, 241):
+        fd = (orc.silu(float(g) + h) - orc.silu(float(g) - h)) / (2 * h)
+        assert abs(orc.silu_grad(float(g)) - fd) <= 1e-9, g
+
+
+def pin_swiglu_backward_matches_torch_autograd(orc):
+    """All seven gradients of the gated block against torch.autograd in float64."""
+    import torch
+    M, H, F = 11, 64, 256
+    d = synth.make_swiglu_inputs(H, F, M, 73)
+    dZ = synth.normal_bf16(73, 60, (M, H), 1.0)
+    t = {n: torch.from_numpy(synth.bf16_to_f64(v)).requires_grad_(True) for n, v in d.items()}
+    Y = torch.nn.functional.silu(t["X"] @ t["Wg"] + t["bg"]) * (t["X"] @ t["Wu"] + t["bu"])
+    Z = Y @ t["W2"] + t["b2"]
+    Z.backward(torch.from_numpy(synth.bf16_to_f64(dZ)))
+    for k in (1, 4):
+        g = orc.swiglu_backward(d["X"], d["Wg"], d["bg"], d["Wu"], d["bu"], d["W2"], dZ, k)
+        for name, ref in (("dX", t["X"].grad), ("dWg", t["Wg"].grad), ("dbg", t["bg"].grad),
+                          ("dWu", t["Wu"].grad), ("dbu", t["bu"].grad), ("dW2", t["W2"].grad),
+                          ("db2", t["b2"].grad)):
+            err = _rel_fro(g[name], ref.numpy())
+            assert err <= 1e-12, (k, name, err)
+
+
+BACKWARD_PINS = [pin_gelu_grad_finite_difference, pin_backward_matches_torch_autograd,
+                 pin_silu_grad_finite_difference, pin_swiglu_backward_matches_torch_autograd]
 
 SWIGLU_PINS = [pin_silu_table_and_expit, pin_silu_odd_part, pin_swiglu_bruteforce_golden,
                pin_swiglu_matches_numpy, pin_swiglu_gate_only, pin_swiglu_k_invariance]

@@ -62,6 +62,18 @@ MUTANTS = {
     "backward_dw2_uses_preactivation": ("acc += oracle_gelu(A[m * F + j]) * widen_bf16(dZ[m * H + n]);",
                                         "acc += A[m * F + j] * widen_bf16(dZ[m * H + n]);"),
     "backward_dy_transposed_w2": ("widen_bf16(W2[j * H + n]);", "widen_bf16(W2[n * H + j]);"),
+    "silu_grad_sigmoid_only": ("return s * (1.0 + g * (1.0 - s));", "return s;"),
+    "silu_grad_sign_flip": ("return s * (1.0 + g * (1.0 - s));", "return s * (1.0 - g * (1.0 - s));"),
+    "swiglu_backward_dg_missing_up": ("dG[m * F + j] = dy * u[j] * oracle_silu_grad(g[j]);",
+                                      "dG[m * F + j] = dy * oracle_silu_grad(g[j]);"),
+    "swiglu_backward_du_uses_sigmoid": ("dU[m * F + j] = dy * oracle_silu(g[j]);",
+                                        "dU[m * F + j] = dy / (1.0 + exp(-g[j]));"),
+    "swiglu_backward_dx_gate_only": (
+        "part += dU[m * F + i * f + jj] * widen_bf16(Wu[h * F + i * f + jj]);", "part += 0.0;"),
+    "swiglu_backward_dw2_without_up": (
+        "acc += oracle_silu(G[m * F + j]) * U[m * F + j] * widen_bf16(dZ[m * H + c]);",
+        "acc += oracle_silu(G[m * F + j]) * widen_bf16(dZ[m * H + c]);"),
+    "swiglu_backward_up_bias_dropped": ("u[j] += widen_bf16(bu[j]);", ""),
     "activation_dropped": ("acc[jj] = (act == ORACLE_ACT_GELU) ? oracle_gelu(a) : a;",
                               "acc[jj] = a;"),
 }
