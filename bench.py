@@ -582,7 +582,10 @@ def run_gpu_linear(args, w: synth.Workload):
 def run_gpu_train(args, w: synth.Workload):
     """One training step of the block: tpmlp_forward_train (keeps Y and the pre-activation)
     then tpmlp_backward (dA, dX summed over shards in the accumulator, dW1, dW2, db1, db2).
-    FLOPs: forward 4 M H F, backward 8 M H F (four GEMMs of 2 M H F each)."""
+    FLOPs: forward 4 M H F, backward 8 M H F (four GEMMs of 2 M H F each).
+    Gated block (--variant train-swiglu): tpmlp_forward_train (keeps Y, G and U) then
+    tpmlp_backward_swiglu; FLOPs: forward 6 M H F, backward 12 M H F (dY 2, dX 4 over the
+    gate and up shards, dWg 2, dWu 2, dW2 2)."""
     import torch
     import tensor_transformer_mlp_tmem_gb300 as tp
 
@@ -594,19 +597,21 @@ def run_gpu_train(args, w: synth.Workload):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
-    d = synth.workload_inputs(w)
+    gated = args.variant == "train-swiglu"
+    d = synth.make_swiglu_inputs(w.H, w.F, w.M, w.seed) if gated else synth.workload_inputs(w)
     dZh = synth.normal_bf16(w.seed, 60, (w.M, w.H), 1.0)
 
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
     X = to_dev(d["X"]).view(w.B, w.S, w.H)
-    W1, W2 = to_dev(d["W1"]), to_dev(d["W2"])
+    W1 = to_dev(d["Wg"] if gated else d["W1"])
+    W2 = to_dev(d["W2"])
     dZ = to_dev(dZh).view(w.B, w.S, w.H)
     M = w.M
     Z = torch.empty_like(X)
     Ys = torch.empty((M, w.F), dtype=torch.bfloat16, device=dev)
-    As = torch.empty_like(Ys)
+    As = torch.empty((M, 2 * w.F if gated else w.F), dtype=torch.bfloat16, device=dev)
     dX = torch.empty_like(X)
     f32 = torch.float32
     dW1 = torch.empty((w.H, w.F), dtype=f32, device=dev)
@@ -615,8 +620,14 @@ def run_gpu_train(args, w: synth.Workload):
     db2 = torch.empty((w.H,), dtype=f32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    mlp = tp.TPMLP(w.H, w.F, w.k)
-    mlp.pack(W1, to_dev(d["b1"]), W2, to_dev(d["b2"]))
+    mlp = tp.TPMLP(w.H, w.F, w.k, swiglu=gated)
+    if gated:
+        Wu = to_dev(d["Wu"])
+        dWu = torch.empty_like(dW1)
+        dbu = torch.empty_like(db1)
+        mlp.pack_swiglu(W1, to_dev(d["bg"]), Wu, to_dev(d["bu"]), W2, to_dev(d["b2"]))
+    else:
+        mlp.pack(W1, to_dev(d["b1"]), W2, to_dev(d["b2"]))
     mlp.reserve(M)
 
     def step(ev=None):
@@ -625,7 +636,12 @@ def run_gpu_train(args, w: synth.Workload):
         tp.tpmlp_forward_train(mlp.ctx, X, w.B, w.S, Z, Ys, As, stream)
         if ev is not None:
             ev[1].record(stream)
-        tp.tpmlp_backward(mlp.ctx, dZ, X, Ys, As, W1, W2, w.B, w.S, dX, dW1, db1, dW2, db2, stream)
+        if gated:
+            tp.tpmlp_backward_swiglu(mlp.ctx, dZ, X, Ys, As, W1, Wu, W2, w.B, w.S, dX, dW1, db1,
+                                     dWu, dbu, dW2, db2, stream)
+        else:
+            tp.tpmlp_backward(mlp.ctx, dZ, X, Ys, As, W1, W2, w.B, w.S, dX, dW1, db1, dW2, db2,
+                              stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -658,11 +674,11 @@ def run_gpu_train(args, w: synth.Workload):
     bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     ms = fwd + bwd
     ms, fwd, bwd = max_over_ranks([ms, fwd, bwd], pg, dev)
-    flops = 12 * M * w.H * w.F
+    flops = (18 if gated else 12) * M * w.H * w.F
     peaks, peak_src = load_peaks()
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     value = whole_job_tflops(world, flops, ms)
-    bwd_tf = 8 * M * w.H * w.F / (bwd * 1e-3) / 1e12
+    bwd_tf = (12 if gated else 8) * M * w.H * w.F / (bwd * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -671,14 +687,18 @@ def run_gpu_train(args, w: synth.Workload):
         "kernel_ms": {"forward_train": fwd, "backward": bwd},
         "config": workload_config(w, {"parallelism": "replicas" if world > 1 else "single GPU",
                                       "flops_per_step": flops,
-                                      "step": "forward_train + backward (dX, dW1, db1, dW2, db2)"},
-                                  variant="gelu"),
-        "roofline": {"bound": "tensor", "kernel": "backward (dA, dX, dW1, dW2 GEMMs + bias sums)",
+                                      "step": ("forward_train + backward_swiglu (dX, dWg, dbg, dWu, "
+                                               "dbu, dW2, db2)") if gated else
+                                              "forward_train + backward (dX, dW1, db1, dW2, db2)"},
+                                  variant="swiglu" if gated else "gelu"),
+        "roofline": {"bound": "tensor",
+                     "kernel": ("backward (dG/dU, dX, dWg, dWu, dW2 GEMMs + bias sums)" if gated
+                                else "backward (dA, dX, dW1, dW2 GEMMs + bias sums)"),
                      "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
                      "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None},
         "gpu_launches": launches, "clocks": clk,
     }
-    line["config"]["variant"] = "train"
+    line["config"]["variant"] = args.variant
     mlp.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -718,13 +738,14 @@ def main():
     ap.add_argument("--workload", default="7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--k", type=int, default=None, help="override the shard count")
     ap.add_argument("--variant", default="gelu",
-                    choices=["gelu", "swiglu", "block", "outproj", "qkv", "train"],
+                    choices=["gelu", "swiglu", "block", "outproj", "qkv", "train", "train-swiglu"],
                     help="gelu: the block of the pages' Megatron figure; swiglu: the gated block; "
                          "block: Z = X + MLP(LayerNorm(X)) (LayerNorm kernel + the GeLU block "
                          "with the residual add in the second GEMM's epilogue); outproj / qkv: "
                          "the tensor-parallel attention's output (row-parallel) and Q/K/V "
                          "(column-parallel) projections on the workload's shape; train: the "
-                         "training forward plus the backward pass")
+                         "training forward plus the backward pass; train-swiglu: the same for "
+                         "the gated block")
     ap.add_argument("--impl", default="tpmlp", choices=["tpmlp", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--cpu-max-rows", type=int, default=4096)
@@ -746,12 +767,12 @@ def main():
     if args.k is not None:
         w = synth.Workload(w.name, w.B, w.S, w.H, w.F, args.k, w.seed)
     if args.impl == "reference":
-        if args.variant in ("outproj", "qkv", "train"):
+        if args.variant in ("outproj", "qkv", "train", "train-swiglu"):
             ap.error("the reference arm covers the MLP variants")
         return run_reference(args, w)
     if args.variant in ("outproj", "qkv"):
         return run_gpu_linear(args, w)
-    if args.variant == "train":
+    if args.variant in ("train", "train-swiglu"):
         return run_gpu_train(args, w)
     return run_gpu(args, w)
 

@@ -256,9 +256,11 @@ TPMLP_API int tpmlp_gemm2_residual(tpmlp_ctx *ctx, const void *Y, int64_t M, voi
 /*
  * Training forward pass of the block: tpmlp_forward, and the activations the backward pass
  * needs are kept in the caller's buffers.
- *   Ysave  device bf16 [B*S, F]: Y = GeLU(X W1 + b1) (the first GEMM's output)
- *   Asave  device bf16 [B*S, F]: the pre-activation A = X W1 + b1
- * GeLU blocks only (not TPMLP_FLAG_SWIGLU). Errors: as tpmlp_forward.
+ *   Ysave  device bf16 [B*S, F]: Y = GeLU(X W1 + b1) (the first GEMM's output); in a
+ *          TPMLP_FLAG_SWIGLU context Y = SiLU(G) * U
+ *   Asave  device bf16 [B*S, F]: the pre-activation A = X W1 + b1; in a TPMLP_FLAG_SWIGLU
+ *          context [B*S, 2F]: G = X Wg + bg in columns [0, F) and U = X Wu + bu in [F, 2F)
+ * Errors: as tpmlp_forward.
  */
 TPMLP_API int tpmlp_forward_train(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z,
                                   void *Ysave, void *Asave, void *stream);
@@ -282,6 +284,33 @@ TPMLP_API int tpmlp_backward(tpmlp_ctx *ctx, const void *dZ, const void *X, cons
                              const void *Asave, const void *W1, const void *W2, int64_t B,
                              int64_t S, void *dX, void *dW1, void *db1, void *dW2, void *db2,
                              void *stream);
+
+/*
+ * Backward pass of the gated (TPMLP_FLAG_SWIGLU) block, Z = sum_i (SiLU(G_i) * U_i) W2_i + b2
+ * with G = X Wg + bg and U = X Wu + bu. gate_up_proj is column-parallel and down_proj
+ * row-parallel (大模型分布式优化技术（一） §5.1; AI大模型分布式训练 §6.1), and the backward pass
+ * repeats the split with one more sum over shards (分布式训练系列第四篇 §4.2-4.3). By the chain rule:
+ *   dY  = dZ W2^T                      per column shard
+ *   dU  = dY * SiLU(G),   dG = dY * U * SiLU'(G),   SiLU'(g) = s (1 + g (1 - s)), s = sigma(g)
+ *   dX  = sum_i (dG_i Wg_i^T + dU_i Wu_i^T)   the backward All-Reduce, in one accumulator
+ *                                             (the k gate shards, then the k up shards)
+ *   dWg = X^T dG,  dbg = sum over tokens of dG;  dWu = X^T dU,  dbu = sum over tokens of dU
+ *   dW2 = Y^T dZ,  db2 = sum over tokens of dZ
+ * Inputs (device): dZ bf16 [B*S, H]; X bf16 [B*S, H]; Ysave [B*S, F] and Asave [B*S, 2F]
+ * from tpmlp_forward_train on this context; Wg, Wu bf16 [H, F] and W2 bf16 [F, H]: the
+ * weights that were packed, in the caller's [in, out] layout. Outputs (device, written, not
+ * accumulated): dX [B*S, H] (bf16, or fp32 with TPMLP_FLAG_Z_FP32); dWg, dWu fp32 [H, F];
+ * dbg, dbu fp32 [F]; dW2 fp32 [F, H]; db2 fp32 [H]. dG and dU go to a context buffer of
+ * [B*S, 2F] bf16, allocated on first use and grown when B*S grows (that growth
+ * synchronises the device). Eleven launches; deterministic.
+ * Errors: INVALID_ARG (also for a context without TPMLP_FLAG_SWIGLU), NOT_PACKED,
+ * MISALIGNED, UNSUPPORTED_SHAPE, OOM, CUDA.
+ */
+TPMLP_API int tpmlp_backward_swiglu(tpmlp_ctx *ctx, const void *dZ, const void *X,
+                                    const void *Ysave, const void *Asave, const void *Wg,
+                                    const void *Wu, const void *W2, int64_t B, int64_t S,
+                                    void *dX, void *dWg, void *dbg, void *dWu, void *dbu,
+                                    void *dW2, void *db2, void *stream);
 
 /*
  * Read and clear the device status word that the kernels set when a bounded wait gives up

@@ -27,6 +27,7 @@ __all__ = [
     "tpmlp_gemm2_residual",
     "tpmlp_linear_create", "tpmlp_linear_pack", "tpmlp_linear_forward", "Linear",
     "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW", "tpmlp_forward_train", "tpmlp_backward",
+    "tpmlp_backward_swiglu",
 ]
 
 TPMLP_OK = 0
@@ -97,6 +98,8 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_linear_pack": ([vp, vp, vp, vp], ctypes.c_int),
         "tpmlp_linear_forward": ([vp, vp, i64, vp, vp], ctypes.c_int),
         "tpmlp_forward_train": ([vp, vp, i64, i64, vp, vp, vp, vp], ctypes.c_int),
+        "tpmlp_backward_swiglu": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, vp,
+                                   vp, vp, vp, vp], ctypes.c_int),
         "tpmlp_backward": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, vp],
                            ctypes.c_int),
         "tpmlp_destroy": ([vp], None),
@@ -273,6 +276,14 @@ def tpmlp_backward(ctx: int, dZ, X, Ysave, Asave, W1, W2, B: int, S: int, dX, dW
         _ptr(dW1), _ptr(db1), _ptr(dW2), _ptr(db2), _stream(stream)), "tpmlp_backward", ctx)
 
 
+def tpmlp_backward_swiglu(ctx: int, dZ, X, Ysave, Asave, Wg, Wu, W2, B: int, S: int, dX, dWg,
+                          dbg, dWu, dbu, dW2, db2, stream=None) -> None:
+    _check(load_library().tpmlp_backward_swiglu(
+        ctx, _ptr(dZ), _ptr(X), _ptr(Ysave), _ptr(Asave), _ptr(Wg), _ptr(Wu), _ptr(W2), B, S,
+        _ptr(dX), _ptr(dWg), _ptr(dbg), _ptr(dWu), _ptr(dbu), _ptr(dW2), _ptr(db2),
+        _stream(stream)), "tpmlp_backward_swiglu", ctx)
+
+
 def tpmlp_destroy(ctx) -> None:
     load_library().tpmlp_destroy(ctx)
 
@@ -379,14 +390,16 @@ class TPMLP:
         return Z
 
     def forward_train(self, X, stream=None):
-        """Returns (Z, Ysave, Asave); Ysave/Asave feed backward()."""
+        """Returns (Z, Ysave, Asave); Ysave/Asave feed backward() (backward_swiglu() for a
+        gated block, whose Asave is [M, 2F]: G then U)."""
         import torch
         B, S, H = X.shape
         self._require(X, torch.bfloat16, (B, S, self.H), "X")
         M = B * S
         Z = torch.empty((B, S, self.H), dtype=self.out_dtype(), device=X.device)
         Ys = torch.empty((M, self.F), dtype=torch.bfloat16, device=X.device)
-        As = torch.empty((M, self.F), dtype=torch.bfloat16, device=X.device)
+        As = torch.empty((M, 2 * self.F if self.swiglu else self.F), dtype=torch.bfloat16,
+                         device=X.device)
         tpmlp_forward_train(self.ctx, X, B, S, Z, Ys, As, stream)
         return Z, Ys, As
 
@@ -404,6 +417,23 @@ class TPMLP:
         db2 = torch.empty((self.H,), dtype=f32, device=dev)
         tpmlp_backward(self.ctx, dZ, X, Ysave, Asave, W1, W2, B, S, dX, dW1, db1, dW2, db2, stream)
         return dX, dW1, db1, dW2, db2
+
+    def backward_swiglu(self, dZ, X, Ysave, Asave, Wg, Wu, W2, stream=None):
+        """Gradients (dX, dWg, dbg, dWu, dbu, dW2, db2) of the gated block for upstream dZ."""
+        import torch
+        B, S, H = X.shape
+        dev = X.device
+        f32 = torch.float32
+        dX = torch.empty((B, S, self.H), dtype=self.out_dtype(), device=dev)
+        dWg = torch.empty((self.H, self.F), dtype=f32, device=dev)
+        dWu = torch.empty((self.H, self.F), dtype=f32, device=dev)
+        dbg = torch.empty((self.F,), dtype=f32, device=dev)
+        dbu = torch.empty((self.F,), dtype=f32, device=dev)
+        dW2 = torch.empty((self.F, self.H), dtype=f32, device=dev)
+        db2 = torch.empty((self.H,), dtype=f32, device=dev)
+        tpmlp_backward_swiglu(self.ctx, dZ, X, Ysave, Asave, Wg, Wu, W2, B, S, dX, dWg, dbg, dWu,
+                              dbu, dW2, db2, stream)
+        return dX, dWg, dbg, dWu, dbu, dW2, db2
 
     def reserve(self, max_tokens: int):
         tpmlp_reserve(self.ctx, max_tokens)

@@ -73,6 +73,8 @@ struct tpmlp_ctx {
     float* zeros = nullptr;        // [max(H, F)] fp32 zeros: the "no bias" of dX
     float* colsum = nullptr;       // partial column sums for the bias gradients
     int64_t colsum_floats = 0;
+    uint16_t* dgu = nullptr;       // gated backward: dG and dU, [rows][2F] bf16
+    int64_t dgu_elems = 0;
 
     // split reduction of the last tiles on CTA pairs (absent with TPMLP_FLAG_FIXED_ORDER)
     float* sk_partial = nullptr;  // [num_sms / 2 pairs][2 units][2 CTAs][128 x 256] fp32 partials
@@ -190,9 +192,11 @@ int ensure_smem_attr(tpmlp_ctx* c, Kernel kern, uint32_t smem, std::atomic<uint6
 // Launch a GEMM kernel with programmatic stream serialisation: its CTAs may be scheduled while
 // the kernel before it in the stream finishes, run their set-up (barriers, tensor memory,
 // descriptor prefetch), and wait in griddep_wait until that kernel's results are visible.
+// b2: the B map of shards [args.k2, args.k) of a second-GEMM reduction (unused otherwise).
 template <typename Kernel>
 cudaError_t launch_overlapped(Kernel kern, int grid, uint32_t smem, cudaStream_t s,
-                              const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args) {
+                              const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
+                              const GemmArgs& args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(tpmlp::kNumThreads, 1, 1);
@@ -203,18 +207,18 @@ cudaError_t launch_overlapped(Kernel kern, int grid, uint32_t smem, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, b, args);
+    return cudaLaunchKernelEx(&cfg, kern, a, b, b2, args);
 }
 
 template <int BN, int STAGES, Mode MODE, bool F32, bool MN = false>
 int launch_gemm(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
-                cudaStream_t s) {
+                cudaStream_t s, const CUtensorMap* b2 = nullptr) {
     auto kern = tpmlp::tpmlp_gemm_kernel<BN, STAGES, MODE, F32, MN>;
     constexpr uint32_t smem = tpmlp::GemmSmem<BN, STAGES>::kTotal;
     static std::atomic<uint64_t> attr_done{0};
     if (int rc = ensure_smem_attr(c, kern, smem, attr_done)) return rc;
     const int grid = std::min(args.num_tiles, c->num_sms);
-    TPMLP_CUDA(c, launch_overlapped(kern, grid, smem, s, a, b, args));
+    TPMLP_CUDA(c, launch_overlapped(kern, grid, smem, s, a, b, b2 ? *b2 : b, args));
     ++c->launches;
     return TPMLP_OK;
 }
@@ -222,14 +226,14 @@ int launch_gemm(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
 // Stage depth per tile width: 192 KB of operand ring in every case.
 template <Mode MODE, bool F32>
 int dispatch_gemm(tpmlp_ctx* c, int bn, const CUtensorMap& a, const CUtensorMap& b,
-                  const GemmArgs& args, cudaStream_t s) {
+                  const GemmArgs& args, cudaStream_t s, const CUtensorMap* b2 = nullptr) {
     switch (bn) {
-        case 256: return launch_gemm<256, TPMLP_STAGES_256, MODE, F32>(c, a, b, args, s);
-        case 128: return launch_gemm<128, 6, MODE, F32>(c, a, b, args, s);
+        case 256: return launch_gemm<256, TPMLP_STAGES_256, MODE, F32>(c, a, b, args, s, b2);
+        case 128: return launch_gemm<128, 6, MODE, F32>(c, a, b, args, s, b2);
         default:
             // the gated layer's tiles hold 2 x 64 columns at least
-            if constexpr (MODE == Mode::kGemm1Gated) return TPMLP_ERR_UNSUPPORTED_SHAPE;
-            else return launch_gemm<64, 8, MODE, F32>(c, a, b, args, s);
+            if constexpr (tpmlp::is_gated(MODE)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+            else return launch_gemm<64, 8, MODE, F32>(c, a, b, args, s, b2);
     }
 }
 
@@ -294,7 +298,7 @@ void plan_split(tpmlp_ctx* c, GemmArgs& a, int pairs, cudaStream_t s) {
 
 template <int STAGES, int NUM_ACC, Mode MODE, bool F32, bool MN = false>
 int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
-                cudaStream_t s) {
+                cudaStream_t s, const CUtensorMap* b2 = nullptr) {
     auto kern = tpmlp::tpmlp_gemm_pair_kernel<STAGES, NUM_ACC, MODE, F32, MN>;
     constexpr uint32_t smem = tpmlp::PairSmem<STAGES, NUM_ACC>::kTotal;
     static_assert(smem <= 232448, "shared memory per CTA");
@@ -310,7 +314,7 @@ int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
     const int pairs = std::min(args.num_tiles, resident);
     GemmArgs run = args;
     plan_split(c, run, pairs, s);
-    TPMLP_CUDA(c, launch_overlapped(kern, 2 * pairs, smem, s, a, b, run));
+    TPMLP_CUDA(c, launch_overlapped(kern, 2 * pairs, smem, s, a, b, b2 ? *b2 : b, run));
     ++c->launches;
     return TPMLP_OK;
 }
@@ -326,6 +330,9 @@ GemmArgs base_args(const tpmlp_ctx* c, int64_t M, int ldo, int bm, int bn, int g
     a.num_tiles = a.m_blocks * a.n_blocks;
     a.group_m = group_m;
     a.status = c->status;
+    a.ldo2 = ldo;
+    a.half = 0;
+    a.k2 = c->k;
     a.sk_first = a.num_tiles;  // no split (set per launch by plan_split)
     return a;
 }
@@ -373,6 +380,16 @@ int run_gemm1(tpmlp_ctx* c, const void* X, int64_t M, void* Y, cudaStream_t s,
         a.f = static_cast<int>(2 * c->f);
         a.n_blocks = static_cast<int>(2 * c->F / tile_rows_b);
         a.num_tiles = a.m_blocks * a.n_blocks;
+        if (A_save) {
+            // training forward: also keep G and U, [M][2F] (U from column F on)
+            a.out2 = A_save;
+            a.ldo2 = static_cast<int>(2 * c->F);
+            a.half = static_cast<int>(c->F);
+            if (pair)
+                return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1GatedTrain, false>(
+                    c, tmX, c->tmW1_pair, a, s);
+            return dispatch_gemm<Mode::kGemm1GatedTrain, false>(c, c->bn1, tmX, c->tmW1, a, s);
+        }
         if (pair)
             return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm1Gated, false>(
                 c, tmX, c->tmW1_pair, a, s);
@@ -674,20 +691,23 @@ int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, vo
 int create_context(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t flags, int kind);
 
 // bf16 [rows][cols] map with a 64 x 64 box: an M-contiguous operand of a weight-gradient GEMM
-// (inner index = output row or column, outer index = token).
-int token_major_map(tpmlp_ctx* c, CUtensorMap* map, const void* ptr, int64_t tokens, int64_t cols) {
+// (inner index = output row or column, outer index = token). ld: row pitch in elements
+// (0: cols).
+int token_major_map(tpmlp_ctx* c, CUtensorMap* map, const void* ptr, int64_t tokens, int64_t cols,
+                    int64_t ld = 0) {
     const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(tokens)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(cols) * 2};
+    const uint64_t strides[1] = {static_cast<uint64_t>(ld ? ld : cols) * 2};
     const uint32_t box[2] = {64, 64};
     return encode_map(c, map, ptr, 2, dims, strides, box);
 }
 
-// fp32 out[R][C] = sum over tokens of Aop[t][r] * Bop[t][c]  (A = X or Y, B = dA or dZ)
+// fp32 out[R][C] = sum over tokens of Aop[t][r] * Bop[t][c]  (A = X or Y, B = dA or dZ);
+// ldb: row pitch of Bop in elements (0: C).
 int run_weight_grad(tpmlp_ctx* c, const void* Aop, int64_t R, const void* Bop, int64_t C,
-                    int64_t tokens, float* out, cudaStream_t s) {
+                    int64_t tokens, float* out, cudaStream_t s, int64_t ldb = 0) {
     CUtensorMap ta, tb;
     int rc = token_major_map(c, &ta, Aop, tokens, R);
-    if (rc || (rc = token_major_map(c, &tb, Bop, tokens, C))) return rc;
+    if (rc || (rc = token_major_map(c, &tb, Bop, tokens, C, ldb))) return rc;
     const int bn = pick_bn(C);
     const bool pair = bn == 256 && !(c->flags & TPMLP_FLAG_SINGLE_SM);
     GemmArgs a{};
@@ -695,6 +715,7 @@ int run_weight_grad(tpmlp_ctx* c, const void* Aop, int64_t R, const void* Bop, i
     a.ldo = static_cast<int>(C);
     a.f = static_cast<int>(C);
     a.k = 1;
+    a.k2 = 1;
     a.kb_tile = static_cast<int>((tokens + tpmlp::kBK - 1) / tpmlp::kBK);
     a.kb_shard = a.kb_tile;
     const int bm = pair ? tpmlp::kPairBM : tpmlp::kBM;
@@ -714,8 +735,10 @@ int run_weight_grad(tpmlp_ctx* c, const void* Aop, int64_t R, const void* Bop, i
     }
 }
 
-// out[c] = sum over the M rows of in[m][c] (bf16 in, fp32 out), deterministic.
-int run_colsum(tpmlp_ctx* c, const void* in, int64_t M, int64_t C, float* out, cudaStream_t s) {
+// out[c] = sum over the M rows of in[m][c] (bf16 in, row pitch ld elements (0: C), fp32 out),
+// deterministic.
+int run_colsum(tpmlp_ctx* c, const void* in, int64_t M, int64_t C, float* out, cudaStream_t s,
+               int64_t ld = 0) {
     const int splits = static_cast<int>(std::min<int64_t>((M + 255) / 256, 128));
     const int rows_per_split = static_cast<int>((M + splits - 1) / splits);
     const int64_t need = static_cast<int64_t>(splits) * C;
@@ -729,8 +752,8 @@ int run_colsum(tpmlp_ctx* c, const void* in, int64_t M, int64_t C, float* out, c
     }
     dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(splits));
     tpmlp::colsum_partial_kernel<<<grid, tpmlp::kColsumThreads, 0, s>>>(
-        static_cast<const uint16_t*>(in), static_cast<int>(M), static_cast<int>(C), rows_per_split,
-        c->colsum);
+        static_cast<const uint16_t*>(in), static_cast<int>(M), static_cast<int>(C),
+        static_cast<int>(ld ? ld : C), rows_per_split, c->colsum);
     TPMLP_CUDA(c, cudaGetLastError());
     tpmlp::colsum_final_kernel<<<static_cast<unsigned>((C + 255) / 256), 256, 0, s>>>(
         c->colsum, splits, static_cast<int>(C), out);
@@ -1064,7 +1087,6 @@ int tpmlp_forward_train(tpmlp_ctx* c, const void* X, int64_t B, int64_t S, void*
                         void* Asave, void* stream) {
     int rc = check_ctx(c);
     if (rc) return rc;
-    if (c->gated) return TPMLP_ERR_INVALID_ARG;
     if ((rc = check_tokens(B, S))) return rc;
     const int64_t M = B * S;
     if (M == 0) return TPMLP_OK;
@@ -1162,6 +1184,116 @@ int tpmlp_backward(tpmlp_ctx* c, const void* dZ, const void* X, const void* Ysav
     return run_colsum(c, dZ, M, c->H, static_cast<float*>(db2), s);
 }
 
+int tpmlp_backward_swiglu(tpmlp_ctx* c, const void* dZ, const void* X, const void* Ysave,
+                          const void* Asave, const void* Wg, const void* Wu, const void* W2,
+                          int64_t B, int64_t S, void* dX, void* dWg, void* dbg, void* dWu,
+                          void* dbu, void* dW2, void* db2, void* stream) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (!c->gated) return TPMLP_ERR_INVALID_ARG;
+    if ((rc = check_tokens(B, S))) return rc;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if (!dZ || !X || !Ysave || !Asave || !Wg || !Wu || !W2 || !dX || !dWg || !dbg || !dWu ||
+        !dbu || !dW2 || !db2)
+        return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    for (const void* p : {dZ, X, Ysave, Asave, Wg, Wu, W2, static_cast<const void*>(dX),
+                          static_cast<const void*>(dWg), static_cast<const void*>(dbg),
+                          static_cast<const void*>(dWu), static_cast<const void*>(dbu),
+                          static_cast<const void*>(dW2), static_cast<const void*>(db2)})
+        if (!aligned16(p)) return TPMLP_ERR_MISALIGNED;
+    const int64_t F = c->F, H = c->H, f = c->f;
+    // dG and dU, [M][2F] (dU from column F on), in the context's gradient buffer
+    if (M * 2 * F > c->dgu_elems) {
+        TPMLP_CUDA(c, cudaDeviceSynchronize());  // the old buffer may still be in use
+        cudaFree(c->dgu);
+        c->dgu = nullptr;
+        c->dgu_elems = 0;
+        const int64_t rows = ((M + tpmlp::kBM - 1) / tpmlp::kBM) * tpmlp::kBM;
+        TPMLP_CUDA(c, cudaMalloc(&c->dgu, static_cast<size_t>(rows * 2 * F) * 2));
+        c->dgu_elems = rows * 2 * F;
+    }
+    if (!c->zeros) {
+        const size_t n = static_cast<size_t>(std::max(H, F));
+        TPMLP_CUDA(c, cudaMalloc(&c->zeros, n * 4));
+        TPMLP_CUDA(c, cudaMemset(c->zeros, 0, n * 4));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The non-gated context's tile choices: the pair kernel where the output width allows.
+    const bool single = (c->flags & TPMLP_FLAG_SINGLE_SM) != 0;
+    const int bn_f = pick_bn(f), bn_h = pick_bn(H);
+    const bool pair_f = bn_f == 256 && !single, pair_h = bn_h == 256 && !single;
+
+    // (1) dY = dZ W2^T per column shard of W2 [F][H] (K-major blocks [k][f][H]); the epilogue
+    //     turns it into dG = dY U SiLU'(G) and dU = dY SiLU(G) with the saved G, U
+    {
+        CUtensorMap tdz, tw2;
+        int r = activation_map(c, dZ, M, H, c->x_map_ptr, c->x_map_rows, c->tmX);
+        if (r) return r;
+        tdz = c->tmX;
+        const uint64_t dims[3] = {static_cast<uint64_t>(H), static_cast<uint64_t>(f),
+                                  static_cast<uint64_t>(c->k)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(H) * 2, static_cast<uint64_t>(f) * H * 2};
+        const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(pair_f ? 128 : bn_f), 1};
+        if ((r = encode_map(c, &tw2, W2, 3, dims, strides, box))) return r;
+        const int tile_n = pair_f ? tpmlp::kPairBN : bn_f;
+        GemmArgs a = base_args(c, M, static_cast<int>(2 * F), pair_f ? tpmlp::kPairBM : tpmlp::kBM,
+                               tile_n, TPMLP_GROUP_M1);
+        a.n_blocks = static_cast<int>(F / tile_n);  // output columns [0, F); rows of pitch 2F
+        a.num_tiles = a.m_blocks * a.n_blocks;
+        a.kb_tile = static_cast<int>(H / tpmlp::kBK);
+        a.kb_shard = a.kb_tile;
+        a.out = c->dgu;
+        a.residual = Asave;
+        a.half = static_cast<int>(F);
+        r = pair_f ? launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kBwdGated, false>(c, tdz, tw2, a, s)
+                   : dispatch_gemm<Mode::kBwdGated, false>(c, bn_f, tdz, tw2, a, s);
+        if (r) return r;
+    }
+    // (2) dX = sum_i (dG_i Wg_i^T + dU_i Wu_i^T): the second GEMM's shard-major reduction over
+    //     2k shards of [dG | dU] -- the gate shards read Wg [H][F] and the up shards Wu [H][F],
+    //     each as [k][H][f] blocks -- all into one accumulator
+    {
+        CUtensorMap tdgu, twg, twu;
+        const uint64_t dims[3] = {static_cast<uint64_t>(f), static_cast<uint64_t>(H),
+                                  static_cast<uint64_t>(c->k)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(F) * 2, static_cast<uint64_t>(f) * 2};
+        const uint32_t box[3] = {tpmlp::kBK, static_cast<uint32_t>(pair_h ? 128 : bn_h), 1};
+        int r = encode_map(c, &twg, Wg, 3, dims, strides, box);
+        if (r || (r = encode_map(c, &twu, Wu, 3, dims, strides, box))) return r;
+        const uint64_t adims[2] = {static_cast<uint64_t>(2 * F), static_cast<uint64_t>(M)};
+        const uint64_t astrides[1] = {static_cast<uint64_t>(2 * F) * 2};
+        const uint32_t abox[2] = {tpmlp::kBK, tpmlp::kBM};
+        if ((r = encode_map(c, &tdgu, c->dgu, 2, adims, astrides, abox))) return r;
+        GemmArgs a = base_args(c, M, static_cast<int>(H), pair_h ? tpmlp::kPairBM : tpmlp::kBM,
+                               pair_h ? tpmlp::kPairBN : bn_h, TPMLP_GROUP_M2);
+        a.k = 2 * c->k;
+        a.k2 = c->k;
+        a.kb_shard = static_cast<int>(f / tpmlp::kBK);
+        a.kb_tile = a.kb_shard * a.k;
+        a.bias = c->zeros;
+        a.out = dX;
+        const bool f32 = (c->flags & TPMLP_FLAG_Z_FP32) != 0;
+        if (pair_h)
+            r = f32 ? launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, true>(c, tdgu, twg, a, s, &twu)
+                    : launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, false>(c, tdgu, twg, a, s, &twu);
+        else
+            r = f32 ? dispatch_gemm<Mode::kGemm2, true>(c, bn_h, tdgu, twg, a, s, &twu)
+                    : dispatch_gemm<Mode::kGemm2, false>(c, bn_h, tdgu, twg, a, s, &twu);
+        if (r) return r;
+    }
+    // (3) dWg = X^T dG, dWu = X^T dU [H][F]; (4) dW2 = Y^T dZ [F][H]: reductions over tokens
+    if ((rc = run_weight_grad(c, X, H, c->dgu, F, M, static_cast<float*>(dWg), s, 2 * F))) return rc;
+    if ((rc = run_weight_grad(c, X, H, c->dgu + F, F, M, static_cast<float*>(dWu), s, 2 * F)))
+        return rc;
+    if ((rc = run_weight_grad(c, Ysave, F, dZ, H, M, static_cast<float*>(dW2), s))) return rc;
+    // (5) dbg, dbu, db2: sums over tokens
+    if ((rc = run_colsum(c, c->dgu, M, F, static_cast<float*>(dbg), s, 2 * F))) return rc;
+    if ((rc = run_colsum(c, c->dgu + F, M, F, static_cast<float*>(dbu), s, 2 * F))) return rc;
+    return run_colsum(c, dZ, M, H, static_cast<float*>(db2), s);
+}
+
 int tpmlp_get_status(tpmlp_ctx* c, void* stream, int32_t* detail) {
     if (!c) return TPMLP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1214,6 +1346,7 @@ void tpmlp_destroy(tpmlp_ctx* c) {
     cudaFree(c->Xn);
     cudaFree(c->zeros);
     cudaFree(c->colsum);
+    cudaFree(c->dgu);
     cudaFree(c->ln_gamma);
     cudaFree(c->ln_beta);
     cudaFree(c->sk_partial);

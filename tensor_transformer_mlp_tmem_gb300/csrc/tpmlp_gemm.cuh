@@ -54,15 +54,29 @@ static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
 // Backward: kGemm1Train writes Y = GeLU(acc + b1) and the pre-activation A = acc + b1;
 // kBwdDA: dA = acc * GeLU'(A) (aux = the saved A); kWeightGrad: plain fp32 acc (no bias), with
 // both operands M-contiguous (the reduction runs over tokens).
+// Gated backward: kGemm1GatedTrain is kGemm1Gated that also writes the pre-activations
+// G = gate + bg and U = up + bu (bf16) to out2; kBwdGated takes acc = dY and the saved G, U
+// (aux) and writes dG = dY U SiLU'(G) and dU = dY SiLU(G).
 enum class Mode : int {
     kGemm1 = 1, kGemm2 = 2, kGemm1Gated = 3, kGemm2Residual = 4, kGemm1Linear = 5,
-    kGemm1Train = 6, kBwdDA = 7, kWeightGrad = 8
+    kGemm1Train = 6, kBwdDA = 7, kWeightGrad = 8, kGemm1GatedTrain = 9, kBwdGated = 10
 };
 
 // Modes whose B operand is the column-sharded weight (tiles inside one shard, K = H).
 __host__ __device__ constexpr bool is_gemm1(Mode m) {
     return m == Mode::kGemm1 || m == Mode::kGemm1Gated || m == Mode::kGemm1Linear ||
-           m == Mode::kGemm1Train || m == Mode::kBwdDA;
+           m == Mode::kGemm1Train || m == Mode::kBwdDA || m == Mode::kGemm1GatedTrain ||
+           m == Mode::kBwdGated;
+}
+
+// Modes whose accumulator holds the gate and up projections of the same outputs.
+__host__ __device__ constexpr bool is_gated(Mode m) {
+    return m == Mode::kGemm1Gated || m == Mode::kGemm1GatedTrain;
+}
+
+// Modes that add a bias in the epilogue.
+__host__ __device__ constexpr bool has_bias(Mode m) {
+    return m != Mode::kBwdDA && m != Mode::kWeightGrad && m != Mode::kBwdGated;
 }
 
 // Wait sites recorded in the status word when a bounded wait gives up: (mode << 8) | site.
@@ -85,7 +99,13 @@ struct GemmArgs {
     void* out;          // [M][ldo] bf16 or fp32
     const void* residual;  // kGemm2Residual: [M][ldo] bf16 added to the output (may equal out);
                            // kBwdDA: the saved pre-activation A [M][ldo] bf16
-    void* out2;            // kGemm1Train: the pre-activation A [M][ldo] bf16
+    void* out2;            // kGemm1Train: the pre-activation A [M][ldo] bf16;
+                           // kGemm1GatedTrain: G and U [M][ldo2] bf16 (U at column half + j)
+    int ldo2;              // row pitch of out2 in elements (kGemm1GatedTrain)
+    int half;              // kGemm1GatedTrain: U's column offset in out2; kBwdGated: dU's and
+                           // U's column offset in out and residual (both of row pitch ldo)
+    int k2;                // second-GEMM reduction: shards [0, k2) read B from the first map,
+                           // shards [k2, k) from the second (shard index i - k2); k2 = k: one map
     int* status;        // device status word
     // Split reduction (CTA-pair kernel only; tpmlp_plan.h). Tiles [0, sk_first) are whole
     // units handed out round robin; the sk_iters = (num_tiles - sk_first) * kb_tile reduction
@@ -106,7 +126,7 @@ constexpr int kSkSlotFloats = 128 * 256;  // one CTA's half of a 256 x 256 accum
 // c0 = part * kCols, and in the gated layer also the same columns of the up half (+ G).
 template <Mode MODE, int WIDTH, typename Fn>
 __device__ __forceinline__ void for_each_warp_slice(int part, Fn&& fn) {
-    if constexpr (MODE == Mode::kGemm1Gated) {
+    if constexpr (is_gated(MODE)) {
         constexpr int G = WIDTH / 2, kCols = G / kEpiParts;
 #pragma unroll 1
         for (int c = part * kCols; c < (part + 1) * kCols; c += 32) {
@@ -313,6 +333,12 @@ __device__ __forceinline__ float silu(float a) {
     return a * rcp_approx(1.0f + ex2_approx(a * -1.44269504088896341f));
 }
 
+// SiLU'(a) = sigma(a) (1 + a (1 - sigma(a))).
+__device__ __forceinline__ float silu_grad(float a) {
+    const float s = rcp_approx(1.0f + ex2_approx(a * -1.44269504088896341f));
+    return s * fmaf(a, 1.0f - s, 1.0f);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // round to nearest even
     return *reinterpret_cast<uint32_t*>(&p);
@@ -366,7 +392,7 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const fl
                                                const void* residual, void* out2, uint32_t stage) {
     const int row0 = row - static_cast<int>(threadIdx.x & 31);
     float x[32];
-    if constexpr (MODE == Mode::kBwdDA || MODE == Mode::kWeightGrad) {
+    if constexpr (!has_bias(MODE)) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);  // no bias
     } else {
@@ -443,27 +469,85 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const fl
 
 // One 32-column slice of the warp's 32 output rows of the gated first layer: the gate values g
 // and the up values u of the same 32 outputs; Y = SiLU(g + bias_g) * (u + bias_u), bf16.
+// TRAIN: also keep the pre-activations for the backward pass, G = g + bias_g at out2[row][col]
+// and U = u + bias_u at out2[row][half + col] (bf16, row pitch ldo2).
+template <bool TRAIN>
 __device__ __forceinline__ void epilogue_gated_slice(const uint32_t (&g)[32], const uint32_t (&u)[32],
                                                      const float* __restrict__ bias_g,
                                                      const float* __restrict__ bias_u,
-                                                     void* out, int row, int M, int ldo, int col,
+                                                     const GemmArgs& args, int row, int col,
                                                      uint32_t stage) {
-    float x[32];
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
+    float gv[32], uv[32];
     const float4* bg4 = reinterpret_cast<const float4*>(bias_g);
     const float4* bu4 = reinterpret_cast<const float4*>(bias_u);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const float4 bg = __ldg(bg4 + j);
         const float4 bu = __ldg(bu4 + j);
-        x[4 * j + 0] = silu(__uint_as_float(g[4 * j + 0]) + bg.x) * (__uint_as_float(u[4 * j + 0]) + bu.x);
-        x[4 * j + 1] = silu(__uint_as_float(g[4 * j + 1]) + bg.y) * (__uint_as_float(u[4 * j + 1]) + bu.y);
-        x[4 * j + 2] = silu(__uint_as_float(g[4 * j + 2]) + bg.z) * (__uint_as_float(u[4 * j + 2]) + bu.z);
-        x[4 * j + 3] = silu(__uint_as_float(g[4 * j + 3]) + bg.w) * (__uint_as_float(u[4 * j + 3]) + bu.w);
+        gv[4 * j + 0] = __uint_as_float(g[4 * j + 0]) + bg.x;
+        gv[4 * j + 1] = __uint_as_float(g[4 * j + 1]) + bg.y;
+        gv[4 * j + 2] = __uint_as_float(g[4 * j + 2]) + bg.z;
+        gv[4 * j + 3] = __uint_as_float(g[4 * j + 3]) + bg.w;
+        uv[4 * j + 0] = __uint_as_float(u[4 * j + 0]) + bu.x;
+        uv[4 * j + 1] = __uint_as_float(u[4 * j + 1]) + bu.y;
+        uv[4 * j + 2] = __uint_as_float(u[4 * j + 2]) + bu.z;
+        uv[4 * j + 3] = __uint_as_float(u[4 * j + 3]) + bu.w;
     }
     uint32_t p[16];
-    pack_slice(x, p);
-    store_rows_coalesced(p, stage, static_cast<__nv_bfloat16*>(out),
-                         row - static_cast<int>(threadIdx.x & 31), M, ldo, col);
+    if constexpr (TRAIN) {
+        __nv_bfloat16* a_save = static_cast<__nv_bfloat16*>(args.out2);
+        pack_slice(gv, p);
+        store_rows_coalesced(p, stage, a_save, row0, args.M, args.ldo2, col);
+        pack_slice(uv, p);
+        store_rows_coalesced(p, stage, a_save, row0, args.M, args.ldo2, args.half + col);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) gv[j] = silu(gv[j]) * uv[j];
+    pack_slice(gv, p);
+    store_rows_coalesced(p, stage, static_cast<__nv_bfloat16*>(args.out), row0, args.M, args.ldo,
+                         col);
+}
+
+// One 32-column slice of the gated backward's first GEMM: v = dY for outputs [col, col + 32)
+// of this lane's row; G and U from the saved pre-activations (aux[row][col], aux[row][half +
+// col], row pitch ldo). Writes dG = dY U SiLU'(G) to out[row][col] and dU = dY SiLU(G) to
+// out[row][half + col] (bf16, row pitch ldo).
+__device__ __forceinline__ void epilogue_bwd_gated_slice(const uint32_t (&v)[32], const GemmArgs& args,
+                                                         int row, int col, uint32_t stage) {
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
+    float dg[32], du[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dg[j] = du[j] = __uint_as_float(v[j]);
+    if (row < args.M) {
+        const __nv_bfloat16* aux = static_cast<const __nv_bfloat16*>(args.residual) +
+                                   static_cast<size_t>(row) * args.ldo + col;
+        const uint4* g4 = reinterpret_cast<const uint4*>(aux);
+        const uint4* u4 = reinterpret_cast<const uint4*>(aux + args.half);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 gq = g4[j], uq = u4[j];
+            const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+            const uint32_t uw[4] = {uq.x, uq.y, uq.z, uq.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int e = 8 * j + 2 * i + h;
+                    const float gg = __uint_as_float(h ? (gw[i] & 0xFFFF0000u) : (gw[i] << 16));
+                    const float uu = __uint_as_float(h ? (uw[i] & 0xFFFF0000u) : (uw[i] << 16));
+                    du[e] *= silu(gg);
+                    dg[e] *= uu * silu_grad(gg);
+                }
+            }
+        }
+    }
+    uint32_t p[16];
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+    pack_slice(dg, p);
+    store_rows_coalesced(p, stage, out, row0, args.M, args.ldo, col);
+    pack_slice(du, p);
+    store_rows_coalesced(p, stage, out, row0, args.M, args.ldo, args.half + col);
 }
 
 // Drain the accumulator columns [base, base + width) of this warp's 32 rows through the
@@ -476,7 +560,7 @@ template <Mode MODE, bool OUT_F32, int WIDTH, typename Release>
 __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs& args, int row,
                                                   int n0, int part, uint32_t stage,
                                                   Release release) {
-    if constexpr (MODE == Mode::kGemm1Gated) {
+    if constexpr (is_gated(MODE)) {
         constexpr int G = WIDTH / 2;
         constexpr int kCols = G / kEpiParts;
         static_assert(kCols % 32 == 0, "gated epilogue slice");
@@ -489,8 +573,8 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs
             ptx::tmem_wait_ld(g);
             ptx::tmem_wait_ld(u);
             if (c + 32 == c0 + kCols) release();
-            epilogue_gated_slice(g, u, args.bias + n0 + c, args.bias + n0 + G + c, args.out, row,
-                                 args.M, args.ldo, n0 / 2 + c, stage);
+            epilogue_gated_slice<MODE == Mode::kGemm1GatedTrain>(
+                g, u, args.bias + n0 + c, args.bias + n0 + G + c, args, row, n0 / 2 + c, stage);
         }
     } else {
         constexpr int kCols = WIDTH / kEpiParts;
@@ -502,8 +586,11 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs
             ptx::tmem_ld_32x32b_x32(taddr + c, v);
             ptx::tmem_wait_ld(v);
             if (c + 32 == c0 + kCols) release();
-            epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo, n0 + c,
-                                          args.residual, args.out2, stage);
+            if constexpr (MODE == Mode::kBwdGated)
+                epilogue_bwd_gated_slice(v, args, row, n0 + c, stage);
+            else
+                epilogue_slice<MODE, OUT_F32>(v, args.bias, args.out, row, args.M, args.ldo,
+                                              n0 + c, args.residual, args.out2, stage);
         }
     }
 }
@@ -517,11 +604,11 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, int t, int& m_blk
 // otherwise wait on DRAM once per 32-column slice; later tiles find the bias in L2.
 template <Mode MODE, int WIDTH>
 __device__ __forceinline__ void prefetch_tile_bias(const GemmArgs& a, int t, int part) {
-    if constexpr (MODE != Mode::kBwdDA && MODE != Mode::kWeightGrad) {
+    if constexpr (has_bias(MODE)) {
         if (t >= a.num_tiles) return;
         int m_blk, n_blk;
         decode_tile(a, t, m_blk, n_blk);
-        constexpr bool kGated = MODE == Mode::kGemm1Gated;
+        constexpr bool kGated = is_gated(MODE);
         constexpr int kCols = (kGated ? WIDTH / 2 : WIDTH) / kEpiParts;  // <= 128: 4 lines
         const int lane = threadIdx.x & 31;
         const int line = lane & 3, half = lane >> 2;  // half 1: the gated layer's up columns
@@ -540,7 +627,8 @@ __device__ __forceinline__ void prefetch_tile_bias(const GemmArgs& a, int t, int
 template <int BN, int STAGES, Mode MODE, bool OUT_F32, bool MN = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     tpmlp_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
     using L = GemmSmem<BN, STAGES>;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, MN);
     constexpr int kCode = static_cast<int>(MODE) << 8;
@@ -580,6 +668,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
+        if (!is_gemm1(MODE) && !MN && args.k2 < args.k) ptx::prefetch_tensormap(&tmB2);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_holder), L::kTmemCols);
@@ -640,8 +729,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     } else {
                         const int i = kb / args.kb_shard;               // shard of this block
                         const int kk = (kb - i * args.kb_shard) * kBK;  // offset inside shard i
+                        const bool second = i >= args.k2;
                         ptx::tma_load_2d(sa, &tmA, full_bar(stage), i * args.f + kk, m0);
-                        ptx::tma_load_3d(sb, &tmB, full_bar(stage), kk, n0, i);
+                        ptx::tma_load_3d(sb, second ? &tmB2 : &tmB, full_bar(stage), kk, n0,
+                                         second ? i - args.k2 : i);
                     }
                     ++issued;
                     if (++stage == STAGES) {

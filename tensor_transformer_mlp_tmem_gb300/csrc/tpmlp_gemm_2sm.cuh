@@ -53,7 +53,8 @@ struct PairSmem {
 template <int STAGES, int NUM_ACC, Mode MODE, bool OUT_F32, bool MN = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     tpmlp_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
     using L = PairSmem<STAGES, NUM_ACC>;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, kPairBN, MN);
     constexpr int kCode = (static_cast<int>(MODE) << 8) | 0x80;  // 0x80: pair kernel
@@ -96,6 +97,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
+        if (!is_gemm1(MODE) && !MN && args.k2 < args.k) ptx::prefetch_tensormap(&tmB2);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(ptx::smem_addr(tmem_holder), L::kTmemCols);
@@ -157,8 +159,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     } else {
                         const int i = kb / args.kb_shard;               // shard of this block
                         const int kk = (kb - i * args.kb_shard) * kBK;  // offset inside shard i
+                        const bool second = i >= args.k2;
                         ptx::tma_load_2d_pair(sa, &tmA, fb, i * args.f + kk, m0);
-                        ptx::tma_load_3d_pair(sb, &tmB, fb, kk, nb, i);
+                        ptx::tma_load_3d_pair(sb, second ? &tmB2 : &tmB, fb, kk, nb,
+                                              second ? i - args.k2 : i);
                     }
                     ++issued;
                     if (++stage == STAGES) {

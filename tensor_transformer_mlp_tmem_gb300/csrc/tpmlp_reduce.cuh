@@ -9,10 +9,11 @@ namespace tpmlp {
 
 constexpr int kColsumThreads = 256;  // 8 eight-column chunks x 32 row lanes = 64 columns
 
-// partial[s][c] = sum of in[r][c] over the rows r of split s (rows_per_split rows each).
+// partial[s][c] = sum of in[r][c] over the rows r of split s (rows_per_split rows each);
+// in has row pitch ld elements.
 __global__ void __launch_bounds__(kColsumThreads)
-    colsum_partial_kernel(const uint16_t* __restrict__ in, int M, int C, int rows_per_split,
-                          float* __restrict__ partial) {
+    colsum_partial_kernel(const uint16_t* __restrict__ in, int M, int C, int ld,
+                          int rows_per_split, float* __restrict__ partial) {
     __shared__ float red[32][65];
     const int chunk = threadIdx.x & 7;
     const int lane_row = threadIdx.x >> 3;
@@ -21,7 +22,7 @@ __global__ void __launch_bounds__(kColsumThreads)
     const int r_end = min(M, r_begin + rows_per_split);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int r = r_begin + lane_row; r < r_end; r += 32) {
-        const uint4 u = *reinterpret_cast<const uint4*>(in + static_cast<size_t>(r) * C + c0);
+        const uint4 u = *reinterpret_cast<const uint4*>(in + static_cast<size_t>(r) * ld + c0);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
