@@ -820,7 +820,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // all of this warp's accumulator columns are in registers: hand it back
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(empty);
+                if (lane == 0) ptx::mbar_arrive_relaxed(empty);
             });
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;

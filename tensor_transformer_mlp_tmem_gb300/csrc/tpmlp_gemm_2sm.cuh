@@ -259,10 +259,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kPairBN;
             const uint32_t empty = ptx::mapa_shared(tempty_bar(acc), 0);  // rank 0's barrier
-            auto release = [&] {
+            auto release = [&] {  // the accumulator's columns are in registers: hand it back
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(empty);
+                if (lane == 0) ptx::mbar_arrive_cluster_relaxed(empty);
             };
             const uint32_t stage_buf = base + L::kEpiOffset + (warp - 2) * kStageSliceBytes;
             bool epilogue = true;
