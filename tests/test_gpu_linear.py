@@ -70,3 +70,16 @@ def test_linear_context_rejects_block_calls_and_vice_versa(lib):
         with pytest.raises(tp.TpmlpError) as e:
             tp.tpmlp_linear_pack(mlp.ctx, to_dev(W), to_dev(b))
         assert e.value.status == tp.TPMLP_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kind,N", [("row", 4096), ("column", 12288)])
+def test_linear_7b_shape_sampled_rows(lib, kind, N):
+    """The projections at the size the benchmark times (M = 8192 tokens, K = 4096, k = 8):
+    rows are independent, so the oracle on sampled rows checks them exactly."""
+    K, k, M = 4096, 8, 8192
+    X, W, b = inputs(K, N, M, 171)
+    out = run(kind, X, W, b, k)
+    rows = synth.sample_rows(M, 16)
+    ref = oracle.linear(kind, np.ascontiguousarray(X[rows]), W, b, k)
+    got = to_f64(out[torch.from_numpy(rows).cuda()])
+    assert_close(got, ref, what=f"{kind} K={K} N={N} k={k} M={M} (sampled rows)")
