@@ -74,9 +74,10 @@ typedef enum {
                                      weights come from tpmlp_pack_shards_swiglu */
 #define TPMLP_FLAG_FIXED_ORDER 0x8u /* never split an output tile's reduction across CTA pairs.
                                      By default, when the last wave of 256 x 256 tiles would
-                                     leave CTA pairs idle, the reductions of the last tiles are
-                                     divided among all pairs and their fp32 partial sums added
-                                     in a fixed order: results are deterministic, but their
+                                     leave CTA pairs idle, or a launch has fewer tiles than
+                                     pairs (a small batch), the reductions of those tiles are
+                                     divided among several pairs and their fp32 partial sums
+                                     added in a fixed order: results are deterministic, but their
                                      last bits then depend on the token count M. With this flag
                                      every tile is summed in one pass in reduction order, so the
                                      pair and single-SM kernels, and any M, give identical bits */

@@ -265,7 +265,7 @@ int max_resident_pairs(tpmlp_ctx* c, Kernel kern, uint32_t smem) {
 //    GEMM (R = 8, 768 blocks) 4.7 % faster; the GPT-3 first GEMM (R = 32, 192 blocks, at 70 %
 //    of a round by the model) 1.3 % slower, hence the half.
 constexpr tpmlp::SplitRule kSplitRule{TPMLP_SPLIT_TAIL_PCT, 16, 64.0 * (1 << 20),
-                                      1.7e15 / 76, 6.0e12, 0.5};
+                                      1.7e15 / 76, 6.0e12, 0.5, 4, 32};
 
 // The split's flags carry an epoch chosen here, per launch. A launch recorded into a CUDA graph
 // would replay with the same epoch and could read partial sums before they are written, so
@@ -279,21 +279,26 @@ bool capturing(cudaStream_t s) {
     return st != cudaStreamCaptureStatusNone;
 }
 
-void plan_split(tpmlp_ctx* c, GemmArgs& a, int pairs, cudaStream_t s) {
+// Returns the number of pairs to launch: min(T, resident), or the plan's count when a launch
+// of fewer tiles than pairs spreads each tile over several pairs.
+int plan_split(tpmlp_ctx* c, GemmArgs& a, int resident, cudaStream_t s) {
     a.sk_first = a.num_tiles;
     a.sk_iters = 0;
-    if (!c->sk_partial || pairs > c->num_sms / 2 || capturing(s)) return;
-    const tpmlp::SplitLaunch L{a.num_tiles, pairs,    a.kb_tile,       a.m_blocks,
+    const int pairs = std::min(a.num_tiles, resident);
+    if (!c->sk_partial || resident > c->num_sms / 2 || capturing(s)) return pairs;
+    const tpmlp::SplitLaunch L{a.num_tiles, resident, a.kb_tile,       a.m_blocks,
                                a.n_blocks,  a.group_m, tpmlp::kPairBM, tpmlp::kPairBN};
     const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, kSplitRule);
     // the counters hold num_sms split tiles (the plan never splits more than 2 * pairs)
-    if (p.sk_first == a.num_tiles || a.num_tiles - p.sk_first > c->num_sms) return;
+    if (p.sk_first == a.num_tiles || a.num_tiles - p.sk_first > c->num_sms) return pairs;
+    if (p.pairs > resident) return pairs;
     a.sk_first = p.sk_first;
     a.sk_iters = p.sk_iters;
     a.sk_partial = c->sk_partial;
     a.sk_count = c->sk_count;
     if (++c->sk_epoch == 0) c->sk_epoch = 1;  // counters start at 0 (epoch 0): never reuse it
     a.sk_epoch = c->sk_epoch;
+    return p.pairs > 0 ? p.pairs : pairs;
 }
 
 template <int STAGES, int NUM_ACC, Mode MODE, bool F32, bool MN = false>
@@ -311,9 +316,8 @@ int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
         resident = max_resident_pairs(c, kern, smem);
         slot.store(resident, std::memory_order_relaxed);
     }
-    const int pairs = std::min(args.num_tiles, resident);
     GemmArgs run = args;
-    plan_split(c, run, pairs, s);
+    const int pairs = plan_split(c, run, resident, s);
     TPMLP_CUDA(c, launch_overlapped(kern, 2 * pairs, smem, s, a, b, b2 ? *b2 : b, run));
     ++c->launches;
     return TPMLP_OK;

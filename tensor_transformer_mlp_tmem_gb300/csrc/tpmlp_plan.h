@@ -95,7 +95,7 @@ TPMLP_HD int work_pair_of(int sk_iters, int num_pairs, long long i) {
     return static_cast<int>(((i + 1) * num_pairs + S - 1) / S - 1);
 }
 
-// Which tiles of a launch are split (sk_first; sk_first == num_tiles: none). Two cases:
+// Which tiles of a launch are split (sk_first; sk_first == num_tiles: none). Three cases:
 //  - A launch of between one and two waves (pairs < T, the second wave at most tail_pct %
 //    full) is split entirely, provided each tile has at least min_blocks reduction blocks and
 //    the operands (A rows of every tile row and B rows of every tile column, kb_tile blocks of
@@ -105,10 +105,17 @@ TPMLP_HD int work_pair_of(int sk_iters, int num_pairs, long long i) {
 //    that is modelled to take under tail_gain of a round: the R tiles' work spread over all
 //    pairs (R / P of a round) plus one read of their operand rows and columns from DRAM,
 //    against a round of whole tiles. Their shares must be non-empty (R * kb_tile >= P).
+//  - A launch of fewer tiles than pairs (a few hundred token rows) runs each tile's reduction
+//    on `parts` = min(max_parts, pairs / T, kb_tile / min_part_blocks) pairs, T * parts pairs
+//    in all, when parts >= 2 (shorter shares cost more in partial sums than they save):
+//    every share then lies inside one tile, so a tile is summed from exactly `parts` partial
+//    sums. Share j of every tile covers the same reduction blocks, so tiles that share an
+//    operand read it in step, as whole tiles do, and no L2 limit applies.
 // A round is 2 * 256 * 256 * 64 * kb_tile FLOP at pair_flops.
 struct SplitPlan {
     int sk_first;
     int sk_iters;
+    int pairs;   // pairs to launch when the plan says so (fewer tiles than pairs); 0: unchanged
 };
 
 struct SplitLaunch {
@@ -124,14 +131,27 @@ struct SplitRule {
     double pair_flops;          // tail split: FLOP/s of one CTA pair
     double dram_Bps;            // ... DRAM bandwidth for the tail's operands
     double tail_gain;           // ... split when the modelled tail is below this share of a round
+    int max_parts;              // fewer tiles than pairs: at most this many pairs per tile
+    int min_part_blocks;        // ... each with at least this many reduction blocks
 };
 
 inline SplitPlan plan_split_tiles(const SplitLaunch& L, const SplitRule& rule) {
-    SplitPlan p{L.num_tiles, 0};
-    if (L.pairs <= 0 || L.kb_tile < rule.min_blocks) return p;
+    SplitPlan p{L.num_tiles, 0, 0};
+    if (L.pairs <= 0 || L.num_tiles <= 0 || L.kb_tile < rule.min_blocks) return p;
     const int waves = L.num_tiles / L.pairs, rem = L.num_tiles % L.pairs;
-    if (rem == 0 || waves < 1) return p;
     const double block_bytes = static_cast<double>(L.kb_tile) * 64 * 2.0;  // one row, all K
+    if (waves == 0) {
+        int parts = L.pairs / L.num_tiles;
+        if (parts > rule.max_parts) parts = rule.max_parts;
+        if (rule.min_part_blocks > 0 && parts > L.kb_tile / rule.min_part_blocks)
+            parts = L.kb_tile / rule.min_part_blocks;
+        if (parts < 2 || L.kb_tile < parts) return p;
+        p.sk_first = 0;
+        p.sk_iters = L.num_tiles * L.kb_tile;
+        p.pairs = L.num_tiles * parts;
+        return p;
+    }
+    if (rem == 0) return p;
     if (waves == 1) {
         if (rem * 100 > L.pairs * rule.tail_pct) return p;
         const double operand_bytes =

@@ -40,12 +40,14 @@ def test_pipeline_wait_runs_out_and_is_reported(lib, stall_lib, single_sm):
     dbg.tpmlp_get_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     dbg.tpmlp_destroy.argtypes = [vp]
 
-    H, F, k, M = 1024, 1024, 2, 256  # 16 reduction blocks per tile: stage 5 is reached
+    # 16 reduction blocks per tile: stage 5 is reached (whole tiles: no tile's reduction is
+    # spread over several pairs, each of which would issue fewer stages)
+    H, F, k, M = 1024, 1024, 2, 256
     d = synth.make_inputs(H, F, M, 191)
     dd = inputs_on_device(d)
     Y = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
     ctx = vp()
-    flags = tp.TPMLP_FLAG_SINGLE_SM if single_sm else 0
+    flags = (tp.TPMLP_FLAG_SINGLE_SM if single_sm else 0) | tp.TPMLP_FLAG_FIXED_ORDER
     assert dbg.tpmlp_create(ctypes.byref(ctx), H, F, k, flags) == 0
     try:
         assert dbg.tpmlp_pack_shards(ctx, dd["W1"].data_ptr(), dd["b1"].data_ptr(),

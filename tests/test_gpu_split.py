@@ -10,7 +10,8 @@ holding the tile's first block, which adds it and runs the epilogue. Here the se
 Checked: the oracle on sampled rows; agreement with TPMLP_FLAG_FIXED_ORDER (every tile in
 one pass) up to fp32 summation order and the bf16 roundings it moves; bitwise determinism
 from call to call; and, for the second GEMM with fp32 output on one Y, that the two
-schedules agree to fp32 accuracy but really differ (the split path ran)."""
+schedules agree to fp32 accuracy but really differ (the split path ran). A launch of fewer
+tiles than pairs spreads each deep tile over up to 4 pairs of at least 32 blocks."""
 import numpy as np
 import pytest
 import torch
@@ -140,6 +141,35 @@ def test_split_of_the_last_tiles(lib):
     assert_close(to_f64(outs["split"][1])[rows], ref["Z"], what="tail-split Z")
 
 
+@pytest.mark.parametrize("Mn", [128, 256, 77])
+def test_split_of_narrow_launches(lib, Mn):
+    """Fewer tiles than pairs (a small batch): at H = 1024, F = 8192 the second GEMM has 4 (or
+    8) tiles 128 blocks deep, and each tile's reduction runs on 4 pairs of 32 blocks. The
+    first GEMM (16 blocks per tile) keeps whole tiles."""
+    Hn, Fn, kn = 1024, 8192, 8
+    d = synth.make_inputs(Hn, Fn, Mn, 271)
+    dd = inputs_on_device(d)
+    outs = {}
+    for name, kw in (("split", {}), ("fixed", dict(fixed_order=True)),
+                     ("split32", dict(z_fp32=True)), ("fixed32", dict(z_fp32=True, fixed_order=True))):
+        with tp.TPMLP(Hn, Fn, kn, **kw) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            Y = mlp.gemm1(dd["X"])
+            Z = mlp.gemm2(Y)
+            Z2 = mlp.gemm2(Y)
+            torch.cuda.synchronize()
+            rc, detail = mlp.status()
+            assert rc == tp.TPMLP_OK, f"device status {detail:#x}"
+            assert torch.equal(Z, Z2)  # deterministic
+            outs[name] = (Y, Z)
+    assert torch.equal(outs["split"][0], outs["fixed"][0])  # the first GEMM is not split
+    a, b = outs["split32"][1].double(), outs["fixed32"][1].double()
+    assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() < 1e-5
+    assert not torch.equal(outs["split32"][1], outs["fixed32"][1]), "no tile was split"
+    ref = oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], kn)["Z"]
+    assert_close(to_f64(outs["split"][1]), ref, what=f"narrow split Z, M={Mn}")
+
+
 def test_forward_in_a_cuda_graph(lib, block):
     """A forward captured into a CUDA graph and replayed on new inputs. Launches enqueued under
     stream capture never split their reduction (a replay would reuse the captured flags'
@@ -177,7 +207,8 @@ def handoff_lib(tmp_path_factory):
 
 
 @pytest.mark.parametrize("Hs,Fs,ks,Ms", [(2560, 2048, 2, 2560),     # whole launches split
-                                         (5120, 16384, 8, 2048)])   # the second GEMM's tail split
+                                         (5120, 16384, 8, 2048),    # the second GEMM's tail split
+                                         (1024, 8192, 8, 128)])     # fewer tiles than pairs
 def test_split_tiles_handed_over_give_identical_bits(lib, handoff_lib, Hs, Fs, ks, Ms):
     """A test build whose first pairs never wait and whose other pairs count in 200 us late:
     the first pair hands every split tile over and the last of the others finishes it through

@@ -33,10 +33,10 @@ int shim_pair_of(int sk_iters, int num_pairs, long long i) {
 }
 void shim_plan(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks, int group_m,
                int* out) {
-    const tpmlp::SplitRule rule{85, 16, 64.0 * (1 << 20), 1.7e15 / 76, 6.0e12, 0.5};
+    const tpmlp::SplitRule rule{85, 16, 64.0 * (1 << 20), 1.7e15 / 76, 6.0e12, 0.5, 4, 32};
     const tpmlp::SplitLaunch L{num_tiles, pairs, kb_tile, m_blocks, n_blocks, group_m, 256, 256};
     tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, rule);
-    out[0] = p.sk_first; out[1] = p.sk_iters;
+    out[0] = p.sk_first; out[1] = p.sk_iters; out[2] = p.pairs;
 }
 }
 """
@@ -129,10 +129,10 @@ def test_random_schedules(sched):
         check_schedule(sched, T, P, kb, rng.choice(choices))
 
 
-def plan(lib, T, P, kb, mb, nb, group_m=8):
-    out = (ctypes.c_int * 2)()
+def plan(lib, T, P, kb, mb, nb, group_m=8, want_pairs=False):
+    out = (ctypes.c_int * 3)()
     lib.shim_plan(T, P, kb, mb, nb, group_m, out)
-    return out[0], out[1]
+    return (out[0], out[1], out[2]) if want_pairs else (out[0], out[1])
 
 
 @pytest.mark.parametrize("P", [74, 75, 76])
@@ -173,3 +173,40 @@ def test_tail_split_keeps_shares_nonempty(sched):
             first, iters = plan(sched, T, P, kb, 16, T // 16 + 1)
             if first != T:
                 assert first == T - R and iters == R * kb and iters >= P
+
+
+def test_narrow_launch_plans(sched):
+    """Fewer tiles than pairs: each tile over min(4, P / T, kb / 32) pairs, when that is at
+    least 2."""
+    P = 76
+    # the second GEMM of a 128-token batch at the 7b shape: 16 column tiles, 256 blocks deep,
+    # one row block (only A, 8 MB, is shared) -> 4 pairs per tile, 64 pairs
+    assert plan(sched, 16, P, 256, 1, 16, want_pairs=True) == (0, 16 * 256, 64)
+    # a 64-block tile over 2 pairs of 32 blocks
+    assert plan(sched, 1, P, 64, 1, 1, want_pairs=True) == (0, 64, 2)
+    # the tiny second GEMM (one tile, 16 blocks) and a 768-row chunk of GPT-2's (9 tiles, 48
+    # blocks): shares under 32 blocks -> whole tiles
+    assert plan(sched, 1, P, 16, 1, 1)[0] == 1
+    assert plan(sched, 9, P, 48, 3, 3)[0] == 9
+    # 40 tiles on 76 pairs: one pair per tile -> whole tiles
+    assert plan(sched, 40, P, 64, 4, 10, want_pairs=True) == (40, 0, 0)
+    # too shallow (12 blocks) -> whole tiles
+    assert plan(sched, 16, P, 12, 1, 16)[0] == 16
+    # two row blocks of the 7b second GEMM (512 tokens): 2 pairs per tile; the tiles of a
+    # column read W2 in step, so W2 need not fit in L2
+    assert plan(sched, 32, P, 256, 2, 16, want_pairs=True) == (0, 32 * 256, 64)
+
+
+@pytest.mark.parametrize("T,kb", [(1, 64), (16, 256), (9, 96), (19, 70), (25, 128), (3, 200)])
+def test_narrow_launch_schedule(sched, T, kb):
+    """Every share of a narrow launch lies inside one tile; a tile has exactly `parts`
+    contributors, the first of which holds its first blocks."""
+    P = 76
+    first, iters, pairs = plan(sched, T, P, kb, 1, T, want_pairs=True)
+    assert first == 0 and iters == T * kb
+    parts = pairs // T
+    assert pairs == T * parts and 2 <= parts <= 4
+    check_schedule(sched, T, pairs, kb, 0)
+    for p in range(pairs):
+        us = walk(sched, 0, iters, kb, p, pairs)
+        assert len(us) == 1 and us[0][0] == p // parts
