@@ -95,9 +95,9 @@ typedef enum {
  *            TPMLP_FLAG_FIXED_ORDER
  * Allocates the packed-weight buffers (2*H*F bf16 + (F+H) fp32), a device status word and,
  * unless TPMLP_FLAG_SINGLE_SM or TPMLP_FLAG_FIXED_ORDER is given, the split-reduction
- * workspace (256 KB of fp32 partial sums and 64 bytes of flags per CTA pair: about 19 MB on
- * 152 SMs); the intermediate activation buffer is allocated by tpmlp_reserve or the first
- * forward.
+ * workspace (two 128 KB slots of fp32 partial sums per CTA, 512 KB per CTA pair, plus
+ * 64 bytes of arrival counters per SM: about 40 MB on 152 SMs); the intermediate activation
+ * buffer is allocated by tpmlp_reserve or the first forward.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ARCH (device is not sm_103), OOM, CUDA.
  */
 TPMLP_API int tpmlp_create(tpmlp_ctx **out, int64_t H, int64_t F, int32_t k, uint32_t flags);
