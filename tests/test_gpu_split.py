@@ -110,6 +110,38 @@ def test_split_weight_gradients(lib):
                      what=f"{name} split vs fixed order")
 
 
+def test_narrow_split_of_weight_gradients(lib):
+    """dW1 [256, 1024] and dW2 [1024, 256] over 8192 tokens: 4 tiles each, 128 reduction blocks
+    deep, so each tile's token reduction runs on 4 pairs."""
+    Hb, Fb, kb, Mb = 256, 1024, 4, 8192
+    d = synth.make_inputs(Hb, Fb, Mb, 281)
+    dZ = synth.normal_bf16(281, 60, (Mb, Hb), 1.0)
+    dd = inputs_on_device(d)
+    outs = {}
+    for fixed in (False, True):
+        with tp.TPMLP(Hb, Fb, kb, fixed_order=fixed) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            X = dd["X"].view(1, Mb, Hb)
+            _, Ys, As = mlp.forward_train(X)
+            g = mlp.backward(to_dev(dZ).view(1, Mb, Hb), X, Ys, As, dd["W1"], dd["W2"])
+            g2 = mlp.backward(to_dev(dZ).view(1, Mb, Hb), X, Ys, As, dd["W1"], dd["W2"])
+            torch.cuda.synchronize()
+            rc, detail = mlp.status()
+            assert rc == tp.TPMLP_OK, f"device status {detail:#x}"
+            for a, b in zip(g, g2):
+                assert torch.equal(a, b)  # deterministic
+            outs[fixed] = g
+    ref = oracle.backward(d["X"], d["W1"], d["b1"], d["W2"], dZ, kb)
+    for i, name in enumerate(("dX", "dW1", "db1", "dW2", "db2")):
+        got = to_f64(outs[False][i]).reshape(ref[name].shape)
+        assert_close(got, ref[name], what=f"narrow split {name}")
+    # fp32 weight gradients: the schedules agree to fp32 accuracy but really differ
+    for i in (1, 3):
+        a, b = outs[False][i].double(), outs[True][i].double()
+        assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() < 1e-5
+        assert not torch.equal(outs[False][i], outs[True][i]), "no weight-gradient tile was split"
+
+
 def test_split_of_the_last_tiles(lib):
     """A launch of several waves keeps whole tiles except its last R = T mod P: at H = 5120,
     F = 16384, M = 2048 the second GEMM has 160 tiles (2 waves + R on 74-76 pairs), each 256
