@@ -300,9 +300,11 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // base 2 with the factor 1/2 folded in (fit_phi.py writes the coefficients):
 //   Phi(-|a|) = t * 2^(P2(t) - a^2 log2(e) / 2).
 // Relative error below 1e-5 over the fp32 range, more than two orders of magnitude under a
-// bf16 step.
-__device__ __forceinline__ float normal_lower_tail(float a) {
-    const float t = rcp_approx(fmaf(fabsf(a), 0.35355339059327376f, 1.0f));
+// bf16 step. normal_tail_t gives t, normal_tail_exp the power of two.
+__device__ __forceinline__ float normal_tail_t(float a) {
+    return rcp_approx(fmaf(fabsf(a), 0.35355339059327376f, 1.0f));
+}
+__device__ __forceinline__ float normal_tail_exp(float a, float t) {
     float p = -2.294616550e-01f;
     p = fmaf(p, t, 9.304409623e-01f);
     p = fmaf(p, t, -1.215087414e+00f);
@@ -311,14 +313,20 @@ __device__ __forceinline__ float normal_lower_tail(float a) {
     p = fmaf(p, t, 5.527308583e-01f);
     p = fmaf(p, t, 1.442202449e+00f);
     p = fmaf(p, t, -2.825744629e+00f);
-    return t * ex2_approx(fmaf(a * a, -0.72134752044448170f, p));
+    return ex2_approx(fmaf(a * a, -0.72134752044448170f, p));
+}
+__device__ __forceinline__ float normal_lower_tail(float a) {
+    const float t = normal_tail_t(a);
+    return t * normal_tail_exp(a, t);
 }
 
-// GeLU in its erf form, a * Phi(a) = a/2 * (1 + erf(a / sqrt 2)), Phi from the lower tail by
-// symmetry: Phi(a) = 1 - Phi(-a) for a >= 0.
+// GeLU in its erf form, a * Phi(a) = a/2 * (1 + erf(a / sqrt 2)), written through the lower
+// tail as max(a, 0) - |a| Phi(-|a|) (for a >= 0 by Phi(a) = 1 - Phi(-a)): no select, and the
+// tail's factor t is multiplied into |a| before the power of two. Fifteen instructions,
+// bias add excluded.
 __device__ __forceinline__ float gelu_erf(float a) {
-    const float q = normal_lower_tail(a);
-    return a * (a < 0.0f ? q : 1.0f - q);
+    const float t = normal_tail_t(a);
+    return fmaf(-(fabsf(a) * t), normal_tail_exp(a, t), fmaxf(a, 0.0f));
 }
 
 // GeLU'(a) = Phi(a) + a phi(a), phi(a) = 2^(-a^2 log2(e) / 2) / sqrt(2 pi) the normal density.

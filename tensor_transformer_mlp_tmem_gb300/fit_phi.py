@@ -70,6 +70,25 @@ def phi_lower_fp32(a: np.ndarray, c2: np.ndarray) -> np.ndarray:
     return (t.astype(np.float64) * np.exp2(e.astype(np.float64))).astype(f32)
 
 
+def gelu_fp32(a: np.ndarray, c2: np.ndarray) -> np.ndarray:
+    """The kernels' GeLU(a) = max(a, 0) - (|a| t) 2^e in float32 steps: t and 2^e as in
+    phi_lower_fp32, the product |a| t rounded, then one fused multiply-add (emulated in
+    float64 and rounded once)."""
+    f32 = np.float32
+    a = np.asarray(a, dtype=f32)
+    aa = np.abs(a)
+    d = (aa.astype(np.float64) * float(f32(0.35355339059327376)) + 1.0).astype(f32)
+    t = (1.0 / d.astype(np.float64)).astype(f32)
+    p = np.full(a.shape, c2[-1], dtype=f32)
+    for ci in c2[-2::-1]:
+        p = (p.astype(np.float64) * t + float(ci)).astype(f32)
+    u = (a.astype(np.float64) * a).astype(f32)
+    e = (u.astype(np.float64) * -float(f32(LOG2E / 2)) + p).astype(f32)
+    x = np.exp2(e.astype(np.float64)).astype(f32)
+    s = (aa.astype(np.float64) * t).astype(f32)
+    return (-(s.astype(np.float64)) * x + np.maximum(a, f32(0)).astype(np.float64)).astype(f32)
+
+
 def c_literals(c2: np.ndarray) -> str:
     return ", ".join(f"{float(v):.9e}f" for v in c2)
 

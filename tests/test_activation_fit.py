@@ -1,9 +1,10 @@
 """Host checks of the constants behind the kernels' activation functions.
 
 The GeLU epilogues evaluate the normal tail Phi(-|a|) with one reciprocal, a degree-7
-polynomial and one exp2 (the Numerical Recipes form of erfc, refitted by fit_phi.py). These
-tests pin that the kernel source holds exactly the fitted constants, and that the formula, run
-in float32 steps on the host, stays far inside a bf16 step of the exact GeLU."""
+polynomial and one exp2 (the Numerical Recipes form of erfc, refitted by fit_phi.py), and
+GeLU(a) as max(a, 0) - |a| Phi(-|a|). These tests pin that the kernel source holds exactly the
+fitted constants, and that the formula, run in float32 steps on the host, stays far inside a
+bf16 step of the exact GeLU."""
 import os
 import re
 
@@ -21,7 +22,7 @@ GEMM_SRC = os.path.join(os.path.dirname(fit_phi.__file__), "csrc", "tpmlp_gemm.c
 
 def kernel_coefficients() -> np.ndarray:
     src = open(GEMM_SRC).read()
-    body = src[src.index("float normal_lower_tail(float a)"):]
+    body = src[src.index("float normal_tail_exp(float a, float t)"):]
     body = body[:body.index("return")]
     lits = re.findall(r"([-+]?\d\.\d+e[-+]\d+)f", body)
     # Horner order in the source: highest degree first
@@ -53,13 +54,11 @@ def test_tail_at_special_points():
 
 
 def test_gelu_from_the_tail_rounds_like_the_exact_gelu():
-    """GeLU(a) = a Phi(a) built from the fitted tail, rounded to bf16, against the exact GeLU
-    rounded to bf16: at most one step apart, and equal almost everywhere."""
+    """The kernels' GeLU, max(a, 0) - (|a| t) 2^e in float32 steps, rounded to bf16, against
+    the exact GeLU rounded to bf16: at most one step apart, and equal almost everywhere."""
     c2 = fit_phi.device_coefficients()
     a = np.linspace(-8.0, 8.0, 400001).astype(np.float32)
-    q = fit_phi.phi_lower_fp32(a, c2)
-    phi = np.where(a < 0, q, (np.float32(1) - q).astype(np.float32))
-    g = (a.astype(np.float64) * phi).astype(np.float32).astype(np.float64)
+    g = fit_phi.gelu_fp32(a, c2).astype(np.float64)
     exact = a.astype(np.float64) * ndtr(a.astype(np.float64))
     gb = synth.round_bf16(g).astype(np.int32)
     eb = synth.round_bf16(exact).astype(np.int32)
@@ -69,3 +68,11 @@ def test_gelu_from_the_tail_rounds_like_the_exact_gelu():
     d = np.abs(ordered(gb) - ordered(eb))
     assert d.max() <= 1
     assert np.mean(d == 0) > 0.999
+
+
+def test_gelu_form_equals_a_times_phi():
+    """max(a, 0) - |a| Phi(-|a|) is a Phi(a) (by Phi(a) = 1 - Phi(-a)): in float64 with the
+    exact tail the two agree to rounding, so the rewrite changes no value beyond float32."""
+    a = np.linspace(-8.0, 8.0, 20001)
+    lhs = np.maximum(a, 0.0) - np.abs(a) * ndtr(-np.abs(a))
+    assert np.max(np.abs(lhs - a * ndtr(a))) < 1e-14
