@@ -301,39 +301,80 @@ __device__ __forceinline__ float rcp_approx(float x) {
 //   Phi(-|a|) = t * 2^(P2(t) - a^2 log2(e) / 2).
 // Relative error below 1e-5 over the fp32 range, more than two orders of magnitude under a
 // bf16 step. normal_tail_t gives t, normal_tail_exp the power of two.
+constexpr int kPhiDegree = 7;
+// P2's coefficients, highest degree first.
+__device__ constexpr float kPhiP2[kPhiDegree + 1] = {
+    -2.294616550e-01f, 9.304409623e-01f, -1.215087414e+00f, 3.299344182e-01f,
+    1.498845778e-02f, 5.527308583e-01f, 1.442202449e+00f, -2.825744629e+00f};
+constexpr float kHalfLog2e = 0.72134752044448170f;  // log2(e) / 2
+
 __device__ __forceinline__ float normal_tail_t(float a) {
     return rcp_approx(fmaf(fabsf(a), 0.35355339059327376f, 1.0f));
 }
 __device__ __forceinline__ float normal_tail_exp(float a, float t) {
-    float p = -2.294616550e-01f;
-    p = fmaf(p, t, 9.304409623e-01f);
-    p = fmaf(p, t, -1.215087414e+00f);
-    p = fmaf(p, t, 3.299344182e-01f);
-    p = fmaf(p, t, 1.498845778e-02f);
-    p = fmaf(p, t, 5.527308583e-01f);
-    p = fmaf(p, t, 1.442202449e+00f);
-    p = fmaf(p, t, -2.825744629e+00f);
-    return ex2_approx(fmaf(a * a, -0.72134752044448170f, p));
+    float p = kPhiP2[0];
+#pragma unroll
+    for (int i = 1; i <= kPhiDegree; ++i) p = fmaf(p, t, kPhiP2[i]);
+    return ex2_approx(fmaf(a * a, -kHalfLog2e, p));
 }
 __device__ __forceinline__ float normal_lower_tail(float a) {
     const float t = normal_tail_t(a);
     return t * normal_tail_exp(a, t);
 }
 
+// Packed fp32x2 arithmetic: two IEEE fp32 operations per instruction, each half rounded
+// exactly like the scalar operation.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_splat(float v) { return f2_pack(v, v); }
+
 // GeLU in its erf form, a * Phi(a) = a/2 * (1 + erf(a / sqrt 2)), written through the lower
 // tail as max(a, 0) - |a| Phi(-|a|) (for a >= 0 by Phi(a) = 1 - Phi(-a)): no select, and the
-// tail's factor t is multiplied into |a| before the power of two. Fifteen instructions,
-// bias add excluded.
-__device__ __forceinline__ float gelu_erf(float a) {
-    const float t = normal_tail_t(a);
-    return fmaf(-(fabsf(a) * t), normal_tail_exp(a, t), fmaxf(a, 0.0f));
+// tail's factor t is multiplied into |a| before the power of two. Two values at a time: the
+// polynomial and the exponent run as packed fp32x2 operations, the reciprocal, exp2, |a| t
+// and the max per value, so the results equal those of the scalar formula bit for bit.
+// Per value about ten instructions, bias add excluded (the epilogue is bound by instruction
+// issue at short reductions).
+__device__ __forceinline__ void gelu_erf2(float& a0, float& a1) {
+    const float t0 = normal_tail_t(a0), t1 = normal_tail_t(a1);
+    const uint64_t T = f2_pack(t0, t1);
+    uint64_t P = f2_splat(kPhiP2[0]);
+#pragma unroll
+    for (int i = 1; i <= kPhiDegree; ++i) P = f2_fma(P, T, f2_splat(kPhiP2[i]));
+    const uint64_t A = f2_pack(a0, a1);
+    float e0, e1;
+    f2_unpack(f2_fma(f2_mul(A, A), f2_splat(-kHalfLog2e), P), e0, e1);
+    const uint64_t X = f2_pack(ex2_approx(e0), ex2_approx(e1));
+    const uint64_t S = f2_pack(-(fabsf(a0) * t0), -(fabsf(a1) * t1));
+    f2_unpack(f2_fma(S, X, f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f))), a0, a1);
 }
 
 // GeLU'(a) = Phi(a) + a phi(a), phi(a) = 2^(-a^2 log2(e) / 2) / sqrt(2 pi) the normal density.
 __device__ __forceinline__ float gelu_grad(float a) {
     const float q = normal_lower_tail(a);
     return (a < 0.0f ? q : 1.0f - q) +
-           a * 0.39894228040143267794f * ex2_approx(a * a * -0.72134752044448170f);
+           a * 0.39894228040143267794f * ex2_approx(a * a * -kHalfLog2e);
 }
 
 // SiLU(a) = a * sigma(a) = a / (1 + e^-a) = a * 1 / (1 + 2^(-a log2 e)).
@@ -408,10 +449,12 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const fl
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float4 bb = __ldg(b4 + j);
-            x[4 * j + 0] = __uint_as_float(v[4 * j + 0]) + bb.x;
-            x[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + bb.y;
-            x[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + bb.z;
-            x[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + bb.w;
+            f2_unpack(f2_add(f2_pack(__uint_as_float(v[4 * j + 0]), __uint_as_float(v[4 * j + 1])),
+                             f2_pack(bb.x, bb.y)),
+                      x[4 * j + 0], x[4 * j + 1]);
+            f2_unpack(f2_add(f2_pack(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])),
+                             f2_pack(bb.z, bb.w)),
+                      x[4 * j + 2], x[4 * j + 3]);
         }
     }
     if constexpr (MODE == Mode::kGemm1Train) {
@@ -422,7 +465,7 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t (&v)[32], const fl
     }
     if constexpr (MODE == Mode::kGemm1 || MODE == Mode::kGemm1Train) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = gelu_erf(x[j]);
+        for (int j = 0; j < 16; ++j) gelu_erf2(x[2 * j], x[2 * j + 1]);
     }
     if constexpr (MODE == Mode::kBwdDA) {
         // dA = dY * GeLU'(A), A the saved (bf16) pre-activation

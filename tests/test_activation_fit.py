@@ -22,10 +22,10 @@ GEMM_SRC = os.path.join(os.path.dirname(fit_phi.__file__), "csrc", "tpmlp_gemm.c
 
 def kernel_coefficients() -> np.ndarray:
     src = open(GEMM_SRC).read()
-    body = src[src.index("float normal_tail_exp(float a, float t)"):]
-    body = body[:body.index("return")]
+    body = src[src.index("float kPhiP2[kPhiDegree + 1] = {"):]
+    body = body[:body.index("}")]
     lits = re.findall(r"([-+]?\d\.\d+e[-+]\d+)f", body)
-    # Horner order in the source: highest degree first
+    # the table holds the highest degree first
     return np.array([float(v) for v in lits[::-1]], dtype=np.float32)
 
 
