@@ -382,6 +382,18 @@ __device__ __forceinline__ float silu(float a) {
     return a * rcp_approx(1.0f + ex2_approx(a * -1.44269504088896341f));
 }
 
+// SiLU(g) * u on two values at once, bit-identical to the scalar silu(g) * u: the products and
+// the sum run as packed fp32x2 operations, exp2 and the reciprocal per value.
+__device__ __forceinline__ void swiglu2(float& g0, float& g1, float u0, float u1) {
+    const uint64_t G = f2_pack(g0, g1);
+    float e0, e1;
+    f2_unpack(f2_mul(G, f2_splat(-1.44269504088896341f)), e0, e1);
+    float d0, d1;
+    f2_unpack(f2_add(f2_splat(1.0f), f2_pack(ex2_approx(e0), ex2_approx(e1))), d0, d1);
+    const uint64_t S = f2_mul(G, f2_pack(rcp_approx(d0), rcp_approx(d1)));
+    f2_unpack(f2_mul(S, f2_pack(u0, u1)), g0, g1);
+}
+
 // SiLU'(a) = sigma(a) (1 + a (1 - sigma(a))).
 __device__ __forceinline__ float silu_grad(float a) {
     const float s = rcp_approx(1.0f + ex2_approx(a * -1.44269504088896341f));
@@ -536,14 +548,17 @@ __device__ __forceinline__ void epilogue_gated_slice(const uint32_t (&g)[32], co
     for (int j = 0; j < 8; ++j) {
         const float4 bg = __ldg(bg4 + j);
         const float4 bu = __ldg(bu4 + j);
-        gv[4 * j + 0] = __uint_as_float(g[4 * j + 0]) + bg.x;
-        gv[4 * j + 1] = __uint_as_float(g[4 * j + 1]) + bg.y;
-        gv[4 * j + 2] = __uint_as_float(g[4 * j + 2]) + bg.z;
-        gv[4 * j + 3] = __uint_as_float(g[4 * j + 3]) + bg.w;
-        uv[4 * j + 0] = __uint_as_float(u[4 * j + 0]) + bu.x;
-        uv[4 * j + 1] = __uint_as_float(u[4 * j + 1]) + bu.y;
-        uv[4 * j + 2] = __uint_as_float(u[4 * j + 2]) + bu.z;
-        uv[4 * j + 3] = __uint_as_float(u[4 * j + 3]) + bu.w;
+        const float bgv[4] = {bg.x, bg.y, bg.z, bg.w}, buv[4] = {bu.x, bu.y, bu.z, bu.w};
+#pragma unroll
+        for (int h = 0; h < 4; h += 2) {
+            const int e = 4 * j + h;
+            f2_unpack(f2_add(f2_pack(__uint_as_float(g[e]), __uint_as_float(g[e + 1])),
+                             f2_pack(bgv[h], bgv[h + 1])),
+                      gv[e], gv[e + 1]);
+            f2_unpack(f2_add(f2_pack(__uint_as_float(u[e]), __uint_as_float(u[e + 1])),
+                             f2_pack(buv[h], buv[h + 1])),
+                      uv[e], uv[e + 1]);
+        }
     }
     uint32_t p[16];
     if constexpr (TRAIN) {
@@ -554,7 +569,7 @@ __device__ __forceinline__ void epilogue_gated_slice(const uint32_t (&g)[32], co
         store_rows_coalesced(p, stage, a_save, row0, args.M, args.ldo2, args.half + col);
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) gv[j] = silu(gv[j]) * uv[j];
+    for (int j = 0; j < 16; ++j) swiglu2(gv[2 * j], gv[2 * j + 1], uv[2 * j], uv[2 * j + 1]);
     pack_slice(gv, p);
     store_rows_coalesced(p, stage, static_cast<__nv_bfloat16*>(args.out), row0, args.M, args.ldo,
                          col);
