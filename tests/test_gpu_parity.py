@@ -79,6 +79,33 @@ def test_forward_matches_oracle_on_workload(lib, name, rows):
     assert np.all(np.isfinite(z))
 
 
+def test_token_count_past_32_bit_element_offsets(lib):
+    """The 7B-shaped block at M = 135168 tokens (B = 33, S = 4096): Y [M, F] holds 2.2e9
+    elements, past 2^31, so the last row blocks' Y and Z addresses need 64-bit index math in
+    both kernels' epilogue stores and in the tensor maps the second GEMM reads Y through. Rows
+    on both sides of the 2^31-element boundary of Y, the last row and a seeded spread are
+    checked against the oracle."""
+    w = synth.WORKLOADS["7b"]
+    B, S = 33, 4096
+    M = B * S
+    edge = (1 << 31) // w.F  # first row of Y whose elements start at or past 2^31
+    assert (M - 1) * w.F >= 1 << 31 and edge < M
+    d = synth.make_inputs(w.H, w.F, M, 17)
+    sel = np.array(sorted(set(synth.sample_rows(M, 24).tolist()) |
+                          {edge - 1, edge, edge + 1, M - 1}), dtype=np.int64)
+    dd = inputs_on_device(d)
+    with tp.TPMLP(w.H, w.F, w.k) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        Z = mlp(dd["X"].view(B, S, w.H))
+        torch.cuda.synchronize()
+        rc, detail = mlp.status()
+        assert rc == tp.TPMLP_OK, f"device status {detail:#x}"
+        z = to_f64(Z.view(M, w.H)[torch.from_numpy(sel).cuda()])
+    ref = oracle.tpmlp(d["X"], d["W1"], d["b1"], d["W2"], d["b2"], w.k, rows=sel)["Z"]
+    assert np.all(np.isfinite(z))
+    assert_close(z, ref, what=f"7b shape, M = {M}")
+
+
 def test_shard_count_sweep(lib):
     """Sweep workload: identical inputs for k = 1, 2, 4, 8, 16; each k against the oracle
     on sampled rows, and every k against k = 1 over the whole output."""
