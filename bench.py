@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -118,6 +119,31 @@ def dist_env():
 
 
 # ------------------------------------------------------------------ clocks
+_UUID_RE = re.compile(r"^GPU-[0-9a-fA-F]{8}(-[0-9a-fA-F]{4}){3}-[0-9a-fA-F]{12}$")
+
+
+def smi_gpu_id(dev_index: int, uuid=None) -> str:
+    """The id `nvidia-smi -i` takes for CUDA device `dev_index`. CUDA ordinals are renumbered
+    under CUDA_VISIBLE_DEVICES and nvidia-smi's indices are not, so use the device's UUID
+    (`uuid`: torch's for the device, looked up when not given), else the matching entry of
+    CUDA_VISIBLE_DEVICES, else the ordinal itself."""
+    if uuid is None:
+        try:
+            import torch
+            uuid = torch.cuda.get_device_properties(dev_index).uuid
+        except Exception:
+            uuid = None
+    if uuid is not None:
+        u = str(uuid)
+        u = u if u.startswith("GPU-") else "GPU-" + u
+        if _UUID_RE.match(u):
+            return u
+    parts = [p.strip() for p in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if p.strip()]
+    if 0 <= dev_index < len(parts):
+        return parts[dev_index]
+    return str(dev_index)
+
+
 class ClockSampler:
     """nvidia-smi samples every 50 ms; stop() keeps the samples taken inside the timed window
     (mark_start / mark_stop) when there are any, else all of them (and says so)."""
@@ -125,8 +151,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, gpu: str):
+        self.gpu = gpu  # an id nvidia-smi -i accepts (smi_gpu_id)
         self.proc = None
         self.path = None
         self.t0 = self.t1 = None
@@ -144,7 +170,7 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except Exception as e:  # no nvidia-smi: record nothing
@@ -356,7 +382,7 @@ def run_gpu(args, w: synth.Workload):
         raise RuntimeError(f"device status after warm-up: {detail:#x}")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(smi_gpu_id(local_rank))
     clocks.start()
     time.sleep(0.3)
     launches0 = mlp.launches
@@ -526,7 +552,7 @@ def run_gpu_linear(args, w: synth.Workload):
         tp.tpmlp_linear_forward(lin.ctx, Xd, M, out, stream)
     torch.cuda.synchronize(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(smi_gpu_id(local_rank))
     clocks.start()
     time.sleep(0.3)
     n0 = tp.tpmlp_launch_count(lin.ctx)
@@ -650,7 +676,7 @@ def run_gpu_train(args, w: synth.Workload):
         step()
     torch.cuda.synchronize(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(smi_gpu_id(local_rank))
     clocks.start()
     time.sleep(0.3)
     n0 = mlp.launches

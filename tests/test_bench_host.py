@@ -96,3 +96,18 @@ def test_algorithmic_bytes():
     assert bench.alg_bytes(w, "gemm2", "block") == bench.alg_bytes(w, "gemm2") + 2 * w.M * w.H
     assert bench.step_flops(w, "swiglu") == 6 * w.M * w.H * w.F
     assert bench.step_flops(w, "gelu") == 4 * w.M * w.H * w.F
+
+
+def test_clock_sampler_queries_the_process_gpu(monkeypatch):
+    """nvidia-smi -i gets the device's UUID when torch has one, else the CUDA_VISIBLE_DEVICES
+    entry of the CUDA ordinal (ordinals are renumbered by it, nvidia-smi indices are not),
+    else the ordinal."""
+    u = "3f2a9c1e-0b7d-4e55-9a21-6c0d8e4b7f10"
+    assert bench.smi_gpu_id(0, uuid=u) == "GPU-" + u
+    assert bench.smi_gpu_id(0, uuid="GPU-" + u) == "GPU-" + u
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "3,5")
+    assert bench.smi_gpu_id(1, uuid="not-a-uuid") == "5"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "GPU-" + u)
+    assert bench.smi_gpu_id(0, uuid="") == "GPU-" + u
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
+    assert bench.smi_gpu_id(2, uuid="") == "2"
