@@ -21,6 +21,10 @@
  *    be 16-byte aligned.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). All
  *    device work is enqueued on it; no call synchronises unless its comment says so.
+ *  - A context belongs to the device that was current when it was created. Every call that
+ *    enqueues work or touches the context's device memory first checks that this device is
+ *    current on the calling thread and returns TPMLP_ERR_INVALID_ARG otherwise (nothing is
+ *    launched; tpmlp_last_error names both devices).
  *  - Every call returns TPMLP_OK (0) or a negative tpmlp_status; no C++ exception or abort
  *    ever crosses this interface. A failed call leaves the context usable unless it
  *    returned TPMLP_ERR_CUDA (a sticky CUDA error, after which the context should be
@@ -343,8 +347,12 @@ TPMLP_API int tpmlp_packed_buffer(const tpmlp_ctx *ctx, int32_t which, const voi
  * that array until the process exits.
  *  - B*S*F*2 > TPMLP_NOALLOC_SCRATCH_BYTES is rejected with TPMLP_ERR_UNSUPPORTED_SHAPE
  *    (tpmlp_last_error states the sizes); nothing is launched.
+ *  - The context's device must be current, as for every call (checked on every call).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *    with the context's device current; make that first call before any stream capture.
+ *    and caches it with the id of the CUDA context it was found in; make that first call
+ *    before any stream capture. After cudaDeviceReset the device's next context has another
+ *    id, and the next call looks the address up again (contexts created before the reset are
+ *    invalid anyway and must be destroyed).
  *  - All calls in the process share the one array per device, and it keeps the previous
  *    call's contents (nothing in it needs to start at zero). Calls whose kernels overlap on
  *    the GPU -- on different streams, or from different contexts -- race on it; serialise them.
@@ -401,6 +409,38 @@ TPMLP_API const char *tpmlp_last_error(const tpmlp_ctx *ctx);
 
 /* The number of kernel launches this context has issued so far (pack + forward). */
 TPMLP_API int64_t tpmlp_launch_count(const tpmlp_ctx *ctx);
+
+/*
+ * The rates two host-side planners work from (no counterpart on the pages; they shape the
+ * schedule, never the result):
+ *   gemm_flops  dense bf16 FLOP/s the GEMMs sustain on the whole device; sets the time of a
+ *               round of output tiles, which the split rule of the CTA-pair kernel (spread the
+ *               last, partial wave's reductions over all pairs?) and the row-chunk planner of
+ *               tpmlp_forward_host weigh against the two rates below
+ *   dram_Bps    HBM bytes/s a stream of reads reaches (the split rule's cost of re-reading a
+ *               split tail's operands)
+ *   copy_Bps    page-locked host <-> device bytes/s per direction with copies both ways at
+ *               once (tpmlp_forward_host's chunk sizes)
+ * tpmlp_create derives them from the device: SMs x 8192 FLOP per clock x the maximum SM clock
+ * x 0.67 (the share a bf16 GEMM holds under a GB300's power cap); 2 x memory clock x bus
+ * width x 0.8; and 168 GB/s (measured over NVLink-C2C). A caller that has measured its own
+ * may set them; 0 keeps a rate as it is. Results never depend on them: only which tiles are
+ * split (and so, by TPMLP_FLAG_FIXED_ORDER's rule, the last bits of split tiles) and the
+ * host-buffer chunk sizes do.
+ * Errors: INVALID_ARG (NULL context or pointer, a negative, NaN or absurd (> 1e18) rate).
+ */
+TPMLP_API int tpmlp_set_device_rates(tpmlp_ctx *ctx, double gemm_flops, double dram_Bps,
+                                     double copy_Bps);
+TPMLP_API int tpmlp_get_device_rates(const tpmlp_ctx *ctx, double *gemm_flops, double *dram_Bps,
+                                     double *copy_Bps);
+
+/*
+ * An id of the library build: 16 hex digits of SHA-256 over its CUDA/C++ sources and compile
+ * flags (no counterpart on the pages). Measurements recorded against one build of the kernels
+ * (DRAM traffic from a profiler, say) can be checked against the build that is running.
+ * Static string.
+ */
+TPMLP_API const char *tpmlp_build_id(void);
 
 #ifdef __cplusplus
 }

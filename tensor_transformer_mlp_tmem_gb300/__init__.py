@@ -27,7 +27,7 @@ __all__ = [
     "tpmlp_gemm2_residual",
     "tpmlp_linear_create", "tpmlp_linear_pack", "tpmlp_linear_forward", "Linear",
     "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW", "tpmlp_forward_train", "tpmlp_backward",
-    "tpmlp_backward_swiglu",
+    "tpmlp_backward_swiglu", "tpmlp_set_device_rates", "tpmlp_get_device_rates", "tpmlp_build_id",
 ]
 
 TPMLP_OK = 0
@@ -106,6 +106,12 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "tpmlp_last_error": ([vp], ctypes.c_char_p),
         "tpmlp_launch_count": ([vp], i64),
+        "tpmlp_set_device_rates": ([vp, ctypes.c_double, ctypes.c_double, ctypes.c_double],
+                                   ctypes.c_int),
+        "tpmlp_get_device_rates": ([vp, ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_double)], ctypes.c_int),
+        "tpmlp_build_id": ([], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -298,6 +304,26 @@ def tpmlp_last_error(ctx) -> str:
 
 def tpmlp_launch_count(ctx) -> int:
     return int(load_library().tpmlp_launch_count(ctx))
+
+
+def tpmlp_set_device_rates(ctx: int, gemm_flops: float = 0.0, dram_Bps: float = 0.0,
+                           copy_Bps: float = 0.0) -> None:
+    """Override the planners' rates (0 keeps a rate as it is)."""
+    _check(load_library().tpmlp_set_device_rates(ctx, gemm_flops, dram_Bps, copy_Bps),
+           "tpmlp_set_device_rates", ctx)
+
+
+def tpmlp_get_device_rates(ctx: int):
+    """(gemm_flops, dram_Bps, copy_Bps) the context's planners use."""
+    g, d, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(load_library().tpmlp_get_device_rates(ctx, ctypes.byref(g), ctypes.byref(d),
+                                                 ctypes.byref(c)), "tpmlp_get_device_rates", ctx)
+    return g.value, d.value, c.value
+
+
+def tpmlp_build_id() -> str:
+    """16 hex digits identifying the library's sources and compile flags."""
+    return load_library().tpmlp_build_id().decode()
 
 
 # ------------------------------------------------------------------ object wrapper

@@ -2,6 +2,7 @@
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -31,6 +32,24 @@ def _inputs():
             + [os.path.join(INCLUDE, "tpmlp.h"), __file__])
 
 
+def source_hash(extra_flags=()) -> str:
+    """16 hex digits of SHA-256 over the library's sources (csrc/, include/tpmlp.h, by
+    relative path and content) and the compile flags. Built into the library
+    (tpmlp_build_id), so that a measurement recorded against one build of the kernels can be
+    told apart from another build's."""
+    h = hashlib.sha256()
+    files = sorted(sources() + glob.glob(os.path.join(CSRC, "*.cuh")) +
+                   glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "tpmlp.h")])
+    for path in files:
+        h.update(os.path.relpath(path, ROOT).encode())
+        h.update(b"\0")
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+        h.update(b"\0")
+    h.update(" ".join([*ARCH_FLAGS, "-O3", *extra_flags]).encode())
+    return h.hexdigest()[:16]
+
+
 def stale() -> bool:
     if not os.path.exists(LIB):
         return True
@@ -48,7 +67,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str =
     tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", INCLUDE,
-           "-I", CSRC, "-DTPMLP_BUILD", *extra_flags, *sources(), "-o", tmp]
+           "-I", CSRC, "-DTPMLP_BUILD", f'-DTPMLP_SOURCE_HASH="{source_hash(extra_flags)}"',
+           *extra_flags, *sources(), "-o", tmp]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd))

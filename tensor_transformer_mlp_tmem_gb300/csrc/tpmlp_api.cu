@@ -81,6 +81,8 @@ struct tpmlp_ctx {
     uint32_t* sk_count = nullptr; // [num_sms split tiles][2 CTAs][epilogue warps] arrivals
     uint32_t sk_epoch = 0;
 
+    tpmlp::DeviceRates rates{};  // the planners' rates (device_rates, or tpmlp_set_device_rates)
+
     int* status = nullptr;  // device status word
     int64_t launches = 0;
     std::string last_error;
@@ -264,8 +266,12 @@ int max_resident_pairs(tpmlp_ctx* c, Kernel kern, uint32_t smem) {
 //    one DRAM read of the tail's operands, under half a round) favours it: the GPT-3 second
 //    GEMM (R = 8, 768 blocks) 4.7 % faster; the GPT-3 first GEMM (R = 32, 192 blocks, at 70 %
 //    of a round by the model) 1.3 % slower, hence the half.
-constexpr tpmlp::SplitRule kSplitRule{TPMLP_SPLIT_TAIL_PCT, 16, 64.0 * (1 << 20),
-                                      1.7e15 / 76, 6.0e12, 0.5, 4, 32};
+// The rule's rates are the context's (device_rates at create, or tpmlp_set_device_rates).
+tpmlp::SplitRule split_rule_of(const tpmlp_ctx* c, int pairs) {
+    tpmlp::SplitRule r = tpmlp::split_rule(c->rates, pairs);
+    r.tail_pct = TPMLP_SPLIT_TAIL_PCT;
+    return r;
+}
 
 // The split's flags carry an epoch chosen here, per launch. A launch recorded into a CUDA graph
 // would replay with the same epoch and could read partial sums before they are written, so
@@ -288,7 +294,7 @@ int plan_split(tpmlp_ctx* c, GemmArgs& a, int resident, cudaStream_t s) {
     if (!c->sk_partial || resident > c->num_sms / 2 || capturing(s)) return pairs;
     const tpmlp::SplitLaunch L{a.num_tiles, resident, a.kb_tile,       a.m_blocks,
                                a.n_blocks,  a.group_m, tpmlp::kPairBM, tpmlp::kPairBN};
-    const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, kSplitRule);
+    const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, split_rule_of(c, c->num_sms / 2));
     // the counters hold num_sms split tiles (the plan never splits more than 2 * pairs)
     if (p.sk_first == a.num_tiles || a.num_tiles - p.sk_first > c->num_sms) return pairs;
     if (p.pairs > resident) return pairs;
@@ -343,9 +349,43 @@ GemmArgs base_args(const tpmlp_ctx* c, int64_t M, int ldo, int bm, int bn, int g
 
 constexpr int kKindBlock = 0, kKindColumn = 1, kKindRow = 2;
 
-// An MLP-block context whose weights are packed.
-int check_ctx(const tpmlp_ctx* c) {
+#ifdef TPMLP_TEST_HOOKS
+// Test builds only: a device index that the current-device query reports instead of the real
+// one (-1: the real one), so that host tests drive the device check without a GPU.
+std::atomic<int> g_test_current_device{-1};
+#endif
+
+cudaError_t current_device(int* dev) {
+#ifdef TPMLP_TEST_HOOKS
+    const int fake = g_test_current_device.load();
+    if (fake >= 0) {
+        *dev = fake;
+        return cudaSuccess;
+    }
+#endif
+    return cudaGetDevice(dev);
+}
+
+// The context's device must be current on the calling thread: the context's buffers, tensor
+// maps and kernel attributes belong to that device, and a launch would otherwise run on
+// another GPU with them. Every entry point that enqueues work or touches the context's device
+// memory checks this first.
+int check_device(tpmlp_ctx* c) {
+    int cur = -1;
+    const cudaError_t e = current_device(&cur);
+    if (e != cudaSuccess) return fail_cuda(c, e, "cudaGetDevice");
+    if (cur != c->device) {
+        c->last_error = "the context belongs to device " + std::to_string(c->device) + " but device " +
+                        std::to_string(cur) + " is current (call cudaSetDevice first)";
+        return TPMLP_ERR_INVALID_ARG;
+    }
+    return TPMLP_OK;
+}
+
+// An MLP-block context on the current device whose weights are packed.
+int check_ctx(tpmlp_ctx* c) {
     if (!c || c->kind != kKindBlock) return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     if (!c->packed) return TPMLP_ERR_NOT_PACKED;
     return TPMLP_OK;
 }
@@ -483,14 +523,7 @@ int check_tokens(int64_t B, int64_t S) {
 
 int z_elem_bytes(const tpmlp_ctx* c) { return (c->flags & TPMLP_FLAG_Z_FP32) ? 4 : 2; }
 
-// Copy-engine bandwidth of page-locked host memory on GB300 (NVLink-C2C), measured with
-// 16-128 MB copies: about 168 GB/s per direction with copies in and out at once (205 GB/s in
-// alone). The chunk planner only needs its ratio to the GEMMs' round times.
-constexpr double kCopyBothBps = 168e9;
-// Sustained dense bf16 rate of the GPU under the power cap (for the round times).
-constexpr double kGemmFlops = 1.7e15;
-
-// Row chunks of tpmlp_forward_host for M tokens (tpmlp_plan.h).
+// Row chunks of tpmlp_forward_host for M tokens (tpmlp_plan.h), timed with the context's rates.
 int plan_host_chunks(const tpmlp_ctx* c, int64_t M, int64_t* rows) {
     tpmlp::ChunkModel m{};
     const int64_t pairs = c->num_sms / 2;
@@ -504,11 +537,11 @@ int plan_host_chunks(const tpmlp_ctx* c, int64_t M, int64_t* rows) {
         const int64_t w = pair[i] ? tpmlp::kPairBN : bn[i];
         g.col_tiles = N[i] / w;
         g.slots = pair[i] ? pairs : c->num_sms;
-        g.tile_s = 2.0 * g.tile_rows * w * K[i] / (kGemmFlops / g.slots);
+        g.tile_s = 2.0 * g.tile_rows * w * K[i] / (c->rates.gemm_flops / g.slots);
     }
     m.x_row_bytes = 2.0 * c->H;
     m.z_row_bytes = static_cast<double>(c->H) * z_elem_bytes(c);
-    m.copy_Bps = kCopyBothBps;
+    m.copy_Bps = c->rates.copy_Bps;
     return tpmlp::plan_chunks(m, M, kHostChunksMax, 64, rows);
 }
 
@@ -814,6 +847,17 @@ int create_context(tpmlp_ctx** out, int64_t H, int64_t F, int32_t k, uint32_t fl
     if (!c) return TPMLP_ERR_OOM;
     c->device = dev;
     c->num_sms = prop.multiProcessorCount;
+    {
+        // the planners' rates from the device's SM count, clock and memory system (an
+        // attribute that cannot be read counts as not reported: 0)
+        int sm_khz = 0, mem_khz = 0, bus_bits = 0;
+        if (cudaDeviceGetAttribute(&sm_khz, cudaDevAttrClockRate, dev) != cudaSuccess) sm_khz = 0;
+        if (cudaDeviceGetAttribute(&mem_khz, cudaDevAttrMemoryClockRate, dev) != cudaSuccess) mem_khz = 0;
+        if (cudaDeviceGetAttribute(&bus_bits, cudaDevAttrGlobalMemoryBusWidth, dev) != cudaSuccess)
+            bus_bits = 0;
+        cudaGetLastError();
+        c->rates = tpmlp::device_rates(c->num_sms, sm_khz, mem_khz, bus_bits);
+    }
     c->H = H;
     c->F = F;
     c->k = k;
@@ -865,6 +909,7 @@ int tpmlp_pack_shards(tpmlp_ctx* c, const void* W1, const void* b1, const void* 
                       void* stream) {
     if (!c || !W1 || !b1 || !W2 || !b2 || c->gated || c->kind != kKindBlock)
         return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     if (!aligned16(W1) || !aligned16(W2) || (reinterpret_cast<uintptr_t>(b1) & 1) ||
         (reinterpret_cast<uintptr_t>(b2) & 1))
         return TPMLP_ERR_MISALIGNED;
@@ -895,6 +940,7 @@ int tpmlp_pack_shards_swiglu(tpmlp_ctx* c, const void* Wg, const void* bg, const
                              const void* bu, const void* W2, const void* b2, void* stream) {
     if (!c || !Wg || !bg || !Wu || !bu || !W2 || !b2 || !c->gated || c->kind != kKindBlock)
         return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     if (!aligned16(Wg) || !aligned16(Wu) || !aligned16(W2) ||
         ((reinterpret_cast<uintptr_t>(bg) | reinterpret_cast<uintptr_t>(bu) |
           reinterpret_cast<uintptr_t>(b2)) & 1))
@@ -926,6 +972,7 @@ int tpmlp_pack_shards_swiglu(tpmlp_ctx* c, const void* Wg, const void* bg, const
 
 int tpmlp_reserve(tpmlp_ctx* c, int64_t max_tokens) {
     if (!c || c->kind != kKindBlock || max_tokens < 0) return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     if (max_tokens > (int64_t(1) << 31)) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     return ensure_y(c, max_tokens);
 }
@@ -975,6 +1022,7 @@ int tpmlp_set_layernorm(tpmlp_ctx* c, const void* gamma, const void* beta, float
                         void* stream) {
     // the block's input, or a column-parallel layer's input (LayerNorm before Q/K/V)
     if (!c || !gamma || !beta || c->kind == kKindRow) return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     if (!(eps >= 0.0f) || eps > 1.0f) return TPMLP_ERR_INVALID_ARG;  // also rejects NaN
     if (c->H > tpmlp::kNormMaxH) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if ((reinterpret_cast<uintptr_t>(gamma) | reinterpret_cast<uintptr_t>(beta)) & 1)
@@ -999,6 +1047,7 @@ int tpmlp_set_layernorm(tpmlp_ctx* c, const void* gamma, const void* beta, float
 
 int tpmlp_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, void* stream) {
     if (!c || M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     if (!c->ln_set) {
         c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
         return TPMLP_ERR_NOT_PACKED;
@@ -1050,6 +1099,7 @@ int tpmlp_gemm2_residual(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, const 
 
 int tpmlp_linear_pack(tpmlp_ctx* c, const void* W, const void* b, void* stream) {
     if (!c || !W || !b || c->kind == kKindBlock) return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     if (!aligned16(W) || (reinterpret_cast<uintptr_t>(b) & 1)) return TPMLP_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     c->packed = false;
@@ -1077,6 +1127,7 @@ int tpmlp_linear_pack(tpmlp_ctx* c, const void* W, const void* b, void* stream) 
 
 int tpmlp_linear_forward(tpmlp_ctx* c, const void* X, int64_t M, void* out, void* stream) {
     if (!c || c->kind == kKindBlock || M < 0) return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     if (!c->packed) return TPMLP_ERR_NOT_PACKED;
     if (M == 0) return TPMLP_OK;
     if (!X || !out) return TPMLP_ERR_INVALID_ARG;
@@ -1300,6 +1351,7 @@ int tpmlp_backward_swiglu(tpmlp_ctx* c, const void* dZ, const void* X, const voi
 
 int tpmlp_get_status(tpmlp_ctx* c, void* stream, int32_t* detail) {
     if (!c) return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     TPMLP_CUDA(c, cudaStreamSynchronize(s));
     int v = 0;
@@ -1379,7 +1431,61 @@ const char* tpmlp_last_error(const tpmlp_ctx* c) { return c ? c->last_error.c_st
 
 int64_t tpmlp_launch_count(const tpmlp_ctx* c) { return c ? c->launches : 0; }
 
+int tpmlp_set_device_rates(tpmlp_ctx* c, double gemm_flops, double dram_Bps, double copy_Bps) {
+    if (!c) return TPMLP_ERR_INVALID_ARG;
+    for (double v : {gemm_flops, dram_Bps, copy_Bps})
+        if (!(v >= 0.0) || v > 1e18) return TPMLP_ERR_INVALID_ARG;  // also rejects NaN
+    if (gemm_flops > 0.0) c->rates.gemm_flops = gemm_flops;
+    if (dram_Bps > 0.0) c->rates.dram_Bps = dram_Bps;
+    if (copy_Bps > 0.0) c->rates.copy_Bps = copy_Bps;
+    c->plan_M = -1;  // re-plan the host-buffer chunks on the next call
+    return TPMLP_OK;
+}
+
+int tpmlp_get_device_rates(const tpmlp_ctx* c, double* gemm_flops, double* dram_Bps,
+                           double* copy_Bps) {
+    if (!c || !gemm_flops || !dram_Bps || !copy_Bps) return TPMLP_ERR_INVALID_ARG;
+    *gemm_flops = c->rates.gemm_flops;
+    *dram_Bps = c->rates.dram_Bps;
+    *copy_Bps = c->rates.copy_Bps;
+    return TPMLP_OK;
+}
+
+#ifndef TPMLP_SOURCE_HASH
+#define TPMLP_SOURCE_HASH "unknown"
+#endif
+const char* tpmlp_build_id(void) { return TPMLP_SOURCE_HASH; }
+
 }  // extern "C"
+
+#ifdef TPMLP_TEST_HOOKS
+// Test builds only (-DTPMLP_TEST_HOOKS): a block or linear context that holds no device
+// memory, recorded as belonging to `device`, and the substitute for the current-device query.
+// With them, host tests drive the argument and device checks of every entry point on a
+// machine without a GPU. tpmlp_destroy releases such a context.
+extern "C" TPMLP_API tpmlp_ctx* tpmlp_test_host_context(int64_t H, int64_t F, int32_t k,
+                                                        int32_t device, int32_t kind,
+                                                        int32_t packed, uint32_t flags) {
+    tpmlp_ctx* c = new (std::nothrow) tpmlp_ctx();
+    if (!c) return nullptr;
+    c->flags = flags;
+    c->gated = (flags & TPMLP_FLAG_SWIGLU) != 0;
+    c->device = device;
+    c->num_sms = 152;
+    c->H = H;
+    c->F = F;
+    c->k = k;
+    c->f = F / k;
+    c->kind = kind;
+    c->packed = packed != 0;
+    c->rates = tpmlp::device_rates(0, 0, 0, 0);
+    return c;
+}
+
+extern "C" TPMLP_API void tpmlp_test_set_current_device(int32_t device) {
+    g_test_current_device.store(device);
+}
+#endif
 
 // ---------------------------------------------------------------------------------------
 // Allocation-free forward pass.
@@ -1397,30 +1503,63 @@ static __device__ __align__(256) unsigned char g_noalloc_y[TPMLP_NOALLOC_SCRATCH
 
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+struct NoallocSlot {
+    unsigned long long ctx_id;  // the CUDA context the address was looked up in
+    void* ptr;                  // device address of g_noalloc_y in that context
+};
+NoallocSlot g_noalloc[kNoallocMaxDevices] = {};
 
-// The device address of g_noalloc_y on the context's device. In host code the array's
-// name is only a host-side stand-in, so the address is looked up once per device, with
-// that device current, and cached.
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_fn_once;
+
+// The unique id of the CUDA context current on this thread (0: none current, or the driver
+// cannot tell). Ids are never reused within a process, so a context created after a device
+// reset gets a new one.
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_fn_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+        cudaGetLastError();
+    });
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// The device address of g_noalloc_y on the context's device, which the caller has checked to
+// be current. In host code the array's name is only a host-side stand-in, so the address is
+// looked up (cudaGetSymbolAddress) on the first call on each device and cached with the id of
+// the CUDA context it belongs to. A later call in another context of that device (after
+// cudaDeviceReset) looks it up again; a call whose context id cannot be read looks it up every
+// time.
 int noalloc_scratch(tpmlp_ctx* c, void** out) {
     if (c->device < 0 || c->device >= kNoallocMaxDevices) return TPMLP_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[c->device]) {
-        int cur = -1;
-        TPMLP_CUDA(c, cudaGetDevice(&cur));
-        if (cur != c->device) {
-            c->last_error = "tpmlp_forward_noalloc: the context's device must be current";
-            return TPMLP_ERR_INVALID_ARG;
-        }
+    NoallocSlot& slot = g_noalloc[c->device];
+    unsigned long long id = current_context_id();
+    if (!slot.ptr || id == 0 || id != slot.ctx_id) {
         void* p = nullptr;
         TPMLP_CUDA(c, cudaGetSymbolAddress(&p, g_noalloc_y));
         if (!p) {
             c->last_error = "cudaGetSymbolAddress returned a null scratch address";
             return TPMLP_ERR_CUDA;
         }
-        g_noalloc_ptr[c->device] = p;
+        if (id == 0) id = current_context_id();  // the lookup made the primary context current
+        slot.ptr = p;
+        slot.ctx_id = id;
     }
-    *out = g_noalloc_ptr[c->device];
+    *out = slot.ptr;
     return TPMLP_OK;
 }
 

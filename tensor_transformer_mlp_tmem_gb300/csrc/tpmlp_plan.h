@@ -31,6 +31,12 @@
 //   comp_c = max(comp_{c-1}, in_c) + sum over both GEMMs of rounds(chunk c) * round time
 //   out_c  = max(out_{c-1}, comp_c) + Z bytes of chunk c / bandwidth out
 // and the pass ends at max(comp_last, out_last).
+//
+// ---------------------------------------------------------------- 3. device rates
+//
+// Both planners weigh the time of a round of tiles against DRAM reads or host-link copies.
+// The rates come from the device a context runs on (device_rates), so that a part with
+// another SM count, clock or memory system plans from its own round times.
 #pragma once
 
 #include <cstdint>
@@ -183,6 +189,60 @@ inline SplitPlan plan_split_tiles(const SplitLaunch& L, const SplitRule& rule) {
     p.sk_first = first;
     p.sk_iters = rem * L.kb_tile;
     return p;
+}
+
+// ---------------------------------------------------------------- device rates
+//
+//   gemm_flops  dense bf16 rate the GEMMs hold: SMs x 8192 FLOP per SM per clock (one
+//               tcgen05 kind::f16 MMA of 128 x 256 x 16 per SM every 128 cycles) x the
+//               maximum SM clock x kGemmClockShare, the share of that the GEMMs keep under
+//               the board's power cap (a cuBLAS bf16 loop: 1.73 PFLOP/s over 152 SMs at a
+//               2.07 GHz maximum, 0.67 of it);
+//   dram_Bps    HBM bandwidth a stream of reads reaches: two transfers per memory clock x
+//               the bus width x kDramShare (a device-to-device copy moves 6.75 TB/s against
+//               the 8.18 TB/s this gives for 8192 bits at 3.996 GHz: 0.8);
+//   copy_Bps    page-locked host <-> device copies per direction, with copies both ways at
+//               once. No device attribute gives it: 168 GB/s, measured over NVLink-C2C with
+//               16-128 MB copies (205 GB/s one way alone).
+// An attribute the device does not report (0) takes the value of a GB300 (152 SMs, 2.07 GHz,
+// 3.996 GHz x 8192 bits).
+struct DeviceRates {
+    double gemm_flops;
+    double dram_Bps;
+    double copy_Bps;
+};
+
+constexpr double kGemmFlopsPerSmClock = 8192.0;
+constexpr double kGemmClockShare = 0.67;
+constexpr double kDramShare = 0.8;
+constexpr double kHostCopyBps = 168e9;
+
+inline DeviceRates device_rates(int num_sms, double sm_clock_khz, double mem_clock_khz,
+                                int mem_bus_bits) {
+    if (num_sms <= 0) num_sms = 152;
+    if (!(sm_clock_khz > 0)) sm_clock_khz = 2070000.0;
+    if (!(mem_clock_khz > 0)) mem_clock_khz = 3996000.0;
+    if (mem_bus_bits <= 0) mem_bus_bits = 8192;
+    DeviceRates r;
+    r.gemm_flops = num_sms * kGemmFlopsPerSmClock * sm_clock_khz * 1e3 * kGemmClockShare;
+    r.dram_Bps = 2.0 * mem_clock_khz * 1e3 * (mem_bus_bits / 8.0) * kDramShare;
+    r.copy_Bps = kHostCopyBps;
+    return r;
+}
+
+// The split rule of a device with `pairs` CTA pairs (tpmlp_gemm_pair_kernel): the thresholds
+// are the measured ones (see plan_split_tiles); the tail model's rates scale with the device.
+inline SplitRule split_rule(const DeviceRates& r, int pairs) {
+    SplitRule s{};
+    s.tail_pct = 85;              // whole split: the second wave at most 85 % full
+    s.min_blocks = 16;            // ... tiles at least 16 blocks deep
+    s.max_operand_bytes = 64.0 * (1 << 20);  // ... operands within 64 MiB of L2
+    s.pair_flops = r.gemm_flops / (pairs > 0 ? pairs : 1);
+    s.dram_Bps = r.dram_Bps;
+    s.tail_gain = 0.5;            // tail split: under half a round of whole tiles
+    s.max_parts = 4;              // fewer tiles than pairs: at most 4 pairs per tile
+    s.min_part_blocks = 32;       // ... of at least 32 blocks each
+    return s;
 }
 
 struct ChunkGemm {

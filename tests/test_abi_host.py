@@ -86,3 +86,140 @@ def test_null_context_everywhere(lib):
 def test_binding_names_match_c_abi():
     for name in declared_symbols():
         assert hasattr(tp, name), f"binding lacks {name}"
+
+
+# ------------------------------------------------------------------ device checks (test build)
+@pytest.fixture(scope="module")
+def hooks(tmp_path_factory):
+    """A test build (-DTPMLP_TEST_HOOKS) that can make contexts holding no device memory,
+    recorded on any device index, and substitute the current-device query: the device check
+    of every entry point runs on a machine without a GPU."""
+    path = _build.build(out=str(tmp_path_factory.mktemp("hooks") / "libtpmlp_hooks.so"),
+                        extra_flags=["-DTPMLP_TEST_HOOKS"])
+    h = ctypes.CDLL(path)
+    vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+    h.tpmlp_test_host_context.argtypes = [i64, i64, i32, i32, i32, i32, u32]
+    h.tpmlp_test_host_context.restype = vp
+    h.tpmlp_test_set_current_device.argtypes = [i32]
+    h.tpmlp_last_error.argtypes = [vp]
+    h.tpmlp_last_error.restype = ctypes.c_char_p
+    h.tpmlp_launch_count.argtypes = [vp]
+    h.tpmlp_launch_count.restype = i64
+    h.tpmlp_destroy.argtypes = [vp]
+    h.tpmlp_set_device_rates.argtypes = [vp, ctypes.c_double, ctypes.c_double, ctypes.c_double]
+    h.tpmlp_get_device_rates.argtypes = [vp] + [ctypes.POINTER(ctypes.c_double)] * 3
+    yield h
+    h.tpmlp_test_set_current_device(-1)
+
+
+BLOCK_CALLS = {
+    # entry point -> arguments after the context (16: a non-null, 16-byte aligned address)
+    "tpmlp_pack_shards": (16, 16, 16, 16, None),
+    "tpmlp_reserve": (1024,),
+    "tpmlp_forward": (16, 1, 64, 16, None),
+    "tpmlp_forward_host": (16, 1, 64, 16, None),
+    "tpmlp_forward_noalloc": (16, 1, 64, 16, None),
+    "tpmlp_gemm1": (16, 64, 16, None),
+    "tpmlp_gemm2": (16, 64, 16, None),
+    "tpmlp_gemm2_residual": (16, 64, 16, 16, None),
+    "tpmlp_set_layernorm": (16, 16, ctypes.c_float(1e-5), None),
+    "tpmlp_layernorm": (16, 64, 16, None),
+    "tpmlp_block_forward": (16, 1, 64, 16, None),
+    "tpmlp_block_forward_host": (16, 1, 64, 16, None),
+    "tpmlp_forward_train": (16, 1, 64, 16, 16, 16, None),
+    "tpmlp_backward": (16, 16, 16, 16, 16, 16, 1, 64, 16, 16, 16, 16, 16, None),
+    "tpmlp_get_status": (None, None),
+}
+GATED_CALLS = {
+    "tpmlp_pack_shards_swiglu": (16, 16, 16, 16, 16, 16, None),
+    "tpmlp_backward_swiglu": (16, 16, 16, 16, 16, 16, 16, 1, 64, 16, 16, 16, 16, 16, 16, 16,
+                              None),
+}
+LINEAR_CALLS = {
+    "tpmlp_linear_pack": (16, 16, None),
+    "tpmlp_linear_forward": (16, 64, 16, None),
+}
+
+
+def call(h, name, ctx, args):
+    fn = getattr(h, name)
+    fn.restype = ctypes.c_int
+    conv = []
+    for a in args:
+        if isinstance(a, ctypes.c_float):
+            conv.append(a)
+        elif a is None:
+            conv.append(ctypes.c_void_p(None))
+        else:
+            conv.append(ctypes.c_int64(a) if not isinstance(a, ctypes._SimpleCData) else a)
+    return fn(ctypes.c_void_p(ctx), *conv)
+
+
+@pytest.mark.parametrize("kind,flags,calls", [(0, 0, BLOCK_CALLS), (0, 0x4, GATED_CALLS),
+                                              (1, 0, LINEAR_CALLS), (2, 0, LINEAR_CALLS)],
+                         ids=["block", "gated", "column", "row"])
+def test_every_entry_point_checks_the_current_device(hooks, kind, flags, calls):
+    """A context of device 3 called while device 0 is current: every entry point that would
+    enqueue work or touch the context's memory returns INVALID_ARG before doing anything, and
+    says why; with device 3 current the same calls get past the check."""
+    H, F, k = 256, 1024, 4
+    ctx = hooks.tpmlp_test_host_context(H, F, k, 3, kind, 1, flags)
+    assert ctx
+    try:
+        hooks.tpmlp_test_set_current_device(0)
+        for name, args in calls.items():
+            assert call(hooks, name, ctx, args) == tp.TPMLP_ERR_INVALID_ARG, name
+            msg = hooks.tpmlp_last_error(ctx).decode()
+            assert "device 3" in msg and "device 0" in msg, (name, msg)
+        assert hooks.tpmlp_launch_count(ctx) == 0
+        # the right device current: an empty batch is a no-op again
+        hooks.tpmlp_test_set_current_device(3)
+        if kind == 0 and not flags:
+            assert call(hooks, "tpmlp_forward", ctx, (16, 0, 64, 16, None)) == tp.TPMLP_OK
+            assert call(hooks, "tpmlp_forward_noalloc", ctx, (16, 0, 64, 16, None)) == tp.TPMLP_OK
+            assert call(hooks, "tpmlp_gemm1", ctx, (16, 0, 16, None)) == tp.TPMLP_OK
+        if kind != 0:
+            assert call(hooks, "tpmlp_linear_forward", ctx, (16, 0, 16, None)) == tp.TPMLP_OK
+        assert hooks.tpmlp_launch_count(ctx) == 0
+    finally:
+        hooks.tpmlp_test_set_current_device(-1)
+        hooks.tpmlp_destroy(ctypes.c_void_p(ctx))
+
+
+def test_unpacked_context_on_its_device(hooks):
+    """With the device current, the next check applies: weights not packed."""
+    ctx = hooks.tpmlp_test_host_context(256, 1024, 4, 2, 0, 0, 0)
+    try:
+        hooks.tpmlp_test_set_current_device(2)
+        assert call(hooks, "tpmlp_forward", ctx, (16, 1, 64, 16, None)) == tp.TPMLP_ERR_NOT_PACKED
+    finally:
+        hooks.tpmlp_test_set_current_device(-1)
+        hooks.tpmlp_destroy(ctypes.c_void_p(ctx))
+
+
+def test_device_rates_set_and_get(hooks):
+    ctx = hooks.tpmlp_test_host_context(256, 1024, 4, 0, 0, 1, 0)
+    try:
+        vals = [ctypes.c_double() for _ in range(3)]
+        refs = [ctypes.byref(v) for v in vals]
+        assert hooks.tpmlp_get_device_rates(ctypes.c_void_p(ctx), *refs) == tp.TPMLP_OK
+        g0, d0, c0 = (v.value for v in vals)
+        assert g0 == pytest.approx(152 * 8192 * 2.07e9 * 0.67) and d0 > 1e12 and c0 == 168e9
+        # 0 keeps a rate; a negative or NaN rate is rejected and changes nothing
+        assert hooks.tpmlp_set_device_rates(ctypes.c_void_p(ctx), 2e15, 0.0, 100e9) == tp.TPMLP_OK
+        assert hooks.tpmlp_set_device_rates(ctypes.c_void_p(ctx), -1.0, 0.0, 0.0) == \
+            tp.TPMLP_ERR_INVALID_ARG
+        assert hooks.tpmlp_set_device_rates(ctypes.c_void_p(ctx), float("nan"), 0.0, 0.0) == \
+            tp.TPMLP_ERR_INVALID_ARG
+        assert hooks.tpmlp_get_device_rates(ctypes.c_void_p(ctx), *refs) == tp.TPMLP_OK
+        assert (vals[0].value, vals[1].value, vals[2].value) == (2e15, d0, 100e9)
+        assert hooks.tpmlp_set_device_rates(None, 1.0, 1.0, 1.0) == tp.TPMLP_ERR_INVALID_ARG
+    finally:
+        hooks.tpmlp_destroy(ctypes.c_void_p(ctx))
+
+
+def test_build_id_names_the_sources(lib):
+    """The running library's id is the hash of the sources and flags it was built from."""
+    bid = tp.tpmlp_build_id()
+    assert re.fullmatch(r"[0-9a-f]{16}", bid)
+    assert bid == _build.source_hash()

@@ -1,9 +1,12 @@
-"""The row-chunk planner of the host-buffer forward pass (csrc/tpmlp_plan.h), on the CPU.
+"""The row-chunk planner of the host-buffer forward pass and the device rates both planners
+work from (csrc/tpmlp_plan.h), on the CPU.
 
 The planner is plain C++; the test builds it into a small shared object with g++ and checks
 that every plan is a valid partition of the rows, that it is the best split under the
 planner's own pipeline model (brute force over all splits on small cases), and that on the
-7b-shaped block it beats the even four-way split the forward pass used before."""
+7b-shaped block it beats the even four-way split the forward pass used before. The rates
+scale with the device's SM count, clock and memory system: a 160-SM part plans its split
+tails and chunks from its own round times."""
 import ctypes
 import itertools
 import os
@@ -34,6 +37,19 @@ int shim_plan(const double* p, int64_t M, int max_chunks, int64_t max_granules, 
 double shim_sim(const double* p, const int64_t* rows, int n) {
     return tpmlp::simulate_chunks(model(p), rows, n);
 }
+void shim_rates(int sms, double sm_khz, double mem_khz, int bus_bits, double* out) {
+    const tpmlp::DeviceRates r = tpmlp::device_rates(sms, sm_khz, mem_khz, bus_bits);
+    out[0] = r.gemm_flops; out[1] = r.dram_Bps; out[2] = r.copy_Bps;
+}
+// split plan of a launch on a device of `sms` SMs at the given clocks (pairs = resident pairs)
+void shim_split(int sms, double sm_khz, int num_tiles, int pairs, int kb_tile, int m_blocks,
+                int n_blocks, int group_m, int* out) {
+    const tpmlp::SplitRule rule =
+        tpmlp::split_rule(tpmlp::device_rates(sms, sm_khz, 3996000.0, 8192), sms / 2);
+    const tpmlp::SplitLaunch L{num_tiles, pairs, kb_tile, m_blocks, n_blocks, group_m, 256, 256};
+    const tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, rule);
+    out[0] = p.sk_first; out[1] = p.sk_iters; out[2] = p.pairs;
+}
 }
 """
 
@@ -51,6 +67,11 @@ def plan(tmp_path_factory):
     lib.shim_plan.restype = ctypes.c_int
     lib.shim_sim.argtypes = [dp, i64p, ctypes.c_int]
     lib.shim_sim.restype = ctypes.c_double
+    lib.shim_rates.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int, dp]
+    lib.shim_rates.restype = None
+    lib.shim_split.argtypes = [ctypes.c_int, ctypes.c_double] + [ctypes.c_int] * 6 + \
+        [ctypes.POINTER(ctypes.c_int)]
+    lib.shim_split.restype = None
     return lib
 
 
@@ -129,3 +150,73 @@ def test_granules_bound_the_search(plan):
     rows = call_plan(plan, params(), M, max_granules=64)
     assert sum(rows) == M
     assert all(r % (64 * 256) == 0 for r in rows[:-1])
+
+
+# ------------------------------------------------------------------ device rates
+def rates(lib, sms, sm_khz=2070000.0, mem_khz=3996000.0, bus_bits=8192):
+    out = (ctypes.c_double * 3)()
+    lib.shim_rates(sms, sm_khz, mem_khz, bus_bits, out)
+    return tuple(out)
+
+
+def split(lib, sms, T, P, kb, mb, nb, group_m=8, sm_khz=2070000.0):
+    out = (ctypes.c_int * 3)()
+    lib.shim_split(sms, sm_khz, T, P, kb, mb, nb, group_m, out)
+    return tuple(out)
+
+
+def test_rates_of_a_gb300(plan):
+    """152 SMs x 8192 FLOP per clock at 2.07 GHz, 0.67 of it under the power cap: within 2 %
+    of the 1.7 PFLOP/s the planners assumed before the rates came from the device; HBM3e at
+    3.996 GHz over 8192 bits, 0.8 of it reachable: 6.5 TB/s."""
+    g, d, c = rates(plan, 152)
+    assert g == pytest.approx(152 * 8192 * 2.07e9 * 0.67, rel=1e-12)
+    assert g == pytest.approx(1.7e15, rel=0.02)
+    assert d == pytest.approx(2 * 3.996e9 * 1024 * 0.8, rel=1e-12)
+    assert c == 168e9
+
+
+def test_rates_scale_with_the_device(plan):
+    g152, d152, _ = rates(plan, 152)
+    g160, _, _ = rates(plan, 160)
+    assert g160 / g152 == pytest.approx(160 / 152, rel=1e-12)
+    g_slow, _, _ = rates(plan, 152, sm_khz=1035000.0)
+    assert g_slow == pytest.approx(g152 / 2, rel=1e-12)
+    _, d_narrow, _ = rates(plan, 152, bus_bits=4096)
+    assert d_narrow == pytest.approx(d152 / 2, rel=1e-12)
+    # attributes the device does not report take a GB300's values
+    assert rates(plan, 0, 0.0, 0.0, 0) == rates(plan, 152)
+
+
+def test_split_follows_the_pair_count(plan):
+    """The GPT-3 second GEMM (768 tiles of 256 x 256, 768 blocks deep, 16 x 48 tiles): on 76
+    pairs its 8-tile tail is spread over all pairs; on a 160-SM part (80 pairs) the tail is 48
+    tiles, 0.6 of a round, and stays whole. The 7b second GEMM (512 tiles, 256 blocks):
+    whole on both (a 56- or 32-tile tail)."""
+    assert split(plan, 152, 768, 76, 768, 16, 48)[:2] == (760, 8 * 768)
+    assert split(plan, 160, 768, 80, 768, 16, 48)[0] == 768
+    assert split(plan, 152, 512, 76, 256, 32, 16)[0] == 512
+    assert split(plan, 160, 512, 80, 256, 32, 16)[0] == 512
+    # a launch of 1.2 waves is split entirely on either part (GPT-2's second GEMM shape)
+    assert split(plan, 152, 96, 76, 48, 32, 3)[:2] == (0, 96 * 48)
+    assert split(plan, 160, 96, 80, 48, 32, 3)[:2] == (0, 96 * 48)
+    # fewer tiles than pairs: 16 tiles of 256 blocks over 4 pairs each, on 76 or 80 pairs
+    assert split(plan, 160, 16, 80, 256, 1, 16) == (0, 16 * 256, 64)
+
+
+def test_chunk_plan_on_a_160_sm_part(plan):
+    """The host-buffer chunks of the 7b block on a 160-SM part (80 pairs, its own round
+    times): a valid partition and the best split under the model."""
+    g, _, c = rates(plan, 160)
+    p = params(pairs=80, rate=g)
+    p[10] = c
+    for M in (8192, 8192 + 300, 4096):
+        rows = call_plan(plan, p, M)
+        assert sum(rows) == M and all(r % 256 == 0 for r in rows[:-1])
+        blocks = -(-M // 256)
+        best = call_sim(plan, p, [M])
+        for n in range(2, 5):
+            for cuts in itertools.combinations(range(1, blocks), n - 1):
+                edges = [0] + [k * 256 for k in cuts] + [M]
+                best = min(best, call_sim(plan, p, [b - a for a, b in zip(edges, edges[1:])]))
+        assert call_sim(plan, p, rows) <= best * (1 + 1e-9)

@@ -33,7 +33,9 @@ int shim_pair_of(int sk_iters, int num_pairs, long long i) {
 }
 void shim_plan(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks, int group_m,
                int* out) {
-    const tpmlp::SplitRule rule{85, 16, 64.0 * (1 << 20), 1.7e15 / 76, 6.0e12, 0.5, 4, 32};
+    // the rule of a GB300 context: 152 SMs (76 pairs) at 2.07 GHz, HBM 3.996 GHz x 8192 bits
+    const tpmlp::SplitRule rule =
+        tpmlp::split_rule(tpmlp::device_rates(152, 2070000.0, 3996000.0, 8192), 76);
     const tpmlp::SplitLaunch L{num_tiles, pairs, kb_tile, m_blocks, n_blocks, group_m, 256, 256};
     tpmlp::SplitPlan p = tpmlp::plan_split_tiles(L, rule);
     out[0] = p.sk_first; out[1] = p.sk_iters; out[2] = p.pairs;
