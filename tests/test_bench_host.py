@@ -1,6 +1,8 @@
 """Host-side logic of bench.py, without a GPU: the max-over-ranks aggregation under a real
 two-rank gloo process group, the whole-job throughput, the clock-sample parser, the traffic
-lines read from profiles/, and the algorithmic byte counts."""
+lines (accepted only for the library build that is running), the peak chosen by the timed
+region's length, the secondary workloads' parser, the summary of a timed workload, and the
+algorithmic byte counts."""
 import os
 import socket
 
@@ -82,10 +84,75 @@ def test_clock_sampler_parses_and_windows(tmp_path):
     assert got["reasons"] == ["sw_power_cap"] and got["window"] == "timed region"
 
 
-def test_traffic_lines_are_read_from_profiles():
-    v = bench.measured_traffic("7b", "gemm1")
-    assert v is None or v > 1e8  # a DRAM byte count per launch when a capture is committed
-    assert bench.measured_traffic("no-such-workload", "gemm1") is None
+def test_traffic_lines_need_the_running_build(tmp_path, monkeypatch):
+    f = tmp_path / "traffic.txt"
+    f.write_text("# DRAM bytes per launch\n"
+                 "traffic gpt3-175b gemm2 5100000000 build 0123456789abcdef\n"
+                 "traffic 7b gemm2 1310000000 build fedcba9876543210\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    v, why = bench.measured_traffic("gpt3-175b", "gemm2", "0123456789abcdef")
+    assert v == 5.1e9 and "0123456789abcdef" in why
+    v, why = bench.measured_traffic("7b", "gemm2", "0123456789abcdef")
+    assert v is None and "another build" in why
+    v, why = bench.measured_traffic("7b", "gemm1", "0123456789abcdef")
+    assert v is None and "no capture" in why
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.txt"))
+    assert bench.measured_traffic("7b", "gemm2", "x")[0] is None
+
+
+def test_committed_traffic_lines_are_well_formed():
+    if not os.path.exists(bench.TRAFFIC_FILE):
+        pytest.skip("no traffic summary committed")
+    import re
+    n = 0
+    for ln in open(bench.TRAFFIC_FILE):
+        if ln.startswith("traffic "):
+            parts = ln.split()
+            assert len(parts) == 6 and parts[4] == "build", ln
+            assert parts[1] in synth.WORKLOADS or parts[1].startswith("custom-"), ln
+            assert parts[2] in ("gemm1", "gemm2") and float(parts[3]) > 1e6, ln
+            assert re.fullmatch(r"[0-9a-f]{16}", parts[5]), ln
+            n += 1
+    assert n >= 1
+
+
+def test_peak_follows_the_timed_region():
+    peaks = {"bf16_tflops": 1960.6, "bf16_tflops_sustained": 1734.7, "hbm_gbs": 6750.0}
+    assert bench.peak_for(peaks, 0.12) == (1960.6, "burst")
+    assert bench.peak_for(peaks, bench.BURST_LIMIT_S + 0.5) == (1734.7, "sustained")
+    assert bench.peak_for({"bf16_tflops": 1900.0}, 5.0) == (1900.0, "sustained")
+
+
+def test_secondary_spec():
+    got = bench.parse_secondary("7b,gpt2-small,sweep-h4096:1/8/16")
+    assert got == [("7b", (8,)), ("gpt2-small", (4,)), ("sweep-h4096", (1, 8, 16))]
+    assert bench.parse_secondary("") == []
+    with pytest.raises(ValueError):
+        bench.parse_secondary("no-such-workload")
+    with pytest.raises(ValueError):
+        bench.parse_secondary("7b:3")  # 16384 / 3 is not a whole number of 64-column blocks
+
+
+def test_summary_of_a_timed_workload():
+    w = synth.WORKLOADS["gpt3-175b"]
+    peaks = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0, "hbm_gbs": 6750.0}
+    res = {"ms_step": 5.0, "t_wall": 0.3, "kernel_ms": {"gemm1": 2.4, "gemm2": 2.6},
+           "ln_ms": None}
+    s = bench.summarize(w, "gelu", res, 1, peaks)
+    assert s["value"] == pytest.approx(w.flops / 5e-3 / 1e12)
+    assert s["peak_regime"] == "burst"
+    assert s["pct_of_dense_bf16_peak"] == pytest.approx(100 * s["value"] / 2000.0)
+    assert s["pct_of_dense_bf16_peak_sustained"] == pytest.approx(100 * s["value"] / 1600.0)
+    r = s["roofline"]
+    assert r["kernel"] == "gemm2" and r["peak"] == 2000.0
+    assert r["achieved"] == pytest.approx(2 * w.M * w.H * w.F / 2.6e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / 2000.0)
+    assert r["frac_sustained"] == pytest.approx(r["achieved"] / 1600.0)
+    hb = s["hbm_gbs_algorithmic"]
+    assert hb["step"] == pytest.approx(bench.block_bytes(w) / 5e-3 / 1e9)
+    assert hb["step_with_y"] == pytest.approx((bench.block_bytes(w) + 4 * w.M * w.F) / 5e-3 / 1e9)
+    res["t_wall"] = 3.0
+    assert bench.summarize(w, "gelu", res, 1, peaks)["roofline"]["peak"] == 1600.0
 
 
 def test_algorithmic_bytes():
@@ -96,6 +163,8 @@ def test_algorithmic_bytes():
     assert bench.alg_bytes(w, "gemm2", "block") == bench.alg_bytes(w, "gemm2") + 2 * w.M * w.H
     assert bench.step_flops(w, "swiglu") == 6 * w.M * w.H * w.F
     assert bench.step_flops(w, "gelu") == 4 * w.M * w.H * w.F
+    # X in, Z out, W1, W2 and both biases once
+    assert bench.block_bytes(w) == 4 * w.M * w.H + 4 * w.H * w.F + 4 * w.F + 4 * w.H
 
 
 def test_clock_sampler_queries_the_process_gpu(monkeypatch):

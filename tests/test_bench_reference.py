@@ -2,8 +2,8 @@
 on the host cores and prints one JSON line with the GPU arm's metric, unit and direction, plus
 the keys the line of a reference run carries (impl, cpu_baseline, e2e with no copies).
 
-Run as the driver runs it, in a subprocess: on the default (7b) workload with a small time
-budget, on the tiny workload, and as a second rank under a torchrun-style environment, which
+Run as the driver runs it, in a subprocess: on the default (GPT-3-175B-shaped) workload with a
+small time budget, on the tiny workload, and as a second rank under a torchrun-style environment, which
 must exit 0 without output (only rank 0 times the oracle)."""
 import json
 import os
@@ -27,7 +27,7 @@ def run_bench(*args, env_extra=None, timeout=240):
 
 
 @pytest.mark.parametrize("workload,extra", [
-    ("7b", ["--reference-budget-s", "3"]),   # the default workload, bounded sample
+    ("gpt3-175b", ["--reference-budget-s", "3"]),   # the default workload, bounded sample
     ("tiny", ["--reference-budget-s", "2"]),
 ])
 def test_reference_arm_line(workload, extra):

@@ -31,7 +31,7 @@ def bench_line(*args):
 def test_bench_line_carries_the_contract(lib, variant):
     steps = 20
     line = bench_line("--workload", "tiny", "--variant", variant, "--steps", str(steps),
-                      "--warmup", "3", "--cpu-budget-s", "1")
+                      "--warmup", "3", "--cpu-budget-s", "1", "--secondary", "")
     w = bench.synth.WORKLOADS["tiny"]
     assert line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
     assert line["n_gpus"] == 1 and line["steps"] == steps and line["warmup"] == 3
@@ -49,6 +49,12 @@ def test_bench_line_carries_the_contract(lib, variant):
     assert roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s"
     assert roof["peak"] > 0 and roof["achieved"] > 0
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) <= 1e-9
+    # a 20-step tiny run is far under a second of work: judged against the burst peak
+    assert line["peak_regime"] == roof["peak_regime"] == "burst"
+    assert line["timed_region_s"] < bench.BURST_LIMIT_S
+    assert roof["frac_burst"] == roof["frac"] and roof["frac_sustained"] >= roof["frac"]
+    assert "traffic" in roof and "traffic_source" in roof
+    assert len(line["build_id"]) == 16
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == "TFLOP/s"
     assert e2e["h2d_bytes_per_step"] == w.M * w.H * 2 == e2e["d2h_bytes_per_step"]
@@ -59,3 +65,23 @@ def test_bench_line_carries_the_contract(lib, variant):
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
     assert "token rows" in cb["sample"]
+
+
+def test_bench_secondary_workloads(lib):
+    """The secondary workloads are timed in the same process and reported with their own
+    throughput, kernel times, roofline and HBM figures; a sweep reports every shard count."""
+    line = bench_line("--workload", "tiny", "--steps", "5", "--warmup", "3", "--no-cpu-baseline",
+                      "--secondary", "gpt2-small,tiny:1/2")
+    sec = line["secondary"]
+    assert sorted(sec) == ["gpt2-small", "tiny-k1", "tiny-k2"]
+    for label, s in sec.items():
+        cfg = s["config"]
+        want = cfg["flops_per_step"] / (s["ms_per_step"] * 1e-3) / 1e12
+        assert abs(s["value"] - want) <= 1e-6 * want, label
+        assert s["gpu_launches"] == 2 * 5, label
+        assert set(s["kernel_ms"]) == {"gemm1", "gemm2"}
+        assert s["roofline"]["kernel"] in ("gemm1", "gemm2")
+        assert s["hbm_gbs_algorithmic"]["step"] > 0
+        assert s["peak_regime"] == "burst"
+    assert sec["tiny-k1"]["config"]["k"] == 1 and sec["tiny-k2"]["config"]["k"] == 2
+    assert sec["gpt2-small"]["config"]["M"] == 8192
