@@ -342,7 +342,6 @@ def time_block(args, w: synth.Workload, variant: str, dev, flush, barrier, d=Non
              else synth.workload_inputs(w))
     X = to_device_bf16(d["X"], dev).view(w.B, w.S, w.H)
     Z = torch.empty((w.B, w.S, w.H), dtype=torch.bfloat16, device=dev)
-    Y = torch.empty((w.M, w.F), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     mlp = tp.TPMLP(w.H, w.F, w.k, swiglu=(variant == "swiglu"))
@@ -350,11 +349,9 @@ def time_block(args, w: synth.Workload, variant: str, dev, flush, barrier, d=Non
         mlp.pack_swiglu(*(to_device_bf16(d[n], dev) for n in ("Wg", "bg", "Wu", "bu", "W2", "b2")))
     else:
         mlp.pack(*(to_device_bf16(d[n], dev) for n in ("W1", "b1", "W2", "b2")))
-    Xn = None
     if variant == "block":
         g, b = ln_params(w.H)
         mlp.set_layernorm(to_device_bf16(g, dev), to_device_bf16(b, dev), 1e-5)
-        Xn = torch.empty((w.M, w.H), dtype=torch.bfloat16, device=dev)
     mlp.reserve(w.M)
     torch.cuda.synchronize(dev)  # the raw weights are released: only the packed copies stay
 
@@ -372,21 +369,14 @@ def time_block(args, w: synth.Workload, variant: str, dev, flush, barrier, d=Non
             ev[1].record(stream)
 
     def staged_step(ev):
-        # the same launches through the per-step entry points, with an event between them to
-        # attribute time to each kernel (the events cost the launches' overlap, so their sum
-        # is a little above a step of the timed region)
+        # the same launches, with the library recording an event between them to attribute
+        # time to each kernel (the events cost the launches' overlap, so their sum is a little
+        # above a step of the timed region)
         ev[0].record(stream)
         if variant == "block":
-            tp.tpmlp_layernorm(mlp.ctx, X, w.M, Xn, stream)
-            ev[3].record(stream)
-            tp.tpmlp_gemm1(mlp.ctx, Xn, w.M, Y, stream)
+            tp.tpmlp_block_forward_marked(mlp.ctx, X, w.B, w.S, Z, ev[3], ev[1], stream)
         else:
-            tp.tpmlp_gemm1(mlp.ctx, X, w.M, Y, stream)
-        ev[1].record(stream)
-        if variant == "block":
-            tp.tpmlp_gemm2_residual(mlp.ctx, Y, w.M, Z, X, stream)
-        else:
-            tp.tpmlp_gemm2(mlp.ctx, Y, w.M, Z, stream)
+            tp.tpmlp_forward_marked(mlp.ctx, X, w.B, w.S, Z, ev[1], stream)
         ev[2].record(stream)
 
     for _ in range(args.warmup):
@@ -472,7 +462,7 @@ def time_block(args, w: synth.Workload, variant: str, dev, flush, barrier, d=Non
             raise RuntimeError(f"{w.name}: device status after e2e steps: {detail:#x}")
         res["e2e_s"] = e2e_s
     mlp.close()
-    del X, Z, Y, Xn
+    del X, Z
     return res, d
 
 
@@ -562,8 +552,9 @@ def run_gpu(args, w: synth.Workload):
         "peak_regime": regime, "timed_region_s": res["t_wall"],
         "wall_ms_per_step_incl_l2_flush": res["t_wall"] * 1e3 / args.steps,
         "kernel_ms": summ["kernel_ms"],
-        "kernel_ms_source": "CUDA events between the launches, over a pass of the same number "
-                            "of steps right after the timed region (same L2 flush)",
+        "kernel_ms_source": "CUDA events the library records between the launches "
+                            "(tpmlp_forward_marked), over a pass of the same number of steps "
+                            "right after the timed region (same L2 flush)",
         "hbm_gbs_algorithmic": summ["hbm_gbs_algorithmic"],
         "config": workload_config(w, {"parallelism": "replicas" if world > 1 else "single GPU",
                                       "output": "bf16"}, variant=variant),

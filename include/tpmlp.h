@@ -112,8 +112,9 @@ TPMLP_API int tpmlp_create(tpmlp_ctx **out, int64_t H, int64_t F, int32_t k, uin
  * W1 is in the pages' math orientation (Y = X W1, AI大模型分布式训练 §2.1 allocates the
  * column-parallel weight as [in_features, out_features / k]), not [out, in].
  * Writes W1p [k][f][H] (each column shard transposed so that its reduction dimension H is
- * contiguous), W2p [k][H][f] (each row shard transposed likewise), and fp32 copies of b1
- * and b2. The raw weights may be freed once the stream has passed this call.
+ * contiguous), W2p [k][H][f] (each row shard transposed likewise; in 16 KB blocks of 128 rows
+ * x 64 columns when the second GEMM runs on CTA pairs, see tpmlp_packed_buffer), and fp32
+ * copies of b1 and b2. The raw weights may be freed once the stream has passed this call.
  * Errors: INVALID_ARG (also: context created with TPMLP_FLAG_SWIGLU), MISALIGNED, CUDA.
  */
 TPMLP_API int tpmlp_pack_shards(tpmlp_ctx *ctx, const void *W1, const void *b1, const void *W2,
@@ -162,6 +163,17 @@ TPMLP_API int tpmlp_reserve(tpmlp_ctx *ctx, int64_t max_tokens);
  * TPMLP_FLAG_FIXED_ORDER computes.
  */
 TPMLP_API int tpmlp_forward(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z, void *stream);
+
+/*
+ * tpmlp_forward that also records the caller's CUDA event `after_gemm1` (a cudaEvent_t passed
+ * as void*) on `stream` between the two kernel launches, so that each kernel can be timed
+ * (cudaEventElapsedTime against events recorded before and after the call). No counterpart on
+ * the pages. The same kernels, layouts and results as tpmlp_forward; the event costs the
+ * overlap of the two launches (a few microseconds). Errors: as tpmlp_forward, plus
+ * INVALID_ARG for a NULL event and CUDA if recording it fails.
+ */
+TPMLP_API int tpmlp_forward_marked(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S, void *Z,
+                                   void *after_gemm1, void *stream);
 
 /*
  * tpmlp_forward on host buffers: X (host, [B,S,H] bf16) in, Z (host, [B,S,H]) out; returns
@@ -249,6 +261,16 @@ TPMLP_API int tpmlp_block_forward_host(tpmlp_ctx *ctx, const void *X_host, int64
                                        void *Z_host, void *stream);
 
 /*
+ * tpmlp_block_forward with the caller's CUDA events `after_layernorm` and `after_gemm1`
+ * recorded on `stream` after the first and the second of its three launches (per-kernel
+ * timing; see tpmlp_forward_marked). Errors: as tpmlp_block_forward, plus INVALID_ARG for a
+ * NULL event and CUDA if recording one fails.
+ */
+TPMLP_API int tpmlp_block_forward_marked(tpmlp_ctx *ctx, const void *X, int64_t B, int64_t S,
+                                         void *Z, void *after_layernorm, void *after_gemm1,
+                                         void *stream);
+
+/*
  * The second step with the residual add (the last launch of tpmlp_block_forward):
  *   Z[m, n] = R[m, n] + (b2[n] + sum_i sum_{j<f} Y[m, i f + j] W2[i f + j, n])
  *   Y device bf16 [M, F]; R device bf16 [M, H]; Z device [M, H] (bf16, or fp32 with
@@ -328,7 +350,10 @@ TPMLP_API int tpmlp_get_status(tpmlp_ctx *ctx, void *stream, int32_t *detail);
  * Where the packed weights live (for tests that unpack and compare them bit for bit).
  *   which: 0 = W1p bf16 [k][f][H], 1 = W2p bf16 [k][H][f], 2 = b1 fp32 [F], 3 = b2 fp32 [H];
  *   for a TPMLP_FLAG_SWIGLU context W1p is [k][2f][H] and b1 [2F], gate/up interleaved in
- *   blocks of G rows (see tpmlp_pack_shards_swiglu).
+ *   blocks of G rows (see tpmlp_pack_shards_swiglu). When H is a multiple of 256 and
+ *   TPMLP_FLAG_SINGLE_SM is not set (the second GEMM runs on CTA pairs), W2p is stored in
+ *   contiguous blocks of 128 rows x 64 columns instead: [k][H/128][f/64][128][64], i.e.
+ *   W2p[i][n][j] sits at ((i (H/128) + n/128) (f/64) + j/64) 8192 + (n%128) 64 + j%64.
  * *ptr receives a device pointer owned by the context; *bytes its size.
  * Errors: INVALID_ARG, NOT_PACKED.
  */

@@ -28,6 +28,7 @@ __all__ = [
     "tpmlp_linear_create", "tpmlp_linear_pack", "tpmlp_linear_forward", "Linear",
     "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW", "tpmlp_forward_train", "tpmlp_backward",
     "tpmlp_backward_swiglu", "tpmlp_set_device_rates", "tpmlp_get_device_rates", "tpmlp_build_id",
+    "tpmlp_forward_marked", "tpmlp_block_forward_marked",
 ]
 
 TPMLP_OK = 0
@@ -84,6 +85,8 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_reserve": ([vp, i64], ctypes.c_int),
         "tpmlp_forward": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_forward_host": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_forward_marked": ([vp, vp, i64, i64, vp, vp, vp], ctypes.c_int),
+        "tpmlp_block_forward_marked": ([vp, vp, i64, i64, vp, vp, vp, vp], ctypes.c_int),
         "tpmlp_forward_noalloc": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_set_layernorm": ([vp, vp, vp, ctypes.c_float, vp], ctypes.c_int),
         "tpmlp_layernorm": ([vp, vp, i64, vp, vp], ctypes.c_int),
@@ -184,6 +187,32 @@ def tpmlp_reserve(ctx: int, max_tokens: int) -> None:
 def tpmlp_forward(ctx: int, X, B: int, S: int, Z, stream=None) -> None:
     _check(load_library().tpmlp_forward(ctx, _ptr(X), B, S, _ptr(Z), _stream(stream)),
            "tpmlp_forward", ctx)
+
+
+def _event(ev) -> int:
+    """cudaEvent_t handle of a torch.cuda.Event (created if it was not yet) or an int."""
+    if isinstance(ev, int):
+        return ev
+    h = int(getattr(ev, "cuda_event", 0) or 0)
+    if not h:
+        ev.record()  # torch creates its event on the first record
+        h = int(ev.cuda_event)
+    return h
+
+
+def tpmlp_forward_marked(ctx: int, X, B: int, S: int, Z, after_gemm1, stream=None) -> None:
+    """tpmlp_forward, recording `after_gemm1` (a torch.cuda.Event or a raw handle) between the
+    two kernel launches."""
+    _check(load_library().tpmlp_forward_marked(ctx, _ptr(X), B, S, _ptr(Z), _event(after_gemm1),
+                                               _stream(stream)), "tpmlp_forward_marked", ctx)
+
+
+def tpmlp_block_forward_marked(ctx: int, X, B: int, S: int, Z, after_layernorm, after_gemm1,
+                               stream=None) -> None:
+    _check(load_library().tpmlp_block_forward_marked(ctx, _ptr(X), B, S, _ptr(Z),
+                                                     _event(after_layernorm), _event(after_gemm1),
+                                                     _stream(stream)),
+           "tpmlp_block_forward_marked", ctx)
 
 
 def tpmlp_forward_host(ctx: int, X_host, B: int, S: int, Z_host, stream=None) -> None:

@@ -118,6 +118,8 @@ struct GemmArgs {
     float* sk_partial;     // [pairs][2: first / last unit][2 CTAs][256 columns][128 rows] fp32
     uint32_t* sk_count;    // [split tiles][2 CTAs][epilogue warps] epoch-tagged arrivals
     uint32_t sk_epoch;     // new for every launch that splits
+    int b_blocked;         // CTA-pair second GEMM: B is the packed operand in 16 KB blocks
+                           // (2-D map of 128-byte rows; see transpose_blocked_bf16_kernel)
 };
 
 constexpr int kSkSlotFloats = 128 * 256;  // one CTA's half of a 256 x 256 accumulator

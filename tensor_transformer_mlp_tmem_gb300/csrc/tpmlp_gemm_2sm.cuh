@@ -161,8 +161,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                         const int kk = (kb - i * args.kb_shard) * kBK;  // offset inside shard i
                         const bool second = i >= args.k2;
                         ptx::tma_load_2d_pair(sa, &tmA, fb, i * args.f + kk, m0);
-                        ptx::tma_load_3d_pair(sb, second ? &tmB2 : &tmB, fb, kk, nb,
-                                              second ? i - args.k2 : i);
+                        if (args.b_blocked)  // block (shard i, rows nb / 128, columns kk / 64)
+                            ptx::tma_load_2d_pair(
+                                sb, &tmB, fb, 0,
+                                ((i * (args.ldo / 128) + nb / 128) * (args.f / kBK) + kk / kBK) * 128);
+                        else
+                            ptx::tma_load_3d_pair(sb, second ? &tmB2 : &tmB, fb, kk, nb,
+                                                  second ? i - args.k2 : i);
                     }
                     ++issued;
                     if (++stage == STAGES) {

@@ -41,6 +41,33 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// W2 [F][H] -> the second GEMM's operand in 16 KB blocks: for shard i, output row n and
+// reduction index j (0 <= j < f), element W2[i f + j][n] sits at
+//   ((i * (H / 128) + n / 128) * (f / 64) + j / 64) * 8192 + (n % 128) * 64 + j % 64,
+// so the 128 rows x 64 columns that one TMA box of the CTA-pair kernel reads are contiguous.
+__global__ void __launch_bounds__(256)
+    transpose_blocked_bf16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
+                                  int f, int H) {
+    __shared__ uint16_t tile[kTransposeTile][kTransposeTile + 2];
+    const int i = blockIdx.z;
+    const int r0 = blockIdx.y * kTransposeTile;  // j
+    const int c0 = blockIdx.x * kTransposeTile;  // n
+    const uint16_t* src = in + static_cast<size_t>(i) * f * H;
+    const int tx = threadIdx.x;
+    for (int y = threadIdx.y; y < kTransposeTile; y += blockDim.y) {
+        const int r = r0 + y, c = c0 + tx;
+        if (r < f && c < H) tile[y][tx] = src[static_cast<size_t>(r) * H + c];
+    }
+    __syncthreads();
+    for (int y = threadIdx.y; y < kTransposeTile; y += blockDim.y) {
+        const int n = c0 + y, j = r0 + tx;
+        if (n < H && j < f) {
+            const size_t blk = (static_cast<size_t>(i) * (H / 128) + n / 128) * (f / 64) + j / 64;
+            out[blk * 8192 + (n % 128) * 64 + j % 64] = tile[tx][y];
+        }
+    }
+}
+
 // Gated first layer: the gate and the up projection are packed into one K-major operand whose
 // rows alternate in blocks of G: for output column j (0 <= j < F) of part p (0 = gate,
 // 1 = up), the packed row is (j / G) * 2G + p * G + (j % G). With G dividing the shard width

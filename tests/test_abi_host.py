@@ -119,6 +119,8 @@ BLOCK_CALLS = {
     "tpmlp_forward": (16, 1, 64, 16, None),
     "tpmlp_forward_host": (16, 1, 64, 16, None),
     "tpmlp_forward_noalloc": (16, 1, 64, 16, None),
+    "tpmlp_forward_marked": (16, 1, 64, 16, 16, None),
+    "tpmlp_block_forward_marked": (16, 1, 64, 16, 16, 16, None),
     "tpmlp_gemm1": (16, 64, 16, None),
     "tpmlp_gemm2": (16, 64, 16, None),
     "tpmlp_gemm2_residual": (16, 64, 16, 16, None),

@@ -26,7 +26,7 @@ def run_block(d, H, F, k, M, z_fp32=False):
 
 
 # ----------------------------------------------------------------------------- packer
-@pytest.mark.parametrize("H,F,k", [(256, 1024, 2), (128, 512, 4), (64, 256, 4)])
+@pytest.mark.parametrize("H,F,k", [(256, 1024, 2), (512, 2048, 4), (128, 512, 4), (64, 256, 4)])
 def test_pack_layout_is_exact_permutation(lib, H, F, k):
     d = synth.make_inputs(H, F, 4, 21)
     dd = inputs_on_device(d)
@@ -38,7 +38,12 @@ def test_pack_layout_is_exact_permutation(lib, H, F, k):
         assert n == H * F * 2
         W1p = device_tensor(p, (k, f, H), "i16").cpu().numpy().view(np.uint16)
         p, _ = tp.tpmlp_packed_buffer(mlp.ctx, 1)
-        W2p = device_tensor(p, (k, H, f), "i16").cpu().numpy().view(np.uint16)
+        if H % 256 == 0:
+            # second GEMM on CTA pairs: 16 KB blocks [k][H/128][f/64][128][64]
+            W2b = device_tensor(p, (k, H // 128, f // 64, 128, 64), "i16").cpu().numpy()
+            W2p = W2b.transpose(0, 1, 3, 2, 4).reshape(k, H, f).view(np.uint16)
+        else:
+            W2p = device_tensor(p, (k, H, f), "i16").cpu().numpy().view(np.uint16)
         p, _ = tp.tpmlp_packed_buffer(mlp.ctx, 2)
         b1p = device_tensor(p, (F,), "f32").cpu().numpy()
         p, _ = tp.tpmlp_packed_buffer(mlp.ctx, 3)
