@@ -7,8 +7,8 @@
 //
 // A CTA-pair launch of T output tiles, each reduced over kb_tile blocks of 64, on P resident
 // pairs. Tile t covers row block m and column block n of the output (decode_tile_mn: groups of
-// group_m row blocks, each swept column by column, so that the tiles running at once share
-// operand rows and columns in L2). Tiles [0, sk_first) are whole units, handed out round robin
+// group_m row blocks, each swept column by column, alternate groups in reverse, so that the
+// tiles running at once share operand rows and columns in L2). Tiles [0, sk_first) are whole units, handed out round robin
 // (pair p: p, p + P, ...).
 // The sk_iters = (T - sk_first) * kb_tile reduction blocks of the remaining tiles, in tile
 // order, are cut into P contiguous shares [floor(S p / P), floor(S (p + 1) / P)) that every
@@ -49,6 +49,11 @@
 
 namespace tpmlp {
 
+// Tile t of a launch of m_blocks x n_blocks tiles: groups of group_m row blocks, each swept
+// column by column, every second group in reverse column order ("snake"), so that a wave of
+// tiles that straddles two groups reads the same column blocks in both. Interleaved A/B
+// against all groups sweeping forward (second GEMM, bit-identical where no tile is split):
+// 587.5 -> 582.5 us at 7b, 2902 -> 2887 us at GPT-3.
 TPMLP_HD void decode_tile_mn(int group_m, int m_blocks, int n_blocks, int t, int& m_blk,
                              int& n_blk) {
     const int per_group = group_m * n_blocks;
@@ -58,6 +63,7 @@ TPMLP_HD void decode_tile_mn(int group_m, int m_blocks, int n_blocks, int t, int
     const int local = t - g * per_group;
     m_blk = first_m + local % gm;
     n_blk = local / gm;
+    if (g & 1) n_blk = n_blocks - 1 - n_blk;
 }
 
 struct WorkCursor {
