@@ -337,6 +337,60 @@ int launch_pair(tpmlp_ctx* c, const CUtensorMap& a, const CUtensorMap& b, const 
 // sweep's 16384 tokens; GPT-2 unchanged.
 bool w2_blocked(const tpmlp_ctx* c) { return c->pair2; }
 
+// The second GEMM on CTA pairs. Reductions at least TPMLP_TALL_MIN_KB blocks deep run their
+// whole waves of 512 x 256 tall units with the TALL kernel (4 stages of 48 KB: two A halves and
+// one shared B tile), and the rest of the output as ordinary tiles in the same launch, split
+// over all pairs when the tail rule says so (tpmlp_plan.h, plan_tall_units).
+#ifndef TPMLP_TALL_MIN_KB
+#define TPMLP_TALL_MIN_KB 128
+#endif
+#ifndef TPMLP_TALL_STAGES
+#define TPMLP_TALL_STAGES 4
+#endif
+template <Mode MODE, bool F32>
+int launch_gemm2_pair(tpmlp_ctx* c, const CUtensorMap& a_map, const CUtensorMap& b_map,
+                      const GemmArgs& args, cudaStream_t s) {
+    if (args.kb_tile >= TPMLP_TALL_MIN_KB) {
+        auto kern = tpmlp::tpmlp_gemm_pair_kernel<TPMLP_TALL_STAGES, 2, MODE, F32, false, true>;
+        constexpr uint32_t smem = tpmlp::PairSmem<TPMLP_TALL_STAGES, 2, true>::kTotal;
+        static_assert(smem <= 232448, "shared memory per CTA");
+        static std::atomic<uint64_t> attr_done{0};
+        if (int rc = ensure_smem_attr(c, kern, smem, attr_done)) return rc;
+        static std::atomic<int> resident_on[64];
+        std::atomic<int>& slot = resident_on[c->device & 63];
+        int resident = slot.load(std::memory_order_relaxed);
+        if (resident <= 0) {
+            resident = max_resident_pairs(c, kern, smem);
+            slot.store(resident, std::memory_order_relaxed);
+        }
+        const tpmlp::TallPlan tall = tpmlp::plan_tall_units(args.M, args.n_blocks, args.group_m, resident);
+        if (tall.tall_units > 0) {
+            GemmArgs run = args;
+            run.tall_units = tall.tall_units;
+            run.tall_m_blocks = tall.tall_m_blocks;
+            run.num_tiles = tall.tiles;
+            run.sk_first = tall.tiles;  // the remaining tiles whole ...
+            run.sk_iters = 0;
+            if (c->sk_partial && resident <= c->num_sms / 2 && !capturing(s) && tall.tiles > 0 &&
+                tall.tiles <= c->num_sms &&
+                tpmlp::tail_split_pays(tall.tiles, args.kb_tile, resident, tall.rows, tall.cols,
+                                       tpmlp::kPairBM, tpmlp::kPairBN,
+                                       split_rule_of(c, c->num_sms / 2))) {
+                run.sk_first = 0;  // ... or spread over all pairs
+                run.sk_iters = tall.tiles * args.kb_tile;
+                run.sk_partial = c->sk_partial;
+                run.sk_count = c->sk_count;
+                if (++c->sk_epoch == 0) c->sk_epoch = 1;
+                run.sk_epoch = c->sk_epoch;
+            }
+            TPMLP_CUDA(c, launch_overlapped(kern, 2 * resident, smem, s, a_map, b_map, b_map, run));
+            ++c->launches;
+            return TPMLP_OK;
+        }
+    }
+    return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, MODE, F32>(c, a_map, b_map, args, s);
+}
+
 GemmArgs base_args(const tpmlp_ctx* c, int64_t M, int ldo, int bm, int bn, int group_m) {
     GemmArgs a{};
     a.M = static_cast<int>(M);
@@ -491,10 +545,8 @@ int run_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, cudaStream_t s,
     if (residual) {
         if (pair) {
             if (c->flags & TPMLP_FLAG_Z_FP32)
-                return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2Residual, true>(
-                    c, tmY, c->tmW2_pair, a, s);
-            return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2Residual, false>(
-                c, tmY, c->tmW2_pair, a, s);
+                return launch_gemm2_pair<Mode::kGemm2Residual, true>(c, tmY, c->tmW2_pair, a, s);
+            return launch_gemm2_pair<Mode::kGemm2Residual, false>(c, tmY, c->tmW2_pair, a, s);
         }
         if (c->flags & TPMLP_FLAG_Z_FP32)
             return dispatch_gemm<Mode::kGemm2Residual, true>(c, c->bn2, tmY, c->tmW2, a, s);
@@ -502,10 +554,8 @@ int run_gemm2(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, cudaStream_t s,
     }
     if (pair) {
         if (c->flags & TPMLP_FLAG_Z_FP32)
-            return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, true>(
-                c, tmY, c->tmW2_pair, a, s);
-        return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, false>(
-            c, tmY, c->tmW2_pair, a, s);
+            return launch_gemm2_pair<Mode::kGemm2, true>(c, tmY, c->tmW2_pair, a, s);
+        return launch_gemm2_pair<Mode::kGemm2, false>(c, tmY, c->tmW2_pair, a, s);
     }
     if (c->flags & TPMLP_FLAG_Z_FP32)
         return dispatch_gemm<Mode::kGemm2, true>(c, c->bn2, tmY, c->tmW2, a, s);

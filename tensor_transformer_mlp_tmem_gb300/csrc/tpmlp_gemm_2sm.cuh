@@ -36,9 +36,11 @@ constexpr uint64_t kSplitWaitNs = TPMLP_SPLIT_WAIT_NS;
 constexpr int kPairBM = 256;  // output rows per pair tile (128 per CTA)
 constexpr int kPairBN = 256;  // output columns per pair tile (B: 128 rows per CTA)
 
-template <int STAGES, int NUM_ACC>
+// TALL: a stage also holds the CTA's 128 rows of A of a tall unit's second half (after the
+// first half's), so that one B tile feeds both halves' MMAs (see GemmArgs::tall_units).
+template <int STAGES, int NUM_ACC, bool TALL = false>
 struct PairSmem {
-    static constexpr uint32_t kABytes = 128 * kBK * 2;  // this CTA's 128 rows of A
+    static constexpr uint32_t kABytes = (TALL ? 2 : 1) * 128 * kBK * 2;  // this CTA's A rows
     static constexpr uint32_t kBBytes = 128 * kBK * 2;  // this CTA's 128 rows of B
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kCtrlBytes = 8 * (2 * STAGES + 2 * NUM_ACC + 1) + 8;
@@ -50,12 +52,21 @@ struct PairSmem {
 
 // MN: both operands M-/N-contiguous (the weight-gradient GEMMs): each CTA loads its 128 rows
 // of A and of B as two 64 (MN) x 64 (K) boxes each (see tpmlp_gemm_kernel).
-template <int STAGES, int NUM_ACC, Mode MODE, bool OUT_F32, bool MN = false>
+// TALL (second-GEMM modes, two accumulators): each pair first computes tall units of
+// 512 x 256 outputs, args.tall_units of them round robin, with both accumulators: per
+// reduction block one B tile and the A tiles of both 256-row halves, two MMAs per 16-deep
+// step. Against two 256 x 256 tiles that is a quarter less operand traffic per multiply-add;
+// the accumulators are not double-buffered then, so a unit's epilogue does not overlap the
+// next unit's MMAs. The launch's tiles follow as usual (see decode_tile).
+template <int STAGES, int NUM_ACC, Mode MODE, bool OUT_F32, bool MN = false, bool TALL = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     tpmlp_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
-    using L = PairSmem<STAGES, NUM_ACC>;
+    static_assert(!TALL || ((MODE == Mode::kGemm2 || MODE == Mode::kGemm2Residual) && !MN &&
+                            NUM_ACC == 2),
+                  "tall units: second GEMM, two accumulators");
+    using L = PairSmem<STAGES, NUM_ACC, TALL>;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, kPairBN, MN);
     constexpr int kCode = (static_cast<int>(MODE) << 8) | 0x80;  // 0x80: pair kernel
 
@@ -116,11 +127,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
+            // the B rows and the A rows of reduction block kb of the second GEMM (shard-major)
+            auto load_b = [&](uint32_t sb, uint32_t fb, int kb, int nb) {
+                const int i = kb / args.kb_shard;
+                const int kk = (kb - i * args.kb_shard) * kBK;
+                const bool second = i >= args.k2;
+                if (args.b_blocked)  // block (shard i, rows nb / 128, columns kk / 64)
+                    ptx::tma_load_2d_pair(
+                        sb, &tmB, fb, 0,
+                        ((i * (args.ldo / 128) + nb / 128) * (args.f / kBK) + kk / kBK) * 128);
+                else
+                    ptx::tma_load_3d_pair(sb, second ? &tmB2 : &tmB, fb, kk, nb,
+                                          second ? i - args.k2 : i);
+            };
+            auto load_a = [&](uint32_t sa, uint32_t fb, int kb, int m0) {
+                const int i = kb / args.kb_shard;
+                ptx::tma_load_2d_pair(sa, &tmA, fb, i * args.f + (kb - i * args.kb_shard) * kBK, m0);
+            };
+            if constexpr (TALL) {
+                for (int u = pair; ok && u < args.tall_units; u += num_pairs) {
+                    int tm, n_blk;
+                    decode_tile_mn(args.group_m, args.tall_m_blocks, args.n_blocks, u, tm, n_blk);
+                    const int m0 = tm * 2 * kPairBM + static_cast<int>(rank) * 128;
+                    const bool second = tm * 2 * kPairBM + kPairBM < args.M;  // second half has rows
+                    const int nb = n_blk * kPairBN + static_cast<int>(rank) * 128;
+                    const uint32_t bytes = 2 * ((second ? 2 : 1) * 128 * kBK * 2 + 128 * kBK * 2);
+                    for (int kb = 0; kb < args.kb_tile; ++kb) {
+                        if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status,
+                                            kCode | kSiteProducer)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sa = base + stage * L::kStageBytes;
+                        const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
+                        load_a(sa, fb, kb, m0);
+                        if (second) load_a(sa + 128 * kBK * 2, fb, kb, m0 + kPairBM);
+                        load_b(sa + L::kABytes, fb, kb, nb);
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
             WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
             int t, kb0, kb1;
             while (ok && work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
                 int m_blk, n_blk;
                 decode_tile(args, t, m_blk, n_blk);
+                if (m_blk >= args.m_blocks) continue;  // an empty half of a tall unit
                 const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;  // this CTA's A rows
                 const int n0 = n_blk * kPairBN;
                 const int nb = n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
@@ -146,7 +203,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     }
 #endif
                     const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // rank 0's barrier
-                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
+                    if (leader)  // both CTAs' A (one 128-row box each) and B tiles
+                        ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * (128 * kBK * 2 + L::kBBytes));
                     if constexpr (MN) {
 #pragma unroll
                         for (int b = 0; b < 2; ++b) {
@@ -157,17 +215,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                         ptx::tma_load_2d_pair(sa, &tmA, fb, kb * kBK, m0);
                         ptx::tma_load_3d_pair(sb, &tmB, fb, kb * kBK, nb_in_shard1, shard1);
                     } else {
-                        const int i = kb / args.kb_shard;               // shard of this block
-                        const int kk = (kb - i * args.kb_shard) * kBK;  // offset inside shard i
-                        const bool second = i >= args.k2;
-                        ptx::tma_load_2d_pair(sa, &tmA, fb, i * args.f + kk, m0);
-                        if (args.b_blocked)  // block (shard i, rows nb / 128, columns kk / 64)
-                            ptx::tma_load_2d_pair(
-                                sb, &tmB, fb, 0,
-                                ((i * (args.ldo / 128) + nb / 128) * (args.f / kBK) + kk / kBK) * 128);
-                        else
-                            ptx::tma_load_3d_pair(sb, second ? &tmB2 : &tmB, fb, kk, nb,
-                                                  second ? i - args.k2 : i);
+                        load_a(sa, fb, kb, m0);
+                        load_b(sb, fb, kb, nb);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -196,9 +245,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         if (leader && lane == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
+            if constexpr (TALL) {
+                // a tall unit takes both accumulators (acc is 0 at the start of each: units
+                // come first and take two each)
+                for (int u = pair; ok && u < args.tall_units; u += num_pairs) {
+                    int tm, n_blk;
+                    decode_tile_mn(args.group_m, args.tall_m_blocks, args.n_blocks, u, tm, n_blk);
+                    const bool second = tm * 2 * kPairBM + kPairBM < args.M;
+                    if (!ptx::mbar_wait(tempty_bar(0), acc_phase ^ 1u, abort_flag, args.status,
+                                        kCode | kSiteMmaAccum) ||
+                        !ptx::mbar_wait(tempty_bar(1), acc_phase ^ 1u, abort_flag, args.status,
+                                        kCode | kSiteMmaAccum)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    for (int kb = 0; kb < args.kb_tile; ++kb) {
+                        if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, args.status,
+                                            kCode | kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t sa = base + stage * L::kStageBytes;
+                        const uint64_t da0 = sdesc_k128(sa);
+                        const uint64_t da1 = sdesc_k128(sa + 128 * kBK * 2);
+                        const uint64_t db = sdesc_k128(sa + L::kABytes);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                            const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
+                            ptx::mma_bf16_ss_pair(tmem_base, da0 + 2u * kk, db + 2u * kk, kIdesc,
+                                                  accumulate);
+                            if (second)
+                                ptx::mma_bf16_ss_pair(tmem_base + kPairBN, da1 + 2u * kk,
+                                                      db + 2u * kk, kIdesc, accumulate);
+                        }
+                        ptx::mma_commit_pair(empty_bar(stage), 0x3);  // stage s free in both CTAs
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit_pair(tfull_bar(0), 0x3);  // both accumulators ready
+                    ptx::mma_commit_pair(tfull_bar(1), 0x3);
+                    acc_phase ^= 1u;
+                }
+            }
             WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
             int t, kb0, kb1;
             while (ok && work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
+                if constexpr (TALL) {
+                    int m_blk, n_blk;
+                    decode_tile(args, t, m_blk, n_blk);
+                    if (m_blk >= args.m_blocks) continue;  // an empty half of a tall unit
+                }
                 if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status,
                                     kCode | kSiteMmaAccum)) {
                     ok = false;
@@ -244,16 +345,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         const int part = (warp - 2) >> 2;
         uint32_t acc = 0, acc_phase = 0;
         const int ew = warp - 2;  // epilogue warp index: its arrival counter in a split tile
+        bool ok_tall = true;
+        if constexpr (TALL) {
+            const uint32_t stage_buf = base + L::kEpiOffset + (warp - 2) * kStageSliceBytes;
+            for (int u = pair; u < args.tall_units; u += num_pairs) {
+                int tm, n_blk;
+                decode_tile_mn(args.group_m, args.tall_m_blocks, args.n_blocks, u, tm, n_blk);
+                const bool second = tm * 2 * kPairBM + kPairBM < args.M;
+                const bool ok = ptx::mbar_wait(tfull_bar(0), acc_phase, abort_flag, args.status,
+                                               kCode | kSiteEpilogue) &&
+                                ptx::mbar_wait(tfull_bar(1), acc_phase, abort_flag, args.status,
+                                               kCode | kSiteEpilogue);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok_tall = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const int row0 = tm * 2 * kPairBM + static_cast<int>(rank) * 128 + q * 32 + lane;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+                auto release = [&] {  // both accumulators' columns are in registers
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(tempty_bar(0), 0));
+                        ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(tempty_bar(1), 0));
+                    }
+                };
+                drain_tall<MODE, OUT_F32, kPairBN>(taddr, taddr + kPairBN, second, args, row0,
+                                                   row0 + kPairBM, n_blk * kPairBN, part,
+                                                   stage_buf, release);
+                acc_phase ^= 1u;
+            }
+        }
         WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
         int t, kb0, kb1;
-        {
+        if (!TALL) {
             WorkCursor first = cur;
             if (work_next(args.sk_first, args.kb_tile, num_pairs, first, t, kb0, kb1))
                 prefetch_tile_bias<MODE, kPairBN>(args, t, part);
         }
-        while (work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
+        while (ok_tall && work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
             int m_blk, n_blk;
             decode_tile(args, t, m_blk, n_blk);
+            if (m_blk >= args.m_blocks) continue;  // an empty half of a tall unit
             const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;
             const int n0 = n_blk * kPairBN;
             bool ok = ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status,

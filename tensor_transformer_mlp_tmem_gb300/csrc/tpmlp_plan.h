@@ -147,6 +147,22 @@ struct SplitRule {
     int min_part_blocks;        // ... each with at least this many reduction blocks
 };
 
+// The last `rem` tiles of a launch (kb_tile blocks deep, spanning `rows` distinct row blocks of
+// tile_rows and `cols` distinct column blocks of tile_cols) are worth spreading over all `pairs`
+// pairs when rem / pairs of a round plus one DRAM read of their operand rows and columns takes
+// under tail_gain of a round of whole tiles, and every pair gets a non-empty share.
+inline bool tail_split_pays(int rem, int kb_tile, int pairs, int rows, int cols, int tile_rows,
+                            int tile_cols, const SplitRule& rule) {
+    if (rem <= 0 || pairs <= 0 || kb_tile < rule.min_blocks) return false;
+    if (static_cast<long long>(rem) * kb_tile < pairs) return false;
+    const double block_bytes = static_cast<double>(kb_tile) * 64 * 2.0;  // one row, all K
+    const double round_s = 2.0 * 256 * 256 * 64 * kb_tile / rule.pair_flops;
+    const double tail_bytes =
+        (static_cast<double>(rows) * tile_rows + static_cast<double>(cols) * tile_cols) * block_bytes;
+    const double tail_s = round_s * rem / pairs + tail_bytes / rule.dram_Bps;
+    return tail_s < rule.tail_gain * round_s;
+}
+
 inline SplitPlan plan_split_tiles(const SplitLaunch& L, const SplitRule& rule) {
     SplitPlan p{L.num_tiles, 0, 0};
     if (L.pairs <= 0 || L.num_tiles <= 0 || L.kb_tile < rule.min_blocks) return p;
@@ -174,7 +190,6 @@ inline SplitPlan plan_split_tiles(const SplitLaunch& L, const SplitRule& rule) {
         p.sk_iters = L.num_tiles * L.kb_tile;
         return p;
     }
-    if (static_cast<long long>(rem) * L.kb_tile < L.pairs) return p;
     // the distinct row and column blocks of the last rem tiles
     const int first = L.num_tiles - rem;
     int m_lo = 1 << 30, m_hi = -1, n_cnt = 0, n_prev = -1;
@@ -186,14 +201,45 @@ inline SplitPlan plan_split_tiles(const SplitLaunch& L, const SplitRule& rule) {
         if (n != n_prev) ++n_cnt;  // the tail walks whole columns of one row group
         n_prev = n;
     }
-    const double round_s = 2.0 * 256 * 256 * 64 * L.kb_tile / rule.pair_flops;
-    const double tail_bytes =
-        (static_cast<double>(m_hi - m_lo + 1) * L.tile_rows + static_cast<double>(n_cnt) * L.tile_cols) *
-        block_bytes;
-    const double tail_s = round_s * rem / L.pairs + tail_bytes / rule.dram_Bps;
-    if (tail_s >= rule.tail_gain * round_s) return p;
+    if (!tail_split_pays(rem, L.kb_tile, L.pairs, m_hi - m_lo + 1, n_cnt, L.tile_rows, L.tile_cols,
+                         rule))
+        return p;
     p.sk_first = first;
     p.sk_iters = rem * L.kb_tile;
+    return p;
+}
+
+// ---------------------------------------------------------------- tall units
+//
+// The second GEMM of a deep reduction runs most of its output as 512 x 256 tall units (two
+// 256 x 256 halves sharing each B tile; GemmArgs::tall_units): as many whole waves of them as
+// there are, `tall_units` = floor(T / P) * P of the T = ceil(M / 512) * n_blocks units. The
+// halves of the remaining units become the launch's ordinary tiles (tiles = 2 (T - tall_units),
+// tile t = half t % 2 of unit tall_units + t / 2), which may be split over all pairs as a tail.
+struct TallPlan {
+    int tall_units;     // 0: no tall units (launch the ordinary kernel)
+    int tall_m_blocks;  // ceil(M / 512)
+    int tiles;          // the ordinary tiles after them
+    int rows, cols;     // distinct 256-row and 256-column blocks of those tiles
+};
+
+inline TallPlan plan_tall_units(int M, int n_blocks, int group_m, int pairs) {
+    TallPlan p{0, (M + 511) / 512, 0, 0, 0};
+    const int T = p.tall_m_blocks * n_blocks;
+    if (pairs <= 0 || T < pairs) return p;
+    p.tall_units = T / pairs * pairs;
+    p.tiles = 2 * (T - p.tall_units);
+    int m_lo = 1 << 30, m_hi = -1, n_cnt = 0, n_prev = -1;
+    for (int u = p.tall_units; u < T; ++u) {
+        int tm, n;
+        decode_tile_mn(group_m, p.tall_m_blocks, n_blocks, u, tm, n);
+        m_lo = 2 * tm < m_lo ? 2 * tm : m_lo;
+        m_hi = 2 * tm + 1 > m_hi ? 2 * tm + 1 : m_hi;
+        if (n != n_prev) ++n_cnt;
+        n_prev = n;
+    }
+    p.rows = m_hi >= m_lo ? m_hi - m_lo + 1 : 0;
+    p.cols = n_cnt;
     return p;
 }
 

@@ -1,0 +1,87 @@
+"""Tall units of the second GEMM (CTA-pair kernel, reductions of at least 128 blocks): whole
+waves of 512 x 256 output units whose two 256-row halves share every B tile, then the rest of
+the output as ordinary 256 x 256 tiles in the same launch (split over all pairs when the tail
+rule says so).
+
+A tall unit sums each output in the same order as a whole tile, so with TPMLP_FLAG_FIXED_ORDER
+its Z must equal the single-SM kernel's bit for bit, at token counts whose last 512-row unit
+is full, has a partial second half, or has an empty second half; also with the residual add
+and with fp32 output. With the split tail the result is checked against the oracle, for
+determinism, and against the fixed order within the split's rounding."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import tensor_transformer_mlp_tmem_gb300 as tp
+from gpu_util import assert_close, inputs_on_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+H, F, K_SHARDS = 4096, 8192, 2  # 16 column blocks, 128 reduction blocks in the second GEMM
+
+
+def forward(dd, M, **kw):
+    with tp.TPMLP(H, F, K_SHARDS, **kw) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        Z = mlp(dd["X"].view(1, M, H))
+        torch.cuda.synchronize()
+        rc, detail = mlp.status()
+        assert rc == tp.TPMLP_OK, f"device status {detail:#x}"
+    return Z.view(M, H)
+
+
+@pytest.mark.parametrize("M", [8192, 5000, 4700])
+def test_tall_units_equal_the_single_sm_kernel(lib, M):
+    """M = 8192: 16 x 16 units, 228 tall + 56 tiles; M = 5000: the last unit's second half
+    holds 136 rows; M = 4700: it holds none (empty halves skipped)."""
+    d = synth.make_inputs(H, F, M, 401)
+    dd = inputs_on_device(d)
+    Z_pair = forward(dd, M, fixed_order=True)
+    Z_single = forward(dd, M, fixed_order=True, single_sm=True)
+    assert torch.equal(Z_pair, Z_single)
+    rows = synth.sample_rows(M, 24)
+    ref = oracle.tpmlp(synth.make_inputs(H, F, M, 401, x_rows=rows)["X"], d["W1"], d["b1"],
+                       d["W2"], d["b2"], K_SHARDS)["Z"]
+    assert_close(to_f64(Z_pair)[rows], ref, what=f"tall Z, M={M}")
+
+
+def test_tall_units_residual_and_fp32(lib):
+    M = 5000
+    d = synth.make_inputs(H, F, M, 402)
+    dd = inputs_on_device(d)
+    outs = {}
+    for single in (False, True):
+        with tp.TPMLP(H, F, K_SHARDS, fixed_order=True, single_sm=single) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            Y = mlp.gemm1(dd["X"])
+            Zr = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+            tp.tpmlp_gemm2_residual(mlp.ctx, Y, M, Zr, dd["X"])
+            torch.cuda.synchronize()
+            assert mlp.status()[0] == tp.TPMLP_OK
+        with tp.TPMLP(H, F, K_SHARDS, fixed_order=True, single_sm=single, z_fp32=True) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            Z32 = mlp.gemm2(Y)
+            torch.cuda.synchronize()
+            assert mlp.status()[0] == tp.TPMLP_OK
+        outs[single] = (Zr, Z32)
+    assert torch.equal(outs[False][0], outs[True][0])
+    assert torch.equal(outs[False][1], outs[True][1])
+
+
+def test_tall_units_with_a_split_tail(lib):
+    """M = 2560: 5 x 16 = 80 units, 76 tall and 8 tiles left, which the tail rule spreads over
+    all pairs."""
+    M = 2560
+    d = synth.make_inputs(H, F, M, 403)
+    dd = inputs_on_device(d)
+    Z1 = forward(dd, M)
+    Z2 = forward(dd, M)
+    assert torch.equal(Z1, Z2)
+    Zf = forward(dd, M, fixed_order=True)
+    assert_close(to_f64(Z1), to_f64(Zf), rel=2e-3, mx=1e-2, what="split tail vs fixed order")
+    rows = synth.sample_rows(M, 24)
+    ref = oracle.tpmlp(synth.make_inputs(H, F, M, 403, x_rows=rows)["X"], d["W1"], d["b1"],
+                       d["W2"], d["b2"], K_SHARDS)["Z"]
+    assert_close(to_f64(Z1)[rows], ref, what="tall + split tail Z vs oracle")
