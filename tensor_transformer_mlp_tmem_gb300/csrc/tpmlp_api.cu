@@ -371,13 +371,15 @@ int launch_gemm2_pair(tpmlp_ctx* c, const CUtensorMap& a_map, const CUtensorMap&
             run.num_tiles = tall.tiles;
             run.sk_first = tall.tiles;  // the remaining tiles whole ...
             run.sk_iters = 0;
-            if (c->sk_partial && resident <= c->num_sms / 2 && !capturing(s) && tall.tiles > 0 &&
-                tall.tiles <= c->num_sms &&
-                tpmlp::tail_split_pays(tall.tiles, args.kb_tile, resident, tall.rows, tall.cols,
+            // ... except their last, partial wave, spread over all pairs when that pays
+            const int whole = tall.tail_first, rem = tall.tiles - whole;
+            if (c->sk_partial && resident <= c->num_sms / 2 && !capturing(s) && rem > 0 &&
+                rem <= c->num_sms &&
+                tpmlp::tail_split_pays(rem, args.kb_tile, resident, tall.rows, tall.cols,
                                        tpmlp::kPairBM, tpmlp::kPairBN,
                                        split_rule_of(c, c->num_sms / 2))) {
-                run.sk_first = 0;  // ... or spread over all pairs
-                run.sk_iters = tall.tiles * args.kb_tile;
+                run.sk_first = whole;
+                run.sk_iters = rem * args.kb_tile;
                 run.sk_partial = c->sk_partial;
                 run.sk_count = c->sk_count;
                 if (++c->sk_epoch == 0) c->sk_epoch = 1;

@@ -215,26 +215,30 @@ inline SplitPlan plan_split_tiles(const SplitLaunch& L, const SplitRule& rule) {
 // 256 x 256 halves sharing each B tile; GemmArgs::tall_units): as many whole waves of them as
 // there are, `tall_units` = floor(T / P) * P of the T = ceil(M / 512) * n_blocks units. The
 // halves of the remaining units become the launch's ordinary tiles (tiles = 2 (T - tall_units),
-// tile t = half t % 2 of unit tall_units + t / 2), which may be split over all pairs as a tail.
+// tile t = half t % 2 of unit tall_units + t / 2): whole waves of them, then a last partial
+// wave that may be split over all pairs as a tail.
 struct TallPlan {
     int tall_units;     // 0: no tall units (launch the ordinary kernel)
     int tall_m_blocks;  // ceil(M / 512)
     int tiles;          // the ordinary tiles after them
-    int rows, cols;     // distinct 256-row and 256-column blocks of those tiles
+    int tail_first;     // their last, partial wave: tiles [tail_first, tiles) ...
+    int rows, cols;     // ... spanning this many 256-row and 256-column blocks
 };
 
 inline TallPlan plan_tall_units(int M, int n_blocks, int group_m, int pairs) {
-    TallPlan p{0, (M + 511) / 512, 0, 0, 0};
+    TallPlan p{0, (M + 511) / 512, 0, 0, 0, 0};
     const int T = p.tall_m_blocks * n_blocks;
     if (pairs <= 0 || T < pairs) return p;
     p.tall_units = T / pairs * pairs;
     p.tiles = 2 * (T - p.tall_units);
+    p.tail_first = p.tiles / pairs * pairs;
     int m_lo = 1 << 30, m_hi = -1, n_cnt = 0, n_prev = -1;
-    for (int u = p.tall_units; u < T; ++u) {
+    for (int t = p.tail_first; t < p.tiles; ++t) {
         int tm, n;
-        decode_tile_mn(group_m, p.tall_m_blocks, n_blocks, u, tm, n);
-        m_lo = 2 * tm < m_lo ? 2 * tm : m_lo;
-        m_hi = 2 * tm + 1 > m_hi ? 2 * tm + 1 : m_hi;
+        decode_tile_mn(group_m, p.tall_m_blocks, n_blocks, p.tall_units + t / 2, tm, n);
+        const int m = 2 * tm + (t & 1);
+        m_lo = m < m_lo ? m : m_lo;
+        m_hi = m > m_hi ? m : m_hi;
         if (n != n_prev) ++n_cnt;
         n_prev = n;
     }

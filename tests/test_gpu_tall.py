@@ -85,3 +85,37 @@ def test_tall_units_with_a_split_tail(lib):
     ref = oracle.tpmlp(synth.make_inputs(H, F, M, 403, x_rows=rows)["X"], d["W1"], d["b1"],
                        d["W2"], d["b2"], K_SHARDS)["Z"]
     assert_close(to_f64(Z1)[rows], ref, what="tall + split tail Z vs oracle")
+
+
+def test_tall_remainder_keeps_whole_waves_and_splits_its_last(lib):
+    """H = 2560 (10 column blocks), M = 6144: 12 x 10 = 120 units, 76 tall, the other 44 give
+    88 tiles = one whole wave of 76 plus 12, which are spread over all pairs. fp32 Z: the
+    split changes the summation order of those 12 tiles only, so the result differs from the
+    fixed order in the last bits (the split ran) and agrees to fp32 accuracy."""
+    h, f, k, M = 2560, 8192, 2, 6144
+    d = synth.make_inputs(h, f, M, 404)
+    dd = inputs_on_device(d)
+    outs = {}
+    with tp.TPMLP(h, f, k, fixed_order=True) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        Y = mlp.gemm1(dd["X"])
+    for fixed in (False, True):
+        with tp.TPMLP(h, f, k, z_fp32=True, fixed_order=fixed) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            outs[fixed] = (mlp.gemm2(Y), mlp.gemm2(Y))
+            torch.cuda.synchronize()
+            assert mlp.status()[0] == tp.TPMLP_OK
+    split, fixed = outs[False][0], outs[True][0]
+    assert torch.equal(outs[False][0], outs[False][1])  # deterministic
+    assert not torch.equal(split, fixed)
+    rel = (torch.linalg.norm(split - fixed) / torch.linalg.norm(fixed)).item()
+    assert rel < 1e-5, rel
+    with tp.TPMLP(h, f, k) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        Z = mlp(dd["X"].view(1, M, h))
+        torch.cuda.synchronize()
+        assert mlp.status()[0] == tp.TPMLP_OK
+    rows = synth.sample_rows(M, 24)
+    ref = oracle.tpmlp(synth.make_inputs(h, f, M, 404, x_rows=rows)["X"], d["W1"], d["b1"],
+                       d["W2"], d["b2"], k)["Z"]
+    assert_close(to_f64(Z.view(M, h))[rows], ref, what="tall remainder with split tail vs oracle")

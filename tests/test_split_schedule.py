@@ -50,7 +50,7 @@ int shim_tall(int M, int n_blocks, int group_m, int pairs, int* out, int* info) 
         const int m = 2 * tm + (t & 1);
         if (m < m_blocks) ++out[m * n_blocks + n];
     }
-    info[0] = p.tiles; info[1] = p.rows; info[2] = p.cols;
+    info[0] = p.tiles; info[1] = p.rows; info[2] = p.cols; info[3] = p.tail_first;
     return p.tall_units;
 }
 void shim_plan(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks, int group_m,
@@ -245,7 +245,7 @@ def test_tall_units_cover_every_tile_once(sched, M, nb, P):
     output tile exactly once; tall units come in whole waves of P."""
     m_blocks = (M + 255) // 256
     out = (ctypes.c_int * (m_blocks * nb))()
-    info = (ctypes.c_int * 3)()
+    info = (ctypes.c_int * 4)()
     tall = sched.shim_tall(M, nb, 8, P, out, info)
     T = (M + 511) // 512 * nb
     if T < P:
@@ -253,6 +253,7 @@ def test_tall_units_cover_every_tile_once(sched, M, nb, P):
         return
     assert tall == T // P * P and tall % P == 0
     assert info[0] == 2 * (T - tall)
+    assert info[3] == info[0] // P * P  # whole waves of the remaining tiles, then the tail
     assert list(out) == [1] * (m_blocks * nb)
 
 
@@ -260,7 +261,7 @@ def test_tall_plans_of_the_workloads(sched):
     """7b (M = 8192, 16 column blocks): 228 tall units, 56 tiles left (the 0.74 wave whole
     tiles had before). GPT-3 (M = 4096, 48 columns): 380 units, 8 tiles left in one column.
     Sweep (M = 16384): 456 units, 112 tiles."""
-    info = (ctypes.c_int * 3)()
+    info = (ctypes.c_int * 4)()
     for M, nb, want_tall, want_tiles in ((8192, 16, 228, 56), (4096, 48, 380, 8), (16384, 16, 456, 112)):
         out = (ctypes.c_int * ((M // 256) * nb))()
         assert sched.shim_tall(M, nb, 8, 76, out, info) == want_tall
@@ -268,3 +269,7 @@ def test_tall_plans_of_the_workloads(sched):
     out = (ctypes.c_int * (16 * 48))()
     sched.shim_tall(4096, 48, 8, 76, out, info)
     assert info[2] == 1 and info[1] == 8  # the GPT-3 remainder: one column block, 8 row blocks
+    # H = 2560, M = 6144: 120 units, 76 tall; 88 tiles = 76 whole + a 12-tile tail in 2 columns
+    out = (ctypes.c_int * (24 * 10))()
+    assert sched.shim_tall(6144, 10, 8, 76, out, info) == 76
+    assert info[0] == 88 and info[3] == 76 and info[2] == 2
