@@ -349,7 +349,7 @@ bool w2_blocked(const tpmlp_ctx* c) { return c->pair2; }
 #endif
 template <Mode MODE, bool F32>
 int launch_gemm2_pair(tpmlp_ctx* c, const CUtensorMap& a_map, const CUtensorMap& b_map,
-                      const GemmArgs& args, cudaStream_t s) {
+                      const GemmArgs& args, cudaStream_t s, const CUtensorMap* b2 = nullptr) {
     if (args.kb_tile >= TPMLP_TALL_MIN_KB) {
         auto kern = tpmlp::tpmlp_gemm_pair_kernel<TPMLP_TALL_STAGES, 2, MODE, F32, false, true>;
         constexpr uint32_t smem = tpmlp::PairSmem<TPMLP_TALL_STAGES, 2, true>::kTotal;
@@ -385,12 +385,13 @@ int launch_gemm2_pair(tpmlp_ctx* c, const CUtensorMap& a_map, const CUtensorMap&
                 if (++c->sk_epoch == 0) c->sk_epoch = 1;
                 run.sk_epoch = c->sk_epoch;
             }
-            TPMLP_CUDA(c, launch_overlapped(kern, 2 * resident, smem, s, a_map, b_map, b_map, run));
+            TPMLP_CUDA(c, launch_overlapped(kern, 2 * resident, smem, s, a_map, b_map,
+                                            b2 ? *b2 : b_map, run));
             ++c->launches;
             return TPMLP_OK;
         }
     }
-    return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, MODE, F32>(c, a_map, b_map, args, s);
+    return launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, MODE, F32>(c, a_map, b_map, args, s, b2);
 }
 
 GemmArgs base_args(const tpmlp_ctx* c, int64_t M, int ldo, int bm, int bn, int group_m) {
@@ -1337,8 +1338,8 @@ int tpmlp_backward(tpmlp_ctx* c, const void* dZ, const void* X, const void* Ysav
         a.out = dX;
         const bool f32 = (c->flags & TPMLP_FLAG_Z_FP32) != 0;
         if (c->pair2)
-            r = f32 ? launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, true>(c, c->tmY, tw1p, a, s)
-                    : launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, false>(c, c->tmY, tw1p, a, s);
+            r = f32 ? launch_gemm2_pair<Mode::kGemm2, true>(c, c->tmY, tw1p, a, s)
+                    : launch_gemm2_pair<Mode::kGemm2, false>(c, c->tmY, tw1p, a, s);
         else
             r = f32 ? dispatch_gemm<Mode::kGemm2, true>(c, c->bn2, c->tmY, tw1, a, s)
                     : dispatch_gemm<Mode::kGemm2, false>(c, c->bn2, c->tmY, tw1, a, s);
@@ -1444,8 +1445,8 @@ int tpmlp_backward_swiglu(tpmlp_ctx* c, const void* dZ, const void* X, const voi
         a.out = dX;
         const bool f32 = (c->flags & TPMLP_FLAG_Z_FP32) != 0;
         if (pair_h)
-            r = f32 ? launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, true>(c, tdgu, twg, a, s, &twu)
-                    : launch_pair<TPMLP_PAIR_STAGES, TPMLP_PAIR_ACC, Mode::kGemm2, false>(c, tdgu, twg, a, s, &twu);
+            r = f32 ? launch_gemm2_pair<Mode::kGemm2, true>(c, tdgu, twg, a, s, &twu)
+                    : launch_gemm2_pair<Mode::kGemm2, false>(c, tdgu, twg, a, s, &twu);
         else
             r = f32 ? dispatch_gemm<Mode::kGemm2, true>(c, bn_h, tdgu, twg, a, s, &twu)
                     : dispatch_gemm<Mode::kGemm2, false>(c, bn_h, tdgu, twg, a, s, &twu);
