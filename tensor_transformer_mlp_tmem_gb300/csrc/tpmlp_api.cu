@@ -115,7 +115,10 @@ struct tpmlp_ctx {
 
 namespace {
 
-constexpr int kHostChunksMax = 4;  // row chunks of tpmlp_forward_host's copy/compute pipeline
+#ifndef TPMLP_HOST_CHUNKS_MAX
+#define TPMLP_HOST_CHUNKS_MAX 4
+#endif
+constexpr int kHostChunksMax = TPMLP_HOST_CHUNKS_MAX;  // row chunks of tpmlp_forward_host's pipeline
 
 using tpmlp::GemmArgs;
 using tpmlp::Mode;
@@ -368,6 +371,7 @@ int launch_gemm2_pair(tpmlp_ctx* c, const CUtensorMap& a_map, const CUtensorMap&
             GemmArgs run = args;
             run.tall_units = tall.tall_units;
             run.tall_m_blocks = tall.tall_m_blocks;
+            run.tall_rest = tall.tall_rest;
             run.num_tiles = tall.tiles;
             run.sk_first = tall.tiles;  // the remaining tiles whole ...
             run.sk_iters = 0;
@@ -600,6 +604,7 @@ int plan_host_chunks(const tpmlp_ctx* c, int64_t M, int64_t* rows) {
         g.col_tiles = N[i] / w;
         g.slots = pair[i] ? pairs : c->num_sms;
         g.tile_s = 2.0 * g.tile_rows * w * K[i] / (c->rates.gemm_flops / g.slots);
+        g.launch_s = tpmlp::kChunkLaunchS;
     }
     m.x_row_bytes = 2.0 * c->H;
     m.z_row_bytes = static_cast<double>(c->H) * z_elem_bytes(c);

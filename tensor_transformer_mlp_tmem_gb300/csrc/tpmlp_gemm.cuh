@@ -120,13 +120,15 @@ struct GemmArgs {
     uint32_t sk_epoch;     // new for every launch that splits
     int b_blocked;         // CTA-pair second GEMM: B is the packed operand in 16 KB blocks
                            // (2-D map of 128-byte rows; see transpose_blocked_bf16_kernel)
-    // Tall units (CTA-pair kernel, TALL instantiation): the output is also cut into 512 x 256
-    // units of two 256-row halves, numbered like tiles over tall_m_blocks = ceil(M / 512) row
-    // blocks. Units [0, tall_units) are computed whole, round robin over the pairs; the tiles
-    // of the launch (num_tiles, sk_*) are then the 256-row halves of the units after them:
-    // tile t is half t % 2 of unit tall_units + t / 2 (a half wholly below row M is empty).
+    // Tall units (CTA-pair kernel, TALL instantiation): the whole 512-row blocks of the output,
+    // tall_m_blocks = floor(M / 512) of them, are also cut into 512 x 256 units of two 256-row
+    // halves, numbered like tiles. Units [0, tall_units) are computed whole, round robin over
+    // the pairs; the tiles of the launch (num_tiles, sk_*) then cover the rest: the halves of
+    // the remaining units (tiles [0, tall_rest)) and the row blocks below the last whole 512
+    // rows (tpmlp_plan.h, decode_tall_rest).
     int tall_units;        // 0: no tall units
     int tall_m_blocks;
+    int tall_rest;
 };
 
 constexpr int kSkSlotFloats = 128 * 256;  // one CTA's half of a 256 x 256 accumulator
@@ -671,16 +673,16 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, const GemmArgs
 }
 
 // Row block (of kBM or kPairBM rows) and column block of tile t; with tall units, of the
-// 256-row half that tile t stands for (see GemmArgs::tall_units). m_blk >= m_blocks: empty.
+// ordinary tile t after them (see GemmArgs::tall_units).
 // A tall unit of the second GEMM (CTA-pair kernel): this warp's share of both accumulators,
-// the first half's rows (accumulator at taddr0, this lane's row row0) and, when `second`, the
-// second half's (taddr1, row1) over the same output columns, 32 columns at a time with both
-// halves' tensor-memory loads in flight together. `release` hands both accumulators back once
-// their last columns are in registers.
+// the first half's rows (accumulator at taddr0, this lane's row row0) and the second half's
+// (taddr1, row1) over the same output columns, 32 columns at a time with both halves'
+// tensor-memory loads in flight together. `release` hands both accumulators back once their
+// last columns are in registers.
 template <Mode MODE, bool OUT_F32, int WIDTH, typename Release>
-__device__ __forceinline__ void drain_tall(uint32_t taddr0, uint32_t taddr1, bool second,
-                                           const GemmArgs& args, int row0, int row1, int n0,
-                                           int part, uint32_t stage, Release release) {
+__device__ __forceinline__ void drain_tall(uint32_t taddr0, uint32_t taddr1, const GemmArgs& args,
+                                           int row0, int row1, int n0, int part, uint32_t stage,
+                                           Release release) {
     static_assert(MODE == Mode::kGemm2 || MODE == Mode::kGemm2Residual, "tall units: second GEMM");
     constexpr int kCols = WIDTH / kEpiParts;
     const int c0 = part * kCols;
@@ -688,26 +690,23 @@ __device__ __forceinline__ void drain_tall(uint32_t taddr0, uint32_t taddr1, boo
     for (int c = c0; c < c0 + kCols; c += 32) {
         uint32_t v0[32], v1[32];
         ptx::tmem_ld_32x32b_x32(taddr0 + c, v0);
-        if (second) ptx::tmem_ld_32x32b_x32(taddr1 + c, v1);
+        ptx::tmem_ld_32x32b_x32(taddr1 + c, v1);
         ptx::tmem_wait_ld(v0);
-        if (second) ptx::tmem_wait_ld(v1);
+        ptx::tmem_wait_ld(v1);
         if (c + 32 == c0 + kCols) release();
         epilogue_slice<MODE, OUT_F32>(v0, args.bias, args.out, row0, args.M, args.ldo, n0 + c,
                                       args.residual, args.out2, stage);
-        if (second)
-            epilogue_slice<MODE, OUT_F32>(v1, args.bias, args.out, row1, args.M, args.ldo, n0 + c,
-                                          args.residual, args.out2, stage);
+        epilogue_slice<MODE, OUT_F32>(v1, args.bias, args.out, row1, args.M, args.ldo, n0 + c,
+                                      args.residual, args.out2, stage);
     }
 }
 
 __device__ __forceinline__ void decode_tile(const GemmArgs& a, int t, int& m_blk, int& n_blk) {
-    if (a.tall_units > 0) {
-        int tm;
-        decode_tile_mn(a.group_m, a.tall_m_blocks, a.n_blocks, a.tall_units + (t >> 1), tm, n_blk);
-        m_blk = 2 * tm + (t & 1);
-    } else {
+    if (a.tall_units > 0)
+        decode_tall_rest(a.group_m, a.tall_m_blocks, a.tall_units, a.tall_rest, a.m_blocks,
+                         a.n_blocks, t, m_blk, n_blk);
+    else
         decode_tile_mn(a.group_m, a.m_blocks, a.n_blocks, t, m_blk, n_blk);
-    }
 }
 
 // Bring the bias of this warp's columns in tile t (the CTA's first) into L2 while the tile's

@@ -53,7 +53,8 @@ struct PairSmem {
 // MN: both operands M-/N-contiguous (the weight-gradient GEMMs): each CTA loads its 128 rows
 // of A and of B as two 64 (MN) x 64 (K) boxes each (see tpmlp_gemm_kernel).
 // TALL (second-GEMM modes, two accumulators): each pair first computes tall units of
-// 512 x 256 outputs, args.tall_units of them round robin, with both accumulators: per
+// 512 x 256 outputs (whole 512-row blocks), args.tall_units of them round robin, with both
+// accumulators: per
 // reduction block one B tile and the A tiles of both 256-row halves, two MMAs per 16-deep
 // step. Against two 256 x 256 tiles that is a quarter less operand traffic per multiply-add;
 // the accumulators are not double-buffered then, so a unit's epilogue does not overlap the
@@ -149,9 +150,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     int tm, n_blk;
                     decode_tile_mn(args.group_m, args.tall_m_blocks, args.n_blocks, u, tm, n_blk);
                     const int m0 = tm * 2 * kPairBM + static_cast<int>(rank) * 128;
-                    const bool second = tm * 2 * kPairBM + kPairBM < args.M;  // second half has rows
                     const int nb = n_blk * kPairBN + static_cast<int>(rank) * 128;
-                    const uint32_t bytes = 2 * ((second ? 2 : 1) * 128 * kBK * 2 + 128 * kBK * 2);
+                    constexpr uint32_t bytes = 2 * L::kStageBytes;  // both CTAs: two A boxes, B
                     for (int kb = 0; kb < args.kb_tile; ++kb) {
                         if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status,
                                             kCode | kSiteProducer)) {
@@ -162,7 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                         const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);
                         if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
                         load_a(sa, fb, kb, m0);
-                        if (second) load_a(sa + 128 * kBK * 2, fb, kb, m0 + kPairBM);
+                        load_a(sa + 128 * kBK * 2, fb, kb, m0 + kPairBM);
                         load_b(sa + L::kABytes, fb, kb, nb);
                         ++issued;
                         if (++stage == STAGES) {
@@ -249,9 +249,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 // a tall unit takes both accumulators (acc is 0 at the start of each: units
                 // come first and take two each)
                 for (int u = pair; ok && u < args.tall_units; u += num_pairs) {
-                    int tm, n_blk;
-                    decode_tile_mn(args.group_m, args.tall_m_blocks, args.n_blocks, u, tm, n_blk);
-                    const bool second = tm * 2 * kPairBM + kPairBM < args.M;
                     if (!ptx::mbar_wait(tempty_bar(0), acc_phase ^ 1u, abort_flag, args.status,
                                         kCode | kSiteMmaAccum) ||
                         !ptx::mbar_wait(tempty_bar(1), acc_phase ^ 1u, abort_flag, args.status,
@@ -276,9 +273,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                             const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
                             ptx::mma_bf16_ss_pair(tmem_base, da0 + 2u * kk, db + 2u * kk, kIdesc,
                                                   accumulate);
-                            if (second)
-                                ptx::mma_bf16_ss_pair(tmem_base + kPairBN, da1 + 2u * kk,
-                                                      db + 2u * kk, kIdesc, accumulate);
+                            ptx::mma_bf16_ss_pair(tmem_base + kPairBN, da1 + 2u * kk,
+                                                  db + 2u * kk, kIdesc, accumulate);
                         }
                         ptx::mma_commit_pair(empty_bar(stage), 0x3);  // stage s free in both CTAs
                         if (++stage == STAGES) {
@@ -351,7 +347,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             for (int u = pair; u < args.tall_units; u += num_pairs) {
                 int tm, n_blk;
                 decode_tile_mn(args.group_m, args.tall_m_blocks, args.n_blocks, u, tm, n_blk);
-                const bool second = tm * 2 * kPairBM + kPairBM < args.M;
                 const bool ok = ptx::mbar_wait(tfull_bar(0), acc_phase, abort_flag, args.status,
                                                kCode | kSiteEpilogue) &&
                                 ptx::mbar_wait(tfull_bar(1), acc_phase, abort_flag, args.status,
@@ -371,7 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                         ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(tempty_bar(1), 0));
                     }
                 };
-                drain_tall<MODE, OUT_F32, kPairBN>(taddr, taddr + kPairBN, second, args, row0,
+                drain_tall<MODE, OUT_F32, kPairBN>(taddr, taddr + kPairBN, args, row0,
                                                    row0 + kPairBM, n_blk * kPairBN, part,
                                                    stage_buf, release);
                 acc_phase ^= 1u;

@@ -28,7 +28,8 @@
 //
 // The model: one copy stream in, one copy stream out, one compute stream.
 //   in_c   = in_{c-1} + X bytes of chunk c / bandwidth in
-//   comp_c = max(comp_{c-1}, in_c) + sum over both GEMMs of rounds(chunk c) * round time
+//   comp_c = max(comp_{c-1}, in_c) + sum over both GEMMs of (rounds(chunk c) * round time
+//            + a fixed cost per launch)
 //   out_c  = max(out_{c-1}, comp_c) + Z bytes of chunk c / bandwidth out
 // and the pass ends at max(comp_last, out_last).
 //
@@ -212,31 +213,61 @@ inline SplitPlan plan_split_tiles(const SplitLaunch& L, const SplitRule& rule) {
 // ---------------------------------------------------------------- tall units
 //
 // The second GEMM of a deep reduction runs most of its output as 512 x 256 tall units (two
-// 256 x 256 halves sharing each B tile; GemmArgs::tall_units): as many whole waves of them as
-// there are, `tall_units` = floor(T / P) * P of the T = ceil(M / 512) * n_blocks units. The
-// halves of the remaining units become the launch's ordinary tiles (tiles = 2 (T - tall_units),
-// tile t = half t % 2 of unit tall_units + t / 2): whole waves of them, then a last partial
-// wave that may be split over all pairs as a tail.
+// 256 x 256 halves sharing each B tile; GemmArgs::tall_units) over the whole 512-row blocks,
+// tall_m_blocks = floor(M / 512) of them: as many whole waves of units as there are,
+// `tall_units` = floor(T / P) * P of the T = tall_m_blocks * n_blocks. The launch's ordinary
+// tiles then cover the rest, in this order:
+//   tiles [0, tall_rest):  the 256-row halves of the remaining units (tall_rest = 2 (T -
+//                          tall_units); tile t = half t % 2 of unit tall_units + t / 2);
+//   tiles [tall_rest, ..): the 256-row blocks below the last whole 512 rows (0, 1 or 2 of
+//                          them), column by column.
+// They run as whole waves, then a last partial wave that may be split over all pairs as a tail.
+// Tall units are used only when they take no more rounds of tiles than ordinary tiles alone
+// (a unit counting two rounds).
 struct TallPlan {
     int tall_units;     // 0: no tall units (launch the ordinary kernel)
-    int tall_m_blocks;  // ceil(M / 512)
-    int tiles;          // the ordinary tiles after them
+    int tall_m_blocks;  // floor(M / 512)
+    int tall_rest;      // ordinary tiles that are halves of the remaining units
+    int tiles;          // all ordinary tiles after the units
     int tail_first;     // their last, partial wave: tiles [tail_first, tiles) ...
     int rows, cols;     // ... spanning this many 256-row and 256-column blocks
 };
 
+// The 256-row block and column block of ordinary tile t of a launch with tall units.
+TPMLP_HD void decode_tall_rest(int group_m, int tall_m_blocks, int tall_units, int tall_rest,
+                               int m_blocks, int n_blocks, int t, int& m_blk, int& n_blk) {
+    if (t < tall_rest) {
+        int tm;
+        decode_tile_mn(group_m, tall_m_blocks, n_blocks, tall_units + (t >> 1), tm, n_blk);
+        m_blk = 2 * tm + (t & 1);
+    } else {
+        const int left = m_blocks - 2 * tall_m_blocks;  // 1 or 2 row blocks below the units
+        const int i = t - tall_rest;
+        m_blk = 2 * tall_m_blocks + i % left;
+        n_blk = i / left;
+    }
+}
+
 inline TallPlan plan_tall_units(int M, int n_blocks, int group_m, int pairs) {
-    TallPlan p{0, (M + 511) / 512, 0, 0, 0, 0};
+    TallPlan p{0, M / 512, 0, 0, 0, 0, 0};
+    const int m_blocks = (M + 255) / 256;
     const int T = p.tall_m_blocks * n_blocks;
     if (pairs <= 0 || T < pairs) return p;
-    p.tall_units = T / pairs * pairs;
-    p.tiles = 2 * (T - p.tall_units);
-    p.tail_first = p.tiles / pairs * pairs;
+    const int units = T / pairs * pairs;
+    const int rest = 2 * (T - units);
+    const int tiles = rest + (m_blocks - 2 * p.tall_m_blocks) * n_blocks;
+    const int rounds_tiles = (m_blocks * n_blocks + pairs - 1) / pairs;
+    const int rounds_tall = 2 * units / pairs + (tiles + pairs - 1) / pairs;
+    if (rounds_tall > rounds_tiles) return p;
+    p.tall_units = units;
+    p.tall_rest = rest;
+    p.tiles = tiles;
+    p.tail_first = tiles / pairs * pairs;
     int m_lo = 1 << 30, m_hi = -1, n_cnt = 0, n_prev = -1;
     for (int t = p.tail_first; t < p.tiles; ++t) {
-        int tm, n;
-        decode_tile_mn(group_m, p.tall_m_blocks, n_blocks, p.tall_units + t / 2, tm, n);
-        const int m = 2 * tm + (t & 1);
+        int m, n;
+        decode_tall_rest(group_m, p.tall_m_blocks, p.tall_units, p.tall_rest, m_blocks, n_blocks,
+                         t, m, n);
         m_lo = m < m_lo ? m : m_lo;
         m_hi = m > m_hi ? m : m_hi;
         if (n != n_prev) ++n_cnt;
@@ -306,7 +337,18 @@ struct ChunkGemm {
     int64_t col_tiles;   // output tiles per row block
     int64_t slots;       // tiles that run at once (resident CTA pairs or SMs)
     double tile_s;       // seconds per round of tiles
+    double launch_s;     // fixed seconds per launch (set-up, first wave's ramp, last wave's drain)
 };
+
+// The fixed cost of one GEMM launch in the chunk model. Host-buffer forward passes timed with
+// plans of at most 1, 2, 3 and 4 chunks were fastest with 3 chunks at GPT-3, 4 at 7b and 2 at
+// GPT-2; without this cost the model preferred 4 chunks everywhere. Interleaved A/B of the
+// planner with 0, 10 and 20 us: GPT-3 5.936 / 5.899 / 5.874 ms, 7b 1.405 / 1.391 / 1.409 ms,
+// GPT-2 0.203 / 0.187 / 0.204 ms.
+#ifndef TPMLP_CHUNK_LAUNCH_S
+#define TPMLP_CHUNK_LAUNCH_S 10e-6
+#endif
+constexpr double kChunkLaunchS = TPMLP_CHUNK_LAUNCH_S;
 
 struct ChunkModel {
     ChunkGemm g[2];
@@ -326,7 +368,7 @@ inline double simulate_chunks(const ChunkModel& m, const int64_t* rows, int n) {
         double t = in > comp ? in : comp;
         for (const ChunkGemm& g : m.g) {
             const int64_t tiles = ceil_div_i64(rows[i], g.tile_rows) * g.col_tiles;
-            t += static_cast<double>(ceil_div_i64(tiles, g.slots)) * g.tile_s;
+            t += static_cast<double>(ceil_div_i64(tiles, g.slots)) * g.tile_s + g.launch_s;
         }
         comp = t;
         out = (out > comp ? out : comp) + static_cast<double>(rows[i]) * m.z_row_bytes / m.copy_Bps;

@@ -4,9 +4,9 @@ the output as ordinary 256 x 256 tiles in the same launch (split over all pairs 
 rule says so).
 
 A tall unit sums each output in the same order as a whole tile, so with TPMLP_FLAG_FIXED_ORDER
-its Z must equal the single-SM kernel's bit for bit, at token counts whose last 512-row unit
-is full, has a partial second half, or has an empty second half; also with the residual add
-and with fp32 output. With the split tail the result is checked against the oracle, for
+its Z must equal the single-SM kernel's bit for bit, at token counts that are whole 512-row
+blocks or leave one or two 256-row blocks below them (those run as ordinary tiles); also with
+the residual add and with fp32 output. With the split tail the result is checked against the oracle, for
 determinism, and against the fixed order within the split's rounding."""
 import numpy as np
 import pytest
@@ -34,8 +34,9 @@ def forward(dd, M, **kw):
 
 @pytest.mark.parametrize("M", [8192, 5000, 4700])
 def test_tall_units_equal_the_single_sm_kernel(lib, M):
-    """M = 8192: 16 x 16 units, 228 tall + 56 tiles; M = 5000: the last unit's second half
-    holds 136 rows; M = 4700: it holds none (empty halves skipped)."""
+    """M = 8192: 16 x 16 units, 228 tall + 56 tiles; M = 5000: 9 whole 512-row blocks as units
+    (76 tall) and two 256-row blocks below them (392 rows) as tiles; M = 4700: one such block
+    (92 rows)."""
     d = synth.make_inputs(H, F, M, 401)
     dd = inputs_on_device(d)
     Z_pair = forward(dd, M, fixed_order=True)

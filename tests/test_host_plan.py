@@ -27,10 +27,12 @@ static tpmlp::ChunkModel model(const double* p) {
         m.g[i].col_tiles = (int64_t)p[4 * i + 1];
         m.g[i].slots = (int64_t)p[4 * i + 2];
         m.g[i].tile_s = p[4 * i + 3];
+        m.g[i].launch_s = p[11];
     }
     m.x_row_bytes = p[8]; m.z_row_bytes = p[9]; m.copy_Bps = p[10];
     return m;
 }
+double shim_launch_s() { return tpmlp::kChunkLaunchS; }
 int shim_plan(const double* p, int64_t M, int max_chunks, int64_t max_granules, int64_t* rows) {
     return tpmlp::plan_chunks(model(p), M, max_chunks, max_granules, rows);
 }
@@ -67,6 +69,8 @@ def plan(tmp_path_factory):
     lib.shim_plan.restype = ctypes.c_int
     lib.shim_sim.argtypes = [dp, i64p, ctypes.c_int]
     lib.shim_sim.restype = ctypes.c_double
+    lib.shim_launch_s.argtypes = []
+    lib.shim_launch_s.restype = ctypes.c_double
     lib.shim_rates.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int, dp]
     lib.shim_rates.restype = None
     lib.shim_split.argtypes = [ctypes.c_int, ctypes.c_double] + [ctypes.c_int] * 6 + \
@@ -75,10 +79,10 @@ def plan(tmp_path_factory):
     return lib
 
 
-def params(H=4096, F=16384, pairs=76, rate=1.7e15):
+def params(H=4096, F=16384, pairs=76, rate=1.7e15, launch_s=10e-6):
     t1 = 2.0 * 256 * 256 * H / (rate / pairs)
     t2 = 2.0 * 256 * 256 * F / (rate / pairs)
-    return [256, F // 256, pairs, t1, 256, H // 256, pairs, t2, 2.0 * H, 2.0 * H, 168e9]
+    return [256, F // 256, pairs, t1, 256, H // 256, pairs, t2, 2.0 * H, 2.0 * H, 168e9, launch_s]
 
 
 def call_plan(lib, p, M, max_chunks=4, max_granules=64):
@@ -126,13 +130,24 @@ def test_plan_is_the_best_split_under_the_model(plan, M, H, F):
 
 
 def test_model_of_one_chunk(plan):
-    """One chunk: copy in, then both GEMMs in rounds, then copy out."""
+    """One chunk: copy in, then both GEMMs in rounds plus their fixed launch costs, then copy
+    out."""
     p = params()
     M = 8192
-    t1 = -(-(M // 256) * 64 // 76) * p[3]
-    t2 = -(-(M // 256) * 16 // 76) * p[7]
+    t1 = -(-(M // 256) * 64 // 76) * p[3] + p[11]
+    t2 = -(-(M // 256) * 16 // 76) * p[7] + p[11]
     want = M * 8192 / 168e9 + t1 + t2 + M * 8192 / 168e9
     assert call_sim(plan, p, [M]) == pytest.approx(want, rel=1e-12)
+
+
+@pytest.mark.parametrize("H,F,M,want", [(12288, 49152, 4096, 3), (4096, 16384, 8192, 4)])
+def test_chunk_counts_that_measured_fastest(plan, H, F, M, want):
+    """With the library's fixed launch cost and a GB300's rates, the planner picks the chunk
+    counts that measured fastest end to end at these shapes: GPT-3 3, 7b 4."""
+    g, _, c = rates(plan, 152)
+    p = params(H=H, F=F, rate=g, launch_s=plan.shim_launch_s())
+    p[10] = c
+    assert len(call_plan(plan, p, M)) == want
 
 
 def test_7b_plan_beats_even_split(plan):

@@ -32,25 +32,25 @@ int shim_pair_of(int sk_iters, int num_pairs, long long i) {
     return tpmlp::work_pair_of(sk_iters, num_pairs, i);
 }
 // tall units of the second GEMM: out[m * n_blocks + n] counts how often 256-row block m,
-// column block n is computed (tall units give two halves, the remaining tiles one each; an
-// empty half below row M is counted at m >= m_blocks); returns the number of tall units and
-// writes the plan's tiles / rows / cols to info[0..2]
+// column block n is computed (tall units give two halves, the ordinary tiles after them one
+// each); returns the number of tall units and writes tiles / rows / cols / tail_first /
+// tall_rest to info[0..4]
 int shim_tall(int M, int n_blocks, int group_m, int pairs, int* out, int* info) {
     const tpmlp::TallPlan p = tpmlp::plan_tall_units(M, n_blocks, group_m, pairs);
     const int m_blocks = (M + 255) / 256;
     for (int u = 0; u < p.tall_units; ++u) {
         int tm, n;
         tpmlp::decode_tile_mn(group_m, p.tall_m_blocks, n_blocks, u, tm, n);
-        for (int h = 0; h < 2; ++h)
-            if (2 * tm + h < m_blocks) ++out[(2 * tm + h) * n_blocks + n];
+        for (int h = 0; h < 2; ++h) ++out[(2 * tm + h) * n_blocks + n];
     }
-    for (int t = 0; t < p.tiles; ++t) {  // GemmArgs::tall_units: tile t = half t % 2 of unit ...
-        int tm, n;
-        tpmlp::decode_tile_mn(group_m, p.tall_m_blocks, n_blocks, p.tall_units + t / 2, tm, n);
-        const int m = 2 * tm + (t & 1);
-        if (m < m_blocks) ++out[m * n_blocks + n];
+    for (int t = 0; t < p.tiles; ++t) {
+        int m, n;
+        tpmlp::decode_tall_rest(group_m, p.tall_m_blocks, p.tall_units, p.tall_rest, m_blocks,
+                                n_blocks, t, m, n);
+        if (m < m_blocks && n < n_blocks) ++out[m * n_blocks + n];
+        else out[0] += 1000;  // out of range: fails the test
     }
-    info[0] = p.tiles; info[1] = p.rows; info[2] = p.cols; info[3] = p.tail_first;
+    info[0] = p.tiles; info[1] = p.rows; info[2] = p.cols; info[3] = p.tail_first; info[4] = p.tall_rest;
     return p.tall_units;
 }
 void shim_plan(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks, int group_m,
@@ -239,31 +239,36 @@ def test_narrow_launch_schedule(sched, T, kb):
 
 @pytest.mark.parametrize("M,nb,P", [(8192, 16, 76), (4096, 48, 76), (16384, 16, 76), (5000, 16, 76),
                                     (4700, 16, 76), (2560, 16, 76), (4097, 16, 74), (1000, 16, 76),
-                                    (12345, 12, 75)])
+                                    (12345, 12, 75), (768, 48, 76), (3584, 48, 76), (6144, 10, 76)])
 def test_tall_units_cover_every_tile_once(sched, M, nb, P):
-    """Tall units (two 256-row halves each) and the tiles after them compute every 256 x 256
-    output tile exactly once; tall units come in whole waves of P."""
+    """Tall units (two 256-row halves each, whole 512-row blocks only) and the tiles after
+    them compute every 256 x 256 output tile exactly once; tall units come in whole waves of
+    P, and only when they take no more rounds than ordinary tiles alone."""
     m_blocks = (M + 255) // 256
     out = (ctypes.c_int * (m_blocks * nb))()
-    info = (ctypes.c_int * 4)()
+    info = (ctypes.c_int * 5)()
     tall = sched.shim_tall(M, nb, 8, P, out, info)
-    T = (M + 511) // 512 * nb
-    if T < P:
-        assert tall == 0
+    T = M // 512 * nb
+    if tall == 0:
+        assert T < P or 2 * (T // P) + -(-(m_blocks * nb - 2 * (T // P) * P) // P) > -(-(m_blocks * nb) // P)
         return
     assert tall == T // P * P and tall % P == 0
-    assert info[0] == 2 * (T - tall)
+    assert info[4] == 2 * (T - tall)
+    assert info[0] == info[4] + (m_blocks - 2 * (M // 512)) * nb
     assert info[3] == info[0] // P * P  # whole waves of the remaining tiles, then the tail
     assert list(out) == [1] * (m_blocks * nb)
+    assert 2 * tall // P + -(-info[0] // P) <= -(-(m_blocks * nb) // P)
 
 
 def test_tall_plans_of_the_workloads(sched):
     """7b (M = 8192, 16 column blocks): 228 tall units, 56 tiles left (the 0.74 wave whole
     tiles had before). GPT-3 (M = 4096, 48 columns): 380 units, 8 tiles left in one column.
-    Sweep (M = 16384): 456 units, 112 tiles."""
-    info = (ctypes.c_int * 4)()
-    for M, nb, want_tall, want_tiles in ((8192, 16, 228, 56), (4096, 48, 380, 8), (16384, 16, 456, 112)):
-        out = (ctypes.c_int * ((M // 256) * nb))()
+    Sweep (M = 16384): 456 units, 112 tiles. A 768-row chunk of GPT-3 (one whole 512-row
+    block: 48 units, under a wave) and 1000 tokens at 7b run no tall units."""
+    info = (ctypes.c_int * 5)()
+    for M, nb, want_tall, want_tiles in ((8192, 16, 228, 56), (4096, 48, 380, 8), (16384, 16, 456, 112),
+                                         (768, 48, 0, 0), (1000, 16, 0, 0)):
+        out = (ctypes.c_int * (-(-M // 256) * nb))()
         assert sched.shim_tall(M, nb, 8, 76, out, info) == want_tall
         assert info[0] == want_tiles
     out = (ctypes.c_int * (16 * 48))()
