@@ -120,3 +120,55 @@ def test_tall_remainder_keeps_whole_waves_and_splits_its_last(lib):
     ref = oracle.tpmlp(synth.make_inputs(h, f, M, 404, x_rows=rows)["X"], d["W1"], d["b1"],
                        d["W2"], d["b2"], k)["Z"]
     assert_close(to_f64(Z.view(M, h))[rows], ref, what="tall remainder with split tail vs oracle")
+
+
+def test_tall_units_in_a_cuda_graph(lib):
+    """M = 2560: 76 tall units and 8 tiles. Captured launches never split, so every replay on
+    new inputs equals the eager forward with TPMLP_FLAG_FIXED_ORDER (also tall units, no
+    split) bit for bit."""
+    M = 2560
+    d = synth.make_inputs(H, F, M, 405)
+    dd = inputs_on_device(d)
+    X0 = dd["X"].view(1, M, H)
+    X1 = torch.flip(X0, dims=[1]).contiguous()
+    with tp.TPMLP(H, F, K_SHARDS, fixed_order=True) as ref:
+        ref.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        want0, want1 = ref(X0), ref(X1)
+        torch.cuda.synchronize()
+    with tp.TPMLP(H, F, K_SHARDS) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        mlp.reserve(M)
+        Xs = X0.clone()
+        Zs = mlp(Xs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            mlp(Xs, Zs)
+        for X, want in ((X1, want1), (X0, want0), (X1, want1)):
+            Xs.copy_(X)
+            Zs.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(Zs, want)
+        assert mlp.status()[0] == tp.TPMLP_OK
+
+
+def test_tall_backward_dx_equals_the_single_sm_kernel(lib):
+    """The backward's dX = sum_i dA_i W1_i^T (128 reduction blocks at F = 8192) runs tall
+    units at M = 2560; with TPMLP_FLAG_FIXED_ORDER it equals the single-SM kernel's dX bit for
+    bit, and so do the weight and bias gradients."""
+    M = 2560
+    d = synth.make_inputs(H, F, M, 406)
+    dd = inputs_on_device(d)
+    X = dd["X"].view(1, M, H)
+    dZ = inputs_on_device({"dZ": synth.normal_bf16(406, 60, (M, H), 1.0)})["dZ"].view(1, M, H)
+    grads = {}
+    for single in (False, True):
+        with tp.TPMLP(H, F, K_SHARDS, fixed_order=True, single_sm=single) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            _, Ys, As = mlp.forward_train(X)
+            grads[single] = mlp.backward(dZ, X, Ys, As, dd["W1"], dd["W2"])
+            torch.cuda.synchronize()
+            assert mlp.status()[0] == tp.TPMLP_OK
+    for a, b in zip(grads[False], grads[True]):
+        assert torch.equal(a, b)
