@@ -177,7 +177,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             while (ok && work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
                 int m_blk, n_blk;
                 decode_tile(args, t, m_blk, n_blk);
-                if (m_blk >= args.m_blocks) continue;  // an empty half of a tall unit
                 const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;  // this CTA's A rows
                 const int n0 = n_blk * kPairBN;
                 const int nb = n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
@@ -291,11 +290,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             WorkCursor cur = work_begin(args.sk_iters, pair, num_pairs);
             int t, kb0, kb1;
             while (ok && work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
-                if constexpr (TALL) {
-                    int m_blk, n_blk;
-                    decode_tile(args, t, m_blk, n_blk);
-                    if (m_blk >= args.m_blocks) continue;  // an empty half of a tall unit
-                }
                 if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status,
                                     kCode | kSiteMmaAccum)) {
                     ok = false;
@@ -382,7 +376,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         while (ok_tall && work_next(args.sk_first, args.kb_tile, num_pairs, cur, t, kb0, kb1)) {
             int m_blk, n_blk;
             decode_tile(args, t, m_blk, n_blk);
-            if (m_blk >= args.m_blocks) continue;  // an empty half of a tall unit
             const int m0 = m_blk * kPairBM + static_cast<int>(rank) * 128;
             const int n0 = n_blk * kPairBN;
             bool ok = ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status,
