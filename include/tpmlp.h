@@ -191,6 +191,36 @@ TPMLP_API int tpmlp_forward_host(tpmlp_ctx *ctx, const void *X_host, int64_t B, 
                        void *stream);
 
 /*
+ * tpmlp_forward on host buffers without waiting: queues the copy of X_host in, the forward,
+ * and the copy of Z out to Z_host, and returns. For a stream of calls (a serving loop): the
+ * context stages each call in one of two device slots in turn, so a call's input copy runs
+ * during the kernels of the call before it and its output copy during those of the call
+ * after it. The kernels run on `stream` after the work already queued there; the copies run
+ * on the context's two copy streams, ordered against the kernels by events. The whole call is
+ * one chunk (no row-chunk plan: in a run of calls the copies are hidden by the neighbours'
+ * kernels, and one full-size launch per GEMM is the fastest). Results equal tpmlp_forward's
+ * for the same token count, bit for bit.
+ *   X_host, Z_host  host bf16 [B,S,H] and [B,S,H] (fp32 with TPMLP_FLAG_Z_FP32). Both stay
+ *                   owned by the caller and must stay valid, X_host unchanged and Z_host
+ *                   unread, until tpmlp_host_wait returns. Buffers of calls in flight at the
+ *                   same time must not overlap. Page-locked memory gives the overlap;
+ *                   pageable memory works but each copy then blocks the host.
+ * A larger token count than any earlier async call's waits for the device once (the slots
+ * grow). Errors: as tpmlp_forward_host; a returned error leaves the calls queued before it
+ * intact (tpmlp_host_wait still waits for them).
+ */
+TPMLP_API int tpmlp_forward_host_async(tpmlp_ctx *ctx, const void *X_host, int64_t B, int64_t S,
+                                       void *Z_host, void *stream);
+
+/*
+ * Waits on the host until every host-buffer call of this context queued so far (the async
+ * ones included) has written its Z to host memory. Errors: INVALID_ARG (NULL ctx), the device
+ * check of every entry point, CUDA (a failed copy or kernel; the device status word, read by
+ * tpmlp_get_status, tells a kernel's timeout apart).
+ */
+TPMLP_API int tpmlp_host_wait(tpmlp_ctx *ctx);
+
+/*
  * The first step alone (column-parallel GEMM of every shard + b1 + GeLU):
  *   Y[m, i f + j] = GeLU(b1[i f + j] + sum_h X[m, h] W1[h, i f + j])   rounded to bf16
  *   X device bf16 [M, H]; Y device bf16 [M, F] (shard i in columns [i f, (i+1) f)).
@@ -259,6 +289,16 @@ TPMLP_API int tpmlp_block_forward(tpmlp_ctx *ctx, const void *X, int64_t B, int6
  */
 TPMLP_API int tpmlp_block_forward_host(tpmlp_ctx *ctx, const void *X_host, int64_t B, int64_t S,
                                        void *Z_host, void *stream);
+
+/*
+ * tpmlp_block_forward_host without waiting, as tpmlp_forward_host_async is to
+ * tpmlp_forward_host: the LayerNorm kernel, the first GEMM and the second GEMM with the
+ * residual add of one call run on `stream` while the neighbouring calls' copies run; Z_host
+ * may equal X_host within one call. Requires tpmlp_set_layernorm.
+ * Errors: as tpmlp_block_forward_host.
+ */
+TPMLP_API int tpmlp_block_forward_host_async(tpmlp_ctx *ctx, const void *X_host, int64_t B,
+                                             int64_t S, void *Z_host, void *stream);
 
 /*
  * tpmlp_block_forward with the caller's CUDA events `after_layernorm` and `after_gemm1`

@@ -28,7 +28,8 @@ __all__ = [
     "tpmlp_linear_create", "tpmlp_linear_pack", "tpmlp_linear_forward", "Linear",
     "TPMLP_LINEAR_COLUMN", "TPMLP_LINEAR_ROW", "tpmlp_forward_train", "tpmlp_backward",
     "tpmlp_backward_swiglu", "tpmlp_set_device_rates", "tpmlp_get_device_rates", "tpmlp_build_id",
-    "tpmlp_forward_marked", "tpmlp_block_forward_marked",
+    "tpmlp_forward_marked", "tpmlp_block_forward_marked", "tpmlp_forward_host_async",
+    "tpmlp_block_forward_host_async", "tpmlp_host_wait",
 ]
 
 TPMLP_OK = 0
@@ -85,6 +86,9 @@ def load_library() -> ctypes.CDLL:
         "tpmlp_reserve": ([vp, i64], ctypes.c_int),
         "tpmlp_forward": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
         "tpmlp_forward_host": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_forward_host_async": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_block_forward_host_async": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
+        "tpmlp_host_wait": ([vp], ctypes.c_int),
         "tpmlp_forward_marked": ([vp, vp, i64, i64, vp, vp, vp], ctypes.c_int),
         "tpmlp_block_forward_marked": ([vp, vp, i64, i64, vp, vp, vp, vp], ctypes.c_int),
         "tpmlp_forward_noalloc": ([vp, vp, i64, i64, vp, vp], ctypes.c_int),
@@ -218,6 +222,23 @@ def tpmlp_block_forward_marked(ctx: int, X, B: int, S: int, Z, after_layernorm, 
 def tpmlp_forward_host(ctx: int, X_host, B: int, S: int, Z_host, stream=None) -> None:
     _check(load_library().tpmlp_forward_host(ctx, _ptr(X_host), B, S, _ptr(Z_host),
                                              _stream(stream)), "tpmlp_forward_host", ctx)
+
+
+def tpmlp_forward_host_async(ctx: int, X_host, B: int, S: int, Z_host, stream=None) -> None:
+    """Queues the forward on host buffers and returns; X_host and Z_host (pinned torch CPU
+    tensors) must stay alive and untouched until tpmlp_host_wait."""
+    _check(load_library().tpmlp_forward_host_async(ctx, _ptr(X_host), B, S, _ptr(Z_host),
+                                                   _stream(stream)), "tpmlp_forward_host_async", ctx)
+
+
+def tpmlp_block_forward_host_async(ctx: int, X_host, B: int, S: int, Z_host, stream=None) -> None:
+    _check(load_library().tpmlp_block_forward_host_async(ctx, _ptr(X_host), B, S, _ptr(Z_host),
+                                                         _stream(stream)),
+           "tpmlp_block_forward_host_async", ctx)
+
+
+def tpmlp_host_wait(ctx: int) -> None:
+    _check(load_library().tpmlp_host_wait(ctx), "tpmlp_host_wait", ctx)
 
 
 def tpmlp_forward_noalloc(ctx: int, X, B: int, S: int, Z, stream=None) -> None:

@@ -52,6 +52,14 @@ struct tpmlp_ctx {
     int64_t plan_M = -1;
     int plan_n = 0;
     int64_t plan_rows[4] = {};
+    // tpmlp_forward_host_async: two staging slots used in turn, so that a call's copies in and
+    // out overlap the kernels of the calls before and after it
+    void* Xa[2] = {};
+    void* Za[2] = {};
+    int64_t async_rows = 0;
+    cudaEvent_t a_in[2] = {}, a_xfree[2] = {}, a_zready[2] = {}, a_zfree[2] = {};
+    bool a_used[2] = {};
+    uint32_t a_calls = 0;
 
     // activation tensor maps of the last call (re-encoded only when pointer or rows change)
     const void* x_map_ptr = nullptr;
@@ -722,6 +730,29 @@ int run_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t
     return TPMLP_OK;
 }
 
+// The copy streams and events of the host-buffer entry points (created on first use).
+int ensure_copy_streams(tpmlp_ctx* c) {
+    if (c->s_in) return TPMLP_OK;
+    cudaStream_t in = nullptr, out = nullptr;
+    TPMLP_CUDA(c, cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking));
+    TPMLP_CUDA(c, cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking));
+    for (int i = 0; i < kHostChunksMax + 1; ++i)
+        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->host_ev[i], cudaEventDisableTiming));
+    for (int i = 0; i < kHostChunksMax; ++i) {
+        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->in_ev[i], cudaEventDisableTiming));
+        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->out_ev[i], cudaEventDisableTiming));
+    }
+    for (int i = 0; i < 2; ++i) {
+        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->a_in[i], cudaEventDisableTiming));
+        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->a_xfree[i], cudaEventDisableTiming));
+        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->a_zready[i], cudaEventDisableTiming));
+        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->a_zfree[i], cudaEventDisableTiming));
+    }
+    c->s_in = in;
+    c->s_out = out;
+    return TPMLP_OK;
+}
+
 // The host-buffer pipeline of tpmlp_forward_host (layer = false) and
 // tpmlp_block_forward_host (layer = true: LayerNorm in front, the residual added by the second
 // GEMM's epilogue). The planned row chunks of X are copied into a device staging buffer on one
@@ -752,16 +783,7 @@ int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, vo
     }
     if ((rc = ensure_y(c, M))) return rc;
     if (layer && (rc = ensure_xn(c, M))) return rc;
-    if (!c->s_in) {
-        TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking));
-        TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking));
-        for (int i = 0; i < kHostChunksMax + 1; ++i)
-            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->host_ev[i], cudaEventDisableTiming));
-        for (int i = 0; i < kHostChunksMax; ++i) {
-            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->in_ev[i], cudaEventDisableTiming));
-            TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->out_ev[i], cudaEventDisableTiming));
-        }
-    }
+    if ((rc = ensure_copy_streams(c))) return rc;
     if (M != c->plan_M) {
         c->plan_n = plan_host_chunks(c, M, c->plan_rows);
         c->plan_M = M;
@@ -802,6 +824,76 @@ int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, vo
     TPMLP_CUDA(c, cudaEventRecord(c->host_ev[1], c->s_out));
     TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->host_ev[1], 0));
     TPMLP_CUDA(c, cudaStreamSynchronize(s));
+    return TPMLP_OK;
+}
+
+// tpmlp_forward_host_async (layer = false) and tpmlp_block_forward_host_async (layer = true):
+// the whole call as one chunk in staging slot (calls made so far) mod 2. Its input copy on the
+// context's input stream waits only until the kernels of the call before last have read the
+// slot, and its output copy on the output stream only for this call's second GEMM, so that in
+// a run of calls the copies of one call overlap the kernels of its neighbours. Nothing here
+// waits on the host; tpmlp_host_wait does.
+int run_host_async(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void* Z_host,
+                   cudaStream_t s, bool layer) {
+    int rc = check_ctx(c);
+    if (rc) return rc;
+    if (layer && !c->ln_set) {
+        c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
+        return TPMLP_ERR_NOT_PACKED;
+    }
+    if ((rc = check_tokens(B, S))) return rc;
+    const int64_t M = B * S;
+    if (M == 0) return TPMLP_OK;
+    if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
+    if ((rc = ensure_copy_streams(c))) return rc;
+    const size_t xbytes = static_cast<size_t>(M) * c->H * 2;
+    const size_t zbytes = static_cast<size_t>(M) * c->H * z_elem_bytes(c);
+    if (M > c->async_rows) {
+        TPMLP_CUDA(c, cudaDeviceSynchronize());  // earlier calls may still use the slots
+        for (int i = 0; i < 2; ++i) {
+            cudaFree(c->Xa[i]);
+            cudaFree(c->Za[i]);
+            c->Xa[i] = c->Za[i] = nullptr;
+            c->a_used[i] = false;
+        }
+        c->async_rows = 0;
+        for (int i = 0; i < 2; ++i) {
+            TPMLP_CUDA(c, cudaMalloc(&c->Xa[i], xbytes));
+            TPMLP_CUDA(c, cudaMalloc(&c->Za[i], zbytes));
+        }
+        c->async_rows = M;
+    }
+    if ((rc = ensure_y(c, M))) return rc;
+    if (layer && (rc = ensure_xn(c, M))) return rc;
+    const int slot = static_cast<int>(c->a_calls & 1u);
+    void* const xs = c->Xa[slot];
+    void* const zs = c->Za[slot];
+    // in: not before the kernels of the slot's previous call have read it
+    if (c->a_used[slot]) TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_in, c->a_xfree[slot], 0));
+    TPMLP_CUDA(c, cudaMemcpyAsync(xs, X_host, xbytes, cudaMemcpyHostToDevice, c->s_in));
+    TPMLP_CUDA(c, cudaEventRecord(c->a_in[slot], c->s_in));
+    // kernels: after the input has arrived and the slot's previous output has been copied out
+    TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->a_in[slot], 0));
+    if (c->a_used[slot]) TPMLP_CUDA(c, cudaStreamWaitEvent(s, c->a_zfree[slot], 0));
+    c->a_used[slot] = true;  // from here on the slot's events belong to this call
+    ++c->a_calls;
+    if (layer) {
+        // the residual add of the second GEMM reads the input slot too
+        if ((rc = run_layernorm(c, xs, M, c->Xn, s)) || (rc = run_gemm1(c, c->Xn, M, c->Y, s)) ||
+            (rc = run_gemm2(c, c->Y, M, zs, s, xs)))
+            return rc;
+        TPMLP_CUDA(c, cudaEventRecord(c->a_xfree[slot], s));
+    } else {
+        if ((rc = run_gemm1(c, xs, M, c->Y, s))) return rc;
+        TPMLP_CUDA(c, cudaEventRecord(c->a_xfree[slot], s));
+        if ((rc = run_gemm2(c, c->Y, M, zs, s))) return rc;
+    }
+    TPMLP_CUDA(c, cudaEventRecord(c->a_zready[slot], s));
+    // out: as soon as this call's second GEMM is done
+    TPMLP_CUDA(c, cudaStreamWaitEvent(c->s_out, c->a_zready[slot], 0));
+    TPMLP_CUDA(c, cudaMemcpyAsync(Z_host, zs, zbytes, cudaMemcpyDeviceToHost, c->s_out));
+    TPMLP_CUDA(c, cudaEventRecord(c->a_zfree[slot], c->s_out));
     return TPMLP_OK;
 }
 
@@ -1114,6 +1206,21 @@ int tpmlp_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, v
     return run_host_pipeline(c, X_host, B, S, Z_host, static_cast<cudaStream_t>(stream), false);
 }
 
+int tpmlp_forward_host_async(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S,
+                             void* Z_host, void* stream) {
+    return run_host_async(c, X_host, B, S, Z_host, static_cast<cudaStream_t>(stream), false);
+}
+
+int tpmlp_host_wait(tpmlp_ctx* c) {
+    if (!c) return TPMLP_ERR_INVALID_ARG;
+    if (int rc = check_device(c)) return rc;
+    if (!c->s_in) return TPMLP_OK;  // no host-buffer call yet
+    // every output copy waits for its call's kernels, which wait for its input copy
+    TPMLP_CUDA(c, cudaStreamSynchronize(c->s_out));
+    TPMLP_CUDA(c, cudaStreamSynchronize(c->s_in));
+    return TPMLP_OK;
+}
+
 int tpmlp_set_layernorm(tpmlp_ctx* c, const void* gamma, const void* beta, float eps,
                         void* stream) {
     // the block's input, or a column-parallel layer's input (LayerNorm before Q/K/V)
@@ -1202,6 +1309,11 @@ int tpmlp_block_forward_marked(tpmlp_ctx* c, const void* X, int64_t B, int64_t S
 int tpmlp_block_forward_host(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S,
                              void* Z_host, void* stream) {
     return run_host_pipeline(c, X_host, B, S, Z_host, static_cast<cudaStream_t>(stream), true);
+}
+
+int tpmlp_block_forward_host_async(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S,
+                                   void* Z_host, void* stream) {
+    return run_host_async(c, X_host, B, S, Z_host, static_cast<cudaStream_t>(stream), true);
 }
 
 int tpmlp_gemm2_residual(tpmlp_ctx* c, const void* Y, int64_t M, void* Z, const void* R,
@@ -1513,6 +1625,12 @@ void tpmlp_destroy(tpmlp_ctx* c) {
     cudaFree(c->Y);
     cudaFree(c->Xs);
     cudaFree(c->Zs);
+    for (int i = 0; i < 2; ++i) {
+        cudaFree(c->Xa[i]);
+        cudaFree(c->Za[i]);
+        for (cudaEvent_t e : {c->a_in[i], c->a_xfree[i], c->a_zready[i], c->a_zfree[i]})
+            if (e) cudaEventDestroy(e);
+    }
     for (cudaEvent_t e : c->host_ev) if (e) cudaEventDestroy(e);
     for (cudaEvent_t e : c->in_ev) if (e) cudaEventDestroy(e);
     for (cudaEvent_t e : c->out_ev) if (e) cudaEventDestroy(e);

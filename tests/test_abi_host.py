@@ -72,6 +72,9 @@ def test_null_context_everywhere(lib):
     assert lib.tpmlp_pack_shards(None, 16, 16, 16, 16, None) == INV
     assert lib.tpmlp_forward(None, 16, 1, 1, 16, None) == INV
     assert lib.tpmlp_forward_host(None, 16, 1, 1, 16, None) == INV
+    assert lib.tpmlp_forward_host_async(None, 16, 1, 1, 16, None) == INV
+    assert lib.tpmlp_block_forward_host_async(None, 16, 1, 1, 16, None) == INV
+    assert lib.tpmlp_host_wait(None) == INV
     assert lib.tpmlp_gemm1(None, 16, 1, 16, None) == INV
     assert lib.tpmlp_gemm2(None, 16, 1, 16, None) == INV
     assert lib.tpmlp_reserve(None, 1) == INV
@@ -118,6 +121,8 @@ BLOCK_CALLS = {
     "tpmlp_reserve": (1024,),
     "tpmlp_forward": (16, 1, 64, 16, None),
     "tpmlp_forward_host": (16, 1, 64, 16, None),
+    "tpmlp_forward_host_async": (16, 1, 64, 16, None),
+    "tpmlp_host_wait": (),
     "tpmlp_forward_noalloc": (16, 1, 64, 16, None),
     "tpmlp_forward_marked": (16, 1, 64, 16, 16, None),
     "tpmlp_block_forward_marked": (16, 1, 64, 16, 16, 16, None),
@@ -128,6 +133,7 @@ BLOCK_CALLS = {
     "tpmlp_layernorm": (16, 64, 16, None),
     "tpmlp_block_forward": (16, 1, 64, 16, None),
     "tpmlp_block_forward_host": (16, 1, 64, 16, None),
+    "tpmlp_block_forward_host_async": (16, 1, 64, 16, None),
     "tpmlp_forward_train": (16, 1, 64, 16, 16, 16, None),
     "tpmlp_backward": (16, 16, 16, 16, 16, 16, 1, 64, 16, 16, 16, 16, 16, None),
     "tpmlp_get_status": (None, None),
@@ -180,6 +186,8 @@ def test_every_entry_point_checks_the_current_device(hooks, kind, flags, calls):
             assert call(hooks, "tpmlp_forward", ctx, (16, 0, 64, 16, None)) == tp.TPMLP_OK
             assert call(hooks, "tpmlp_forward_noalloc", ctx, (16, 0, 64, 16, None)) == tp.TPMLP_OK
             assert call(hooks, "tpmlp_gemm1", ctx, (16, 0, 16, None)) == tp.TPMLP_OK
+            assert call(hooks, "tpmlp_forward_host_async", ctx, (16, 0, 64, 16, None)) == tp.TPMLP_OK
+            assert call(hooks, "tpmlp_host_wait", ctx, ()) == tp.TPMLP_OK  # nothing queued
         if kind != 0:
             assert call(hooks, "tpmlp_linear_forward", ctx, (16, 0, 16, None)) == tp.TPMLP_OK
         assert hooks.tpmlp_launch_count(ctx) == 0

@@ -58,6 +58,10 @@ def test_bench_line_carries_the_contract(lib, variant):
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == "TFLOP/s"
     assert e2e["h2d_bytes_per_step"] == w.M * w.H * 2 == e2e["d2h_bytes_per_step"]
+    assert "tpmlp_host_wait" in e2e["api"] and e2e["steps"] >= 3
+    sync = e2e["synchronous_calls"]
+    assert sync["value"] > 0 and abs(sync["value"] * sync["ms_per_step"] -
+                                     e2e["value"] * e2e["ms_per_step"]) <= 1e-6 * e2e["value"] * e2e["ms_per_step"]
     assert line["gpu_launches"] == 2 * steps  # two GEMM launches per forward
     clk = line["clocks"]
     assert clk is not None and clk["sm_mhz"] > 0 and clk["sm_max_mhz"] >= clk["sm_mhz"]
