@@ -90,6 +90,8 @@ struct tpmlp_ctx {
     uint32_t sk_epoch = 0;
 
     tpmlp::DeviceRates rates{};  // the planners' rates (device_rates, or tpmlp_set_device_rates)
+    // row group of the tall units' sweep, for the last (512-row blocks, column blocks, pairs)
+    int tall_group = 8, tall_group_m = -1, tall_group_n = -1, tall_group_pairs = -1;
 
     int* status = nullptr;  // device status word
     int64_t launches = 0;
@@ -374,9 +376,20 @@ int launch_gemm2_pair(tpmlp_ctx* c, const CUtensorMap& a_map, const CUtensorMap&
             resident = max_resident_pairs(c, kern, smem);
             slot.store(resident, std::memory_order_relaxed);
         }
-        const tpmlp::TallPlan tall = tpmlp::plan_tall_units(args.M, args.n_blocks, args.group_m, resident);
+        // the row group of the units' sweep: the one whose rounds read the least from DRAM
+        const int tall_m = args.M / (2 * tpmlp::kPairBM);
+        if (tall_m != c->tall_group_m || args.n_blocks != c->tall_group_n ||
+            resident != c->tall_group_pairs) {
+            c->tall_group = tpmlp::pick_tall_group(tall_m, args.n_blocks, resident);
+            c->tall_group_m = tall_m;
+            c->tall_group_n = args.n_blocks;
+            c->tall_group_pairs = resident;
+        }
+        const int group = c->tall_group;
+        const tpmlp::TallPlan tall = tpmlp::plan_tall_units(args.M, args.n_blocks, group, resident);
         if (tall.tall_units > 0) {
             GemmArgs run = args;
+            run.group_m = group;
             run.tall_units = tall.tall_units;
             run.tall_m_blocks = tall.tall_m_blocks;
             run.tall_rest = tall.tall_rest;

@@ -41,6 +41,7 @@
 #pragma once
 
 #include <cstdint>
+#include <vector>
 
 #if defined(__CUDACC__)
 #define TPMLP_HD __host__ __device__ __forceinline__
@@ -276,6 +277,61 @@ inline TallPlan plan_tall_units(int M, int n_blocks, int group_m, int pairs) {
     p.rows = m_hi >= m_lo ? m_hi - m_lo + 1 : 0;
     p.cols = n_cnt;
     return p;
+}
+
+// DRAM reads of a launch's tall units under a round model: each round of `pairs` units (and
+// then the remaining units, whose halves run as tiles, as one more round) loads the union of
+// its units' 512-row blocks of A and 256-column panels of B once, and L2 keeps nothing from
+// one round to the next. Counted in B panels: a 512-row block of A is two of them. At 7b
+// (16 x 16 units on 76 pairs) it gives the second GEMM's DRAM reads that ncu measured for
+// row groups of 1, 2, 4 and 8, to the MB (0.856, 0.889, 0.856 and 0.931 GB).
+inline long long tall_round_panels(int group_m, int tall_m_blocks, int n_blocks, int pairs) {
+    const int T = tall_m_blocks * n_blocks;
+    if (pairs <= 0 || T <= 0) return 0;
+    const int units = T / pairs * pairs;
+    std::vector<int> m_seen(tall_m_blocks, -1), n_seen(n_blocks, -1);
+    long long total = 0;
+    int round = -1, rows = 0, cols = 0;
+    for (int u = 0; u < T; ++u) {
+        const int r = u < units ? u / pairs : units / pairs;
+        if (r != round) {
+            total += 2LL * rows + cols;
+            rows = cols = 0;
+            round = r;
+        }
+        int m, n;
+        decode_tile_mn(group_m, tall_m_blocks, n_blocks, u, m, n);
+        if (m_seen[m] != r) {
+            m_seen[m] = r;
+            ++rows;
+        }
+        if (n_seen[n] != r) {
+            n_seen[n] = r;
+            ++cols;
+        }
+    }
+    return total + 2LL * rows + cols;
+}
+
+// Row groups the tall units may sweep by (whole 512-row blocks), in order of preference.
+constexpr int kTallGroups[5] = {8, 4, 16, 2, 1};
+
+// The row group whose rounds read the least under tall_round_panels (the first of kTallGroups
+// on a tie). Interleaved A/B with groups of 8, 4, 2 and 1 (bit-identical outputs): 7b 577.5,
+// 575.1, 577.8 and 573.1 us per second GEMM, GPT-3 2596, 2610, 2633 and 2649 us, M = 16384
+// at H = 4096 1174, 1171, 1177 and 1170 us, each within 1 % of the group this picks.
+inline int pick_tall_group(int tall_m_blocks, int n_blocks, int pairs) {
+    int best = kTallGroups[0];
+    long long best_bytes = -1;
+    for (int g : kTallGroups) {
+        if (g > tall_m_blocks && g != kTallGroups[0]) continue;  // same order as the whole
+        const long long b = tall_round_panels(g, tall_m_blocks, n_blocks, pairs);
+        if (best_bytes < 0 || b < best_bytes) {
+            best = g;
+            best_bytes = b;
+        }
+    }
+    return best;
 }
 
 // ---------------------------------------------------------------- device rates

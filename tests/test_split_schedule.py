@@ -53,6 +53,12 @@ int shim_tall(int M, int n_blocks, int group_m, int pairs, int* out, int* info) 
     info[0] = p.tiles; info[1] = p.rows; info[2] = p.cols; info[3] = p.tail_first; info[4] = p.tall_rest;
     return p.tall_units;
 }
+long long shim_tall_round_panels(int group_m, int tall_m_blocks, int n_blocks, int pairs) {
+    return tpmlp::tall_round_panels(group_m, tall_m_blocks, n_blocks, pairs);
+}
+int shim_pick_tall_group(int tall_m_blocks, int n_blocks, int pairs) {
+    return tpmlp::pick_tall_group(tall_m_blocks, n_blocks, pairs);
+}
 void shim_plan(int num_tiles, int pairs, int kb_tile, int m_blocks, int n_blocks, int group_m,
                int* out) {
     // the rule of a GB300 context: 152 SMs (76 pairs) at 2.07 GHz, HBM 3.996 GHz x 8192 bits
@@ -79,6 +85,9 @@ def sched(tmp_path_factory):
     lib.shim_pair_of.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_longlong]
     lib.shim_plan.argtypes = [ctypes.c_int] * 6 + [ip]
     lib.shim_tall.argtypes = [ctypes.c_int] * 4 + [ip, ip]
+    lib.shim_tall_round_panels.argtypes = [ctypes.c_int] * 4
+    lib.shim_tall_round_panels.restype = ctypes.c_longlong
+    lib.shim_pick_tall_group.argtypes = [ctypes.c_int] * 3
     return lib
 
 
@@ -237,17 +246,18 @@ def test_narrow_launch_schedule(sched, T, kb):
         assert len(us) == 1 and us[0][0] == p // parts
 
 
+@pytest.mark.parametrize("group", [8, 1, 2, 4, 16])
 @pytest.mark.parametrize("M,nb,P", [(8192, 16, 76), (4096, 48, 76), (16384, 16, 76), (5000, 16, 76),
                                     (4700, 16, 76), (2560, 16, 76), (4097, 16, 74), (1000, 16, 76),
                                     (12345, 12, 75), (768, 48, 76), (3584, 48, 76), (6144, 10, 76)])
-def test_tall_units_cover_every_tile_once(sched, M, nb, P):
+def test_tall_units_cover_every_tile_once(sched, M, nb, P, group):
     """Tall units (two 256-row halves each, whole 512-row blocks only) and the tiles after
     them compute every 256 x 256 output tile exactly once; tall units come in whole waves of
     P, and only when they take no more rounds than ordinary tiles alone."""
     m_blocks = (M + 255) // 256
     out = (ctypes.c_int * (m_blocks * nb))()
     info = (ctypes.c_int * 5)()
-    tall = sched.shim_tall(M, nb, 8, P, out, info)
+    tall = sched.shim_tall(M, nb, group, P, out, info)
     T = M // 512 * nb
     if tall == 0:
         assert T < P or 2 * (T // P) + -(-(m_blocks * nb - 2 * (T // P) * P) // P) > -(-(m_blocks * nb) // P)
@@ -278,3 +288,44 @@ def test_tall_plans_of_the_workloads(sched):
     out = (ctypes.c_int * (24 * 10))()
     assert sched.shim_tall(6144, 10, 8, 76, out, info) == 76
     assert info[0] == 88 and info[3] == 76 and info[2] == 2
+
+
+def round_union_panels(group, tm, nb, P):
+    """The round model by brute force: the tiles' (row block, column block) in launch order
+    (groups of `group` row blocks, each swept column by column, every second group in
+    reverse), cut into rounds of P (the rest one more round); a round costs 2 per distinct
+    512-row block and 1 per distinct 256-column panel."""
+    order = []
+    for g0 in range(0, tm, group):
+        rows = list(range(g0, min(g0 + group, tm)))
+        cols = list(range(nb)) if (g0 // group) % 2 == 0 else list(range(nb - 1, -1, -1))
+        order += [(m, n) for n in cols for m in rows]
+    units = len(order) // P * P
+    rounds = [order[i:i + P] for i in range(0, units, P)] + ([order[units:]] if units < len(order) else [])
+    return sum(2 * len({m for m, _ in r}) + len({n for _, n in r}) for r in rounds)
+
+
+@pytest.mark.parametrize("tm,nb,P", [(16, 16, 76), (8, 48, 76), (32, 16, 76), (9, 16, 76),
+                                     (13, 12, 75), (24, 10, 76), (5, 7, 74)])
+def test_tall_round_model(sched, tm, nb, P):
+    """The library's round model equals the brute-force union count for every row group."""
+    for g in (1, 2, 4, 8, 16):
+        assert sched.shim_tall_round_panels(g, tm, nb, P) == round_union_panels(g, tm, nb, P), g
+
+
+def test_tall_group_choice_of_the_workloads(sched):
+    """The model's DRAM reads at 7b match ncu's (second GEMM, 512-row block = 2 panels of
+    16384 x 256 bf16 = 8.39 MB each): groups of 1, 2, 4, 8 read 0.856, 0.889, 0.856 and
+    0.931 GB. The choice: 4 at 7b (tied with 1; 4 comes first), 8 at GPT-3 (M = 4096,
+    48 column blocks), 1 for M = 16384 at H = 4096; every pick is the minimum."""
+    panel = 16384 * 256 * 2
+    for g, gb in ((1, 0.856), (2, 0.889), (4, 0.856), (8, 0.931)):
+        assert abs(sched.shim_tall_round_panels(g, 16, 16, 76) * panel / 1e9 - gb) < 0.0015, g
+    assert sched.shim_pick_tall_group(16, 16, 76) == 4
+    assert sched.shim_pick_tall_group(8, 48, 76) == 8
+    assert sched.shim_pick_tall_group(32, 16, 76) == 1
+    for tm, nb, P in ((16, 16, 76), (8, 48, 76), (32, 16, 76), (9, 16, 76), (3, 40, 76)):
+        best = sched.shim_pick_tall_group(tm, nb, P)
+        assert best in (1, 2, 4, 8, 16)
+        costs = [sched.shim_tall_round_panels(g, tm, nb, P) for g in (1, 2, 4, 8, 16)]
+        assert sched.shim_tall_round_panels(best, tm, nb, P) == min(costs)
