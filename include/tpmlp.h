@@ -81,10 +81,13 @@ typedef enum {
                                      leave CTA pairs idle, or a launch has fewer tiles than
                                      pairs (a small batch), the reductions of those tiles are
                                      divided among several pairs and their fp32 partial sums
-                                     added in a fixed order: results are deterministic, but their
-                                     last bits then depend on the token count M. With this flag
-                                     every tile is summed in one pass in reduction order, so the
-                                     pair and single-SM kernels, and any M, give identical bits */
+                                     added in a fixed order; and in deep second GEMMs every
+                                     second round of 512 x 256 units sums its reduction blocks
+                                     last to first (the blocks still in L2 first). Results are
+                                     deterministic, but their last bits then depend on the token
+                                     count M. With this flag every tile is summed in one pass in
+                                     reduction order, so the pair and single-SM kernels, and any
+                                     M, give identical bits */
 
 /*
  * Create a context for one block shape on the current CUDA device.

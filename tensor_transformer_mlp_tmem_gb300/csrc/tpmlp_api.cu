@@ -390,6 +390,8 @@ int launch_gemm2_pair(tpmlp_ctx* c, const CUtensorMap& a_map, const CUtensorMap&
         if (tall.tall_units > 0) {
             GemmArgs run = args;
             run.group_m = group;
+            // every second round sweeps the reduction backwards, except in the fixed order
+            run.tall_serpentine = (c->flags & TPMLP_FLAG_FIXED_ORDER) ? 0 : 1;
             run.tall_units = tall.tall_units;
             run.tall_m_blocks = tall.tall_m_blocks;
             run.tall_rest = tall.tall_rest;

@@ -129,6 +129,10 @@ struct GemmArgs {
     int tall_units;        // 0: no tall units
     int tall_m_blocks;
     int tall_rest;
+    // 1: a unit of an odd round (unit / pairs odd) sweeps its reduction blocks from the last
+    // to the first, so that it starts on the operand blocks the round before it loaded last,
+    // which are still in L2. Its sums then run in the opposite order (last bits may differ).
+    int tall_serpentine;
 };
 
 constexpr int kSkSlotFloats = 128 * 256;  // one CTA's half of a 256 x 256 accumulator

@@ -152,7 +152,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                     const int m0 = tm * 2 * kPairBM + static_cast<int>(rank) * 128;
                     const int nb = n_blk * kPairBN + static_cast<int>(rank) * 128;
                     constexpr uint32_t bytes = 2 * L::kStageBytes;  // both CTAs: two A boxes, B
-                    for (int kb = 0; kb < args.kb_tile; ++kb) {
+                    const bool backwards = args.tall_serpentine && ((u / num_pairs) & 1);
+                    for (int i = 0; i < args.kb_tile; ++i) {
+                        const int kb = backwards ? args.kb_tile - 1 - i : i;
                         if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status,
                                             kCode | kSiteProducer)) {
                             ok = false;

@@ -122,6 +122,40 @@ def test_tall_remainder_keeps_whole_waves_and_splits_its_last(lib):
     assert_close(to_f64(Z.view(M, h))[rows], ref, what="tall remainder with split tail vs oracle")
 
 
+def test_tall_serpentine_rounds(lib):
+    """M = 8192 at H = 4096: 228 tall units in three rounds of 76. By default the second
+    round sums its reduction blocks last to first; with fp32 Z those units differ from the
+    fixed order in the last bits and agree to fp32 accuracy, the first and third rounds'
+    units equal it bit for bit, and repeated launches give the same bits."""
+    M = 8192
+    d = synth.make_inputs(H, F, M, 406)
+    dd = inputs_on_device(d)
+    with tp.TPMLP(H, F, K_SHARDS, fixed_order=True) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        Y = mlp.gemm1(dd["X"])
+    outs = {}
+    for fixed in (False, True):
+        with tp.TPMLP(H, F, K_SHARDS, z_fp32=True, fixed_order=fixed) as mlp:
+            mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+            outs[fixed] = (mlp.gemm2(Y), mlp.gemm2(Y))
+            torch.cuda.synchronize()
+            assert mlp.status()[0] == tp.TPMLP_OK
+    serp, fixed = outs[False][0], outs[True][0]
+    assert torch.equal(outs[False][0], outs[False][1])  # deterministic
+    # which 512 x 256 units ran in the second round: same row group and order as the library
+    # picks (pick_tall_group: 4 row blocks of 512 at this shape, 16 x 16 units)
+    group, tm, nb, P = 4, M // 512, H // 256, 76
+    order = []
+    for g0 in range(0, tm, group):
+        cols = list(range(nb)) if (g0 // group) % 2 == 0 else list(range(nb - 1, -1, -1))
+        order += [(m, n) for n in cols for m in range(g0, min(g0 + group, tm))]
+    diff = (serp != fixed).view(tm, 512, nb, 256).any(dim=3).any(dim=1).cpu()
+    for u, (m, n) in enumerate(order[:3 * P]):
+        assert bool(diff[m, n]) == (u // P == 1), (u, m, n)
+    rel = (torch.linalg.norm(serp - fixed) / torch.linalg.norm(fixed)).item()
+    assert rel < 1e-5, rel
+
+
 def test_tall_units_in_a_cuda_graph(lib):
     """M = 2560: 76 tall units and 8 tiles. Captured launches never split, so every replay on
     new inputs equals the eager forward with TPMLP_FLAG_FIXED_ORDER (also tall units, no
