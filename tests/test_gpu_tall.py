@@ -187,22 +187,27 @@ def test_tall_units_in_a_cuda_graph(lib):
         assert mlp.status()[0] == tp.TPMLP_OK
 
 
-def test_tall_backward_dx_equals_the_single_sm_kernel(lib):
+@pytest.mark.parametrize("M", [2560, 8192])
+def test_tall_backward_dx_equals_the_single_sm_kernel(lib, M):
     """The backward's dX = sum_i dA_i W1_i^T (128 reduction blocks at F = 8192) runs tall
-    units at M = 2560; with TPMLP_FLAG_FIXED_ORDER it equals the single-SM kernel's dX bit for
-    bit, and so do the weight and bias gradients."""
-    M = 2560
+    units, at M = 2560 in one round and at M = 8192 in three. With TPMLP_FLAG_FIXED_ORDER dX
+    and the weight and bias gradients equal the single-SM kernel's bit for bit; by default
+    (split tails, a backward second round) they agree with them closely."""
     d = synth.make_inputs(H, F, M, 406)
     dd = inputs_on_device(d)
     X = dd["X"].view(1, M, H)
     dZ = inputs_on_device({"dZ": synth.normal_bf16(406, 60, (M, H), 1.0)})["dZ"].view(1, M, H)
     grads = {}
-    for single in (False, True):
-        with tp.TPMLP(H, F, K_SHARDS, fixed_order=True, single_sm=single) as mlp:
+    for single, fixed in ((False, True), (True, True), (False, False)):
+        with tp.TPMLP(H, F, K_SHARDS, fixed_order=fixed, single_sm=single) as mlp:
             mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
             _, Ys, As = mlp.forward_train(X)
-            grads[single] = mlp.backward(dZ, X, Ys, As, dd["W1"], dd["W2"])
+            grads[single, fixed] = mlp.backward(dZ, X, Ys, As, dd["W1"], dd["W2"])
             torch.cuda.synchronize()
             assert mlp.status()[0] == tp.TPMLP_OK
-    for a, b in zip(grads[False], grads[True]):
+    for a, b in zip(grads[False, True], grads[True, True]):
         assert torch.equal(a, b)
+    for a, b in zip(grads[False, False], grads[True, True]):
+        a, b = a.float(), b.float()
+        rel = (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item()
+        assert rel < 5e-3, rel  # dX is bf16: its rounding may flip; the fp32 gradients far closer
