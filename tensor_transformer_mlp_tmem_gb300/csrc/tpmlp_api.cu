@@ -21,6 +21,12 @@
 #include "tpmlp_pack.cuh"
 #include "tpmlp_plan.h"
 
+// Row chunks of tpmlp_forward_host's pipeline at most (sizes the context's event arrays).
+#ifndef TPMLP_HOST_CHUNKS_MAX
+#define TPMLP_HOST_CHUNKS_MAX 4
+#endif
+static_assert(TPMLP_HOST_CHUNKS_MAX >= 1 && TPMLP_HOST_CHUNKS_MAX <= 16, "host chunk limit");
+
 struct tpmlp_ctx {
     int device = -1;
     int num_sms = 0;
@@ -47,11 +53,12 @@ struct tpmlp_ctx {
     void* Zs = nullptr;
     int64_t stage_rows = 0;
     cudaStream_t s_in = nullptr, s_out = nullptr;  // its copy streams (created on first use)
-    cudaEvent_t host_ev[5] = {}, in_ev[4] = {}, out_ev[4] = {};
+    cudaEvent_t host_ev[TPMLP_HOST_CHUNKS_MAX + 1] = {}, in_ev[TPMLP_HOST_CHUNKS_MAX] = {},
+                out_ev[TPMLP_HOST_CHUNKS_MAX] = {};
     // row chunks of the last tpmlp_forward_host call (re-planned when M changes)
     int64_t plan_M = -1;
     int plan_n = 0;
-    int64_t plan_rows[4] = {};
+    int64_t plan_rows[TPMLP_HOST_CHUNKS_MAX] = {};
     // tpmlp_forward_host_async: two staging slots used in turn, so that a call's copies in and
     // out overlap the kernels of the calls before and after it
     void* Xa[2] = {};
@@ -125,9 +132,6 @@ struct tpmlp_ctx {
 
 namespace {
 
-#ifndef TPMLP_HOST_CHUNKS_MAX
-#define TPMLP_HOST_CHUNKS_MAX 4
-#endif
 constexpr int kHostChunksMax = TPMLP_HOST_CHUNKS_MAX;  // row chunks of tpmlp_forward_host's pipeline
 
 using tpmlp::GemmArgs;
@@ -745,26 +749,25 @@ int run_layernorm(tpmlp_ctx* c, const void* X, int64_t M, void* Xn, cudaStream_t
     return TPMLP_OK;
 }
 
-// The copy streams and events of the host-buffer entry points (created on first use).
+// The copy streams and events of the host-buffer entry points, created on first use. After a
+// failure the next call creates only what is still missing; tpmlp_destroy releases them all.
 int ensure_copy_streams(tpmlp_ctx* c) {
-    if (c->s_in) return TPMLP_OK;
-    cudaStream_t in = nullptr, out = nullptr;
-    TPMLP_CUDA(c, cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking));
-    TPMLP_CUDA(c, cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking));
-    for (int i = 0; i < kHostChunksMax + 1; ++i)
-        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->host_ev[i], cudaEventDisableTiming));
-    for (int i = 0; i < kHostChunksMax; ++i) {
-        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->in_ev[i], cudaEventDisableTiming));
-        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->out_ev[i], cudaEventDisableTiming));
-    }
-    for (int i = 0; i < 2; ++i) {
-        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->a_in[i], cudaEventDisableTiming));
-        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->a_xfree[i], cudaEventDisableTiming));
-        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->a_zready[i], cudaEventDisableTiming));
-        TPMLP_CUDA(c, cudaEventCreateWithFlags(&c->a_zfree[i], cudaEventDisableTiming));
-    }
-    c->s_in = in;
-    c->s_out = out;
+    if (c->s_in && c->s_out) return TPMLP_OK;
+    auto event = [c](cudaEvent_t& e) -> int {
+        if (!e) TPMLP_CUDA(c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        return TPMLP_OK;
+    };
+    int rc;
+    for (cudaEvent_t& e : c->host_ev)
+        if ((rc = event(e))) return rc;
+    for (int i = 0; i < kHostChunksMax; ++i)
+        if ((rc = event(c->in_ev[i])) || (rc = event(c->out_ev[i]))) return rc;
+    for (int i = 0; i < 2; ++i)
+        if ((rc = event(c->a_in[i])) || (rc = event(c->a_xfree[i])) ||
+            (rc = event(c->a_zready[i])) || (rc = event(c->a_zfree[i])))
+            return rc;
+    if (!c->s_in) TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking));
+    if (!c->s_out) TPMLP_CUDA(c, cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking));
     return TPMLP_OK;
 }
 
@@ -1229,7 +1232,7 @@ int tpmlp_forward_host_async(tpmlp_ctx* c, const void* X_host, int64_t B, int64_
 int tpmlp_host_wait(tpmlp_ctx* c) {
     if (!c) return TPMLP_ERR_INVALID_ARG;
     if (int rc = check_device(c)) return rc;
-    if (!c->s_in) return TPMLP_OK;  // no host-buffer call yet
+    if (!c->s_in || !c->s_out) return TPMLP_OK;  // no host-buffer call has queued work
     // every output copy waits for its call's kernels, which wait for its input copy
     TPMLP_CUDA(c, cudaStreamSynchronize(c->s_out));
     TPMLP_CUDA(c, cudaStreamSynchronize(c->s_in));
