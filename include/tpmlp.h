@@ -187,7 +187,8 @@ TPMLP_API int tpmlp_forward_marked(tpmlp_ctx *ctx, const void *X, int64_t B, int
  * planned once per token count under a pipeline model of the copies and of the GEMMs' rounds
  * of tiles (small end chunks, tile counts that fill whole rounds). Page-locked host memory
  * gives asynchronous, full-speed copies; pageable memory works but is slower.
- * Staging buffers are owned by the context and grow on demand.
+ * Staging buffers are owned by the context and grow on demand. Not for stream capture: while
+ * `stream` is capturing it returns INVALID_ARG and queues nothing.
  * Errors: as tpmlp_forward.
  */
 TPMLP_API int tpmlp_forward_host(tpmlp_ctx *ctx, const void *X_host, int64_t B, int64_t S, void *Z_host,
@@ -209,7 +210,8 @@ TPMLP_API int tpmlp_forward_host(tpmlp_ctx *ctx, const void *X_host, int64_t B, 
  *                   same time must not overlap. Page-locked memory gives the overlap;
  *                   pageable memory works but each copy then blocks the host.
  * A larger token count than any earlier async call's waits for the device once (the slots
- * grow). Errors: as tpmlp_forward_host; a returned error leaves the calls queued before it
+ * grow). Not for stream capture (INVALID_ARG, nothing queued).
+ * Errors: as tpmlp_forward_host; a returned error leaves the calls queued before it
  * intact (tpmlp_host_wait still waits for them).
  */
 TPMLP_API int tpmlp_forward_host_async(tpmlp_ctx *ctx, const void *X_host, int64_t B, int64_t S,

@@ -776,10 +776,18 @@ int ensure_copy_streams(tpmlp_ctx* c) {
 // GEMM's epilogue). The planned row chunks of X are copied into a device staging buffer on one
 // copy stream, each chunk's kernels run on `s` once its rows have arrived, and each chunk of Z
 // is copied out on a second copy stream as soon as its second GEMM is done.
+// The host-buffer entry points queue work on the context's own copy streams, which a CUDA
+// graph capture of `s` cannot take in; they refuse to run under capture.
+int refuse_capture(tpmlp_ctx* c, cudaStream_t s) {
+    if (!capturing(s)) return TPMLP_OK;
+    c->last_error = "host-buffer entry points cannot run under stream capture";
+    return TPMLP_ERR_INVALID_ARG;
+}
+
 int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void* Z_host,
                       cudaStream_t s, bool layer) {
     int rc = check_ctx(c);
-    if (rc) return rc;
+    if (rc || (rc = refuse_capture(c, s))) return rc;
     if (layer && !c->ln_set) {
         c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
         return TPMLP_ERR_NOT_PACKED;
@@ -854,7 +862,7 @@ int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, vo
 int run_host_async(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void* Z_host,
                    cudaStream_t s, bool layer) {
     int rc = check_ctx(c);
-    if (rc) return rc;
+    if (rc || (rc = refuse_capture(c, s))) return rc;
     if (layer && !c->ln_set) {
         c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
         return TPMLP_ERR_NOT_PACKED;

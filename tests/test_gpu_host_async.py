@@ -105,3 +105,28 @@ def test_async_layer_and_in_place(lib):
         assert mlp.status()[0] == tp.TPMLP_OK
     assert torch.equal(Zd, za)
     assert torch.equal(Zd2, xi)
+
+
+def test_host_entry_points_refuse_stream_capture(lib):
+    """Under stream capture both host-buffer entry points return INVALID_ARG and queue
+    nothing (their copy streams cannot join the caller's graph)."""
+    M = 256
+    d = synth.make_inputs(H, F, M, 341)
+    dd = inputs_on_device(d)
+    Xh = host_bf16(d["X"])
+    Zh = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+    with tp.TPMLP(H, F, K_SHARDS) as mlp:
+        mlp.pack(dd["W1"], dd["b1"], dd["W2"], dd["b2"])
+        torch.cuda.synchronize()
+        for fn in (tp.tpmlp_forward_host_async, tp.tpmlp_forward_host):
+            g = torch.cuda.CUDAGraph()
+            with pytest.raises(tp.TpmlpError) as err:
+                with torch.cuda.graph(g):
+                    fn(mlp.ctx, Xh, 1, M, Zh)
+            assert err.value.status == tp.TPMLP_ERR_INVALID_ARG
+        # the context still works afterwards
+        tp.tpmlp_forward_host_async(mlp.ctx, Xh, 1, M, Zh)
+        tp.tpmlp_host_wait(mlp.ctx)
+        Zd = mlp(dd["X"].view(1, M, H)).view(M, H).cpu()
+        assert mlp.status()[0] == tp.TPMLP_OK
+    assert torch.equal(Zd, Zh)
