@@ -771,11 +771,6 @@ int ensure_copy_streams(tpmlp_ctx* c) {
     return TPMLP_OK;
 }
 
-// The host-buffer pipeline of tpmlp_forward_host (layer = false) and
-// tpmlp_block_forward_host (layer = true: LayerNorm in front, the residual added by the second
-// GEMM's epilogue). The planned row chunks of X are copied into a device staging buffer on one
-// copy stream, each chunk's kernels run on `s` once its rows have arrived, and each chunk of Z
-// is copied out on a second copy stream as soon as its second GEMM is done.
 // The host-buffer entry points queue work on the context's own copy streams, which a CUDA
 // graph capture of `s` cannot take in; they refuse to run under capture.
 int refuse_capture(tpmlp_ctx* c, cudaStream_t s) {
@@ -784,10 +779,15 @@ int refuse_capture(tpmlp_ctx* c, cudaStream_t s) {
     return TPMLP_ERR_INVALID_ARG;
 }
 
+// The host-buffer pipeline of tpmlp_forward_host (layer = false) and
+// tpmlp_block_forward_host (layer = true: LayerNorm in front, the residual added by the second
+// GEMM's epilogue). The planned row chunks of X are copied into a device staging buffer on one
+// copy stream, each chunk's kernels run on `s` once its rows have arrived, and each chunk of Z
+// is copied out on a second copy stream as soon as its second GEMM is done.
 int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void* Z_host,
                       cudaStream_t s, bool layer) {
     int rc = check_ctx(c);
-    if (rc || (rc = refuse_capture(c, s))) return rc;
+    if (rc) return rc;
     if (layer && !c->ln_set) {
         c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
         return TPMLP_ERR_NOT_PACKED;
@@ -795,6 +795,7 @@ int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, vo
     if ((rc = check_tokens(B, S))) return rc;
     const int64_t M = B * S;
     if (M == 0) return TPMLP_OK;
+    if ((rc = refuse_capture(c, s))) return rc;
     if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
     if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if (M > c->stage_rows) {
@@ -862,7 +863,7 @@ int run_host_pipeline(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, vo
 int run_host_async(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void* Z_host,
                    cudaStream_t s, bool layer) {
     int rc = check_ctx(c);
-    if (rc || (rc = refuse_capture(c, s))) return rc;
+    if (rc) return rc;
     if (layer && !c->ln_set) {
         c->last_error = "LayerNorm parameters not set (tpmlp_set_layernorm)";
         return TPMLP_ERR_NOT_PACKED;
@@ -870,6 +871,7 @@ int run_host_async(tpmlp_ctx* c, const void* X_host, int64_t B, int64_t S, void*
     if ((rc = check_tokens(B, S))) return rc;
     const int64_t M = B * S;
     if (M == 0) return TPMLP_OK;
+    if ((rc = refuse_capture(c, s))) return rc;
     if (!X_host || !Z_host) return TPMLP_ERR_INVALID_ARG;
     if (M > (int64_t(1) << 31) - 1) return TPMLP_ERR_UNSUPPORTED_SHAPE;
     if ((rc = ensure_copy_streams(c))) return rc;
