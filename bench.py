@@ -305,7 +305,7 @@ BURST_LIMIT_S = 1.0  # timed regions shorter than this run before the power cap 
 
 
 def peak_for(peaks: dict, timed_s: float):
-    """The dense bf16 peak a timed region of `timed_s` seconds is judged against: the burst
+    """The dense bf16 peak a timed region of `timed_s` seconds is compared with: the burst
     figure (cuBLAS best of 10) below BURST_LIMIT_S of continuous work, else the sustained one
     (a seconds-long cuBLAS loop under the power cap). Returns (peak, regime)."""
     burst = peaks["bf16_tflops"]

@@ -49,7 +49,7 @@ def test_bench_line_carries_the_contract(lib, variant):
     assert roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s"
     assert roof["peak"] > 0 and roof["achieved"] > 0
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) <= 1e-9
-    # a 20-step tiny run is far under a second of work: judged against the burst peak
+    # a 20-step tiny run is far under a second of work: compared with the burst peak
     assert line["peak_regime"] == roof["peak_regime"] == "burst"
     assert line["timed_region_s"] < bench.BURST_LIMIT_S
     assert roof["frac_burst"] == roof["frac"] and roof["frac_sustained"] >= roof["frac"]
